@@ -1,0 +1,189 @@
+"""ctypes binding of libattn.so: argument marshalling only.
+
+Every computation happens in the library's CUDA kernels; these wrappers only
+check tensor shapes/dtypes, allocate outputs (and the decode workspace) with
+torch, and pass raw device pointers plus the current CUDA stream.  If the
+library is missing they raise -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libattn.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "attn.h")
+
+_STATUS = {
+    0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_WORKSPACE",
+    4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_DEVICE",
+}
+PAGE_TOKENS = 16
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {_STATUS.get(status, status)}")
+        self.status = status
+
+
+_lib = None
+
+c_int, c_float, c_void_p, c_size_t = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+c_u32_p = ctypes.POINTER(ctypes.c_uint32)
+
+_SIGNATURES = {
+    "attn_status_string": (ctypes.c_char_p, [c_int]),
+    "attn_version": (c_int, []),
+    "attn_prefill": (c_int, [c_void_p] * 5 + [c_int] * 5 + [c_float, c_int, c_void_p]),
+    "attn_decode_num_slots": (c_int, [c_int] * 4),
+    "attn_decode_workspace_bytes": (c_size_t, [c_int] * 4),
+    "attn_decode_paged": (c_int, [c_void_p] * 7 + [c_int] * 9 + [c_float, c_void_p, c_size_t, c_void_p]),
+    "attn_combine": (c_int, [c_void_p] * 3 + [c_int] * 3 + [c_void_p, c_void_p, c_void_p]),
+    "attn_device_status": (c_int, [c_u32_p, c_int]),
+}
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libattn.so (loaded once).  Raises if it was not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with attention_attn_prefill_gb300.build.build()")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the entry points include/attn.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise AttnError(status, where)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream or 0)
+
+
+def _dev(t: torch.Tensor, dtype, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None, causal: bool = True,
+            out: torch.Tensor | None = None, lse: torch.Tensor | None = None, return_lse: bool = True,
+            stream=None):
+    """Prefill attention: q [B,S,Hq,d], k/v [B,S,Hkv,d] bf16 -> (o [B,S,Hq,d] bf16, lse [B,Hq,S] f32)."""
+    B, S, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, S, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, S, Hkv, d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    st = lib().attn_prefill(
+        _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
+        _dev(out, torch.bfloat16, "out"), _dev(lse, torch.float32, "lse") if lse is not None else None,
+        B, Hq, Hkv, S, d, float(scale), 1 if causal else 0, _stream_handle(stream))
+    _check(st, "attn_prefill")
+    return out, lse
+
+
+def decode_num_slots(max_blocks_per_seq: int, num_splits: int = 1, split_tokens: int = 0,
+                     page_size: int = PAGE_TOKENS) -> int:
+    return int(lib().attn_decode_num_slots(max_blocks_per_seq, page_size, num_splits, split_tokens))
+
+
+def decode_workspace_bytes(num_seqs: int, Hq: int, d: int, slots: int) -> int:
+    return int(lib().attn_decode_workspace_bytes(num_seqs, Hq, d, slots))
+
+
+def decode_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
+                 seq_lens: torch.Tensor, scale: float | None = None, num_splits: int = 1, split_tokens: int = 0,
+                 out: torch.Tensor | None = None, lse: torch.Tensor | None = None, return_lse: bool = True,
+                 workspace: torch.Tensor | None = None, stream=None):
+    """Paged split-KV decode: q [N,Hq,d]; caches [num_blocks,16,Hkv,d] bf16 -> (o [N,Hq,d], lse [N,Hq])."""
+    N, Hq, d = q.shape
+    num_blocks, page, Hkv, dk = k_cache.shape
+    if dk != d or v_cache.shape != k_cache.shape:
+        raise ValueError("caches must be [num_blocks, page, Hkv, d] matching q")
+    if block_table.dim() != 2 or block_table.shape[0] != N or seq_lens.shape != (N,):
+        raise ValueError("block_table must be [N, max_blocks] and seq_lens [N]")
+    max_blocks = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    slots = decode_num_slots(max_blocks, num_splits, split_tokens, page)
+    if slots < 1:
+        raise AttnError(1, "attn_decode_num_slots")
+    need = decode_workspace_bytes(N, Hq, d, slots)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((N, Hq), dtype=torch.float32, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().attn_decode_paged(
+        _dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.bfloat16, "k_cache"),
+        _dev(v_cache, torch.bfloat16, "v_cache"), _dev(block_table, torch.int32, "block_table"),
+        _dev(seq_lens, torch.int32, "seq_lens"), _dev(out, torch.bfloat16, "out"),
+        _dev(lse, torch.float32, "lse") if lse is not None else None,
+        N, Hq, Hkv, d, page, max_blocks, num_blocks, num_splits, split_tokens, float(scale), ws_ptr, ws_bytes,
+        _stream_handle(stream))
+    _check(st, "attn_decode_paged")
+    return out, lse
+
+
+def combine(part_o: torch.Tensor, part_m: torch.Tensor, part_l: torch.Tensor, out: torch.Tensor | None = None,
+            lse: torch.Tensor | None = None, return_lse: bool = True, stream=None):
+    """Merge partials: part_o [rows, splits, d], part_m/part_l [rows, splits] f32 -> (o [rows,d] bf16, lse [rows])."""
+    rows, splits, d = part_o.shape
+    if part_m.shape != (rows, splits) or part_l.shape != (rows, splits):
+        raise ValueError("part_m and part_l must be [rows, splits]")
+    if out is None:
+        out = torch.empty((rows, d), dtype=torch.bfloat16, device=part_o.device)
+    if lse is None and return_lse:
+        lse = torch.empty((rows,), dtype=torch.float32, device=part_o.device)
+    st = lib().attn_combine(
+        _dev(part_o, torch.float32, "part_o"), _dev(part_m, torch.float32, "part_m"),
+        _dev(part_l, torch.float32, "part_l"), rows, splits, d, _dev(out, torch.bfloat16, "out"),
+        _dev(lse, torch.float32, "lse") if lse is not None else None, _stream_handle(stream))
+    _check(st, "attn_combine")
+    return out, lse
+
+
+def device_status(clear: bool = True) -> int:
+    """First device-side error code recorded by a kernel (0 = none); synchronises the device."""
+    code = ctypes.c_uint32(0)
+    _check(lib().attn_device_status(ctypes.byref(code), 1 if clear else 0), "attn_device_status")
+    return int(code.value)

@@ -1,0 +1,211 @@
+// C-ABI layer of libattn.so: argument checks, TMA descriptor encoding and
+// kernel dispatch.  See include/attn.h for the contract of each entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn.h"
+#include "decode.h"
+#include "prefill.h"
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr int kPage = 16;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 3-D bf16 tensor map; dims innermost first, strides in bytes for dims 1 and 2.
+bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1,
+               uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1, stride2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+attn_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_DEVICE: return "ATTN_ERR_DEVICE";
+  }
+  return "ATTN_ERR_UNKNOWN";
+}
+
+int attn_version(void) { return kVersion; }
+
+attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                           int S, int d, float scale, int causal, void* stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  // TMA coordinates are int32 and each map dimension must stay below 2^32
+  if (static_cast<int64_t>(Hq) * d > (1 << 30) || S > (1 << 30) || B > 65535 || Hq > 65535)
+    return ATTN_ERR_INVALID_ARG;
+
+  attn::PrefillMaps maps;
+  const uint64_t q_row = static_cast<uint64_t>(Hq) * d * 2, kv_row = static_cast<uint64_t>(Hkv) * d * 2;
+  const uint32_t rows = static_cast<uint32_t>(attn::prefill_tile_rows());
+  if (!encode_3d(&maps.q, q, static_cast<uint64_t>(Hq) * d, S, B, q_row, q_row * S, 64, rows, 1) ||
+      !encode_3d(&maps.k, k, static_cast<uint64_t>(Hkv) * d, S, B, kv_row, kv_row * S, 64, rows, 1) ||
+      !encode_3d(&maps.v, v, static_cast<uint64_t>(Hkv) * d, S, B, kv_row, kv_row * S, 64, rows, 1) ||
+      !encode_3d(&maps.o, o, static_cast<uint64_t>(Hq) * d, S, B, q_row, q_row * S, 64, rows, 1))
+    return ATTN_ERR_CUDA;
+
+  attn::PrefillParams p;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.S = S;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.causal = causal ? 1 : 0;
+  const int per_cta = attn::prefill_rows_per_cta();
+  p.num_qblocks = (S + per_cta - 1) / per_cta;
+  p.n_kv_total = (S + 127) / 128;
+  if (p.num_qblocks > 65535) return ATTN_ERR_INVALID_ARG;
+  return from_cuda(attn::prefill_launch(d, maps, p, static_cast<cudaStream_t>(stream)));
+}
+
+int attn_decode_num_slots(int max_blocks_per_seq, int page_size, int num_splits, int split_tokens) {
+  if (max_blocks_per_seq < 1 || page_size != kPage) return 0;
+  if (split_tokens > 0) {
+    if (split_tokens % page_size) return 0;
+    const int64_t max_tokens = static_cast<int64_t>(max_blocks_per_seq) * page_size;
+    return static_cast<int>((max_tokens + split_tokens - 1) / split_tokens);
+  }
+  if (split_tokens < 0 || num_splits < 1) return 0;
+  return num_splits < max_blocks_per_seq ? num_splits : max_blocks_per_seq;
+}
+
+size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d, int slots) {
+  if (num_seqs < 1 || Hq < 1 || d < 1 || slots < 1) return 0;
+  if (slots == 1) return 0;
+  return static_cast<size_t>(num_seqs) * Hq * slots * (static_cast<size_t>(d) + 2) * sizeof(float);
+}
+
+attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                                const int32_t* seq_lens, void* o, float* lse, int num_seqs, int Hq, int Hkv, int d,
+                                int page_size, int max_blocks_per_seq, int num_blocks, int num_splits,
+                                int split_tokens, float scale, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr || seq_lens == nullptr ||
+      o == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (num_seqs < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_blocks_per_seq < 1 || num_blocks < 1)
+    return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (page_size != kPage) return ATTN_ERR_UNSUPPORTED;
+  if (d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;  // query heads per KV head fill at most 16 MMA rows
+  if (num_seqs > 65535 || Hkv > 65535) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(num_blocks) * page_size > (int64_t(1) << 31) - 1) return ATTN_ERR_INVALID_ARG;
+  const int slots = attn_decode_num_slots(max_blocks_per_seq, page_size, num_splits, split_tokens);
+  if (slots < 1 || slots > 65535) return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_decode_workspace_bytes(num_seqs, Hq, d, slots);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+    return ATTN_ERR_WORKSPACE;
+
+  attn::DecodeMaps maps;
+  const uint64_t row = static_cast<uint64_t>(Hkv) * d * 2;
+  const uint64_t tokens = static_cast<uint64_t>(num_blocks) * page_size;
+  if (!encode_3d(&maps.k, k_cache, d, Hkv, tokens, static_cast<uint64_t>(d) * 2, row, 64, 1, page_size) ||
+      !encode_3d(&maps.v, v_cache, d, Hkv, tokens, static_cast<uint64_t>(d) * 2, row, 64, 1, page_size))
+    return ATTN_ERR_CUDA;
+
+  attn::DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.N = num_seqs;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.splits = slots;
+  p.split_pages = split_tokens > 0 ? split_tokens / page_size : 0;
+  p.num_splits = split_tokens > 0 ? 0 : slots;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.write_final = slots == 1 ? 1 : 0;
+  float* ws = static_cast<float*>(workspace);
+  const size_t nrow = static_cast<size_t>(num_seqs) * Hq;
+  p.part_o = slots > 1 ? ws : nullptr;
+  p.part_m = slots > 1 ? ws + nrow * slots * d : nullptr;
+  p.part_l = slots > 1 ? ws + nrow * slots * (d + 1) : nullptr;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = attn::decode_split_launch(d, maps, p, st);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  if (slots > 1) e = attn::combine_launch(d, p.part_o, p.part_m, p.part_l, static_cast<int>(nrow), slots, o, lse, st);
+  return from_cuda(e);
+}
+
+attn_status_t attn_combine(const float* part_o, const float* part_m, const float* part_l, int rows,
+                           int num_splits, int d, void* o, float* lse, void* stream) {
+  if (part_o == nullptr || part_m == nullptr || part_l == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(part_o) || !aligned16(o) || (reinterpret_cast<uintptr_t>(part_m) & 3u) ||
+      (reinterpret_cast<uintptr_t>(part_l) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (rows < 1 || num_splits < 1) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+  return from_cuda(attn::combine_launch(d, part_o, part_m, part_l, rows, num_splits, o, lse,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_device_status(uint32_t* code, int clear) {
+  if (code == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+  uint32_t a = 0, b = 0;
+  if (attn::prefill_status(&a, clear != 0) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (attn::decode_status(&b, clear != 0) != cudaSuccess) return ATTN_ERR_CUDA;
+  *code = a != 0 ? a : b;
+  return ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,458 @@
+// Paged split-KV decode and the log-sum-exp combine on sm_103a.
+//
+// What it computes: one query token per sequence attends to all seq_len
+// cached tokens ("Why your local LLM feels dumber than it is" (Part 3.14),
+// section "What attention is trying to calculate"), read through a block
+// table of 16-token pages ("GPU Datapath: Where Every Byte Moves in One LLM
+// Inference Step", section D "Paged decode attention -- the zero-reuse
+// stream").  The history is cut into contiguous page-aligned groups; each
+// group yields a partial (normalised output, local max, local sum) and the
+// partials are merged with weights l_i * exp(m_i - M) (section "Why the
+// calculation is split into groups").
+//
+// Split kernel: one CTA per (split, KV head, sequence).  Each of its warps
+// owns every NW-th page of the split and runs its own TMA pipeline: the page's
+// K and V rows for this KV head arrive as 16-row x 128-byte panels (128-byte
+// swizzle) on an mbarrier.  The G query heads that share the KV head form the
+// rows of a 16 x d matrix (padded with zeros), so S = Q K^T and O += P V are
+// m16n8k16 tensor-core products: at d = 256 and G = 8 the stream needs about
+// 8 flops per byte, more than the FP32 pipes sustain next to HBM.  Online
+// softmax runs in registers with quad shuffles; O is rescaled lazily.  The
+// warps' states are merged in shared memory; the CTA writes either the final
+// bf16 output + LSE (one split) or its partial.
+//
+// Combine kernel: one warp per (sequence, query head) merges the partials.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <cstdint>
+
+#include "decode.h"
+#include "sm103.cuh"
+
+namespace attn {
+
+__device__ uint32_t g_decode_status;
+
+namespace {
+
+constexpr int PAGE = 16;
+constexpr int PANEL_BYTES = PAGE * 128;  // 16 token rows x 64 bf16
+constexpr float RESCALE_LOG2_THRESHOLD = 8.0f;
+constexpr float LN2 = 0.693147180559945309f;
+
+template <int D, int NW, int NS>
+struct DLayout {
+  static constexpr int PANELS = D / 64;
+  static constexpr int KV_BYTES = PANELS * PANEL_BYTES;  // one page of K (or V) for one KV head
+  static constexpr int STAGE_BYTES = 2 * KV_BYTES;
+  static constexpr int Q_OFF = 0;
+  static constexpr int Q_BYTES = 16 * D * 2;
+  static constexpr int STAGE_OFF = (Q_OFF + Q_BYTES + 1023) & ~1023;
+  static constexpr int WARP_BYTES = NS * STAGE_BYTES;
+  static constexpr int BAR_OFF = STAGE_OFF + NW * WARP_BYTES;
+  static constexpr int USED = BAR_OFF + NW * NS * 8;
+  static constexpr int ALLOC = USED + 1024;
+  // per-warp merge record (after its pipeline drains): m[16], l[16], o[16][D]
+  static constexpr int MERGE_BYTES = 32 * 4 + 16 * D * 4;
+  static_assert(MERGE_BYTES <= WARP_BYTES, "merge record must fit in a warp's stages");
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Byte offset of element (row, x) in a stack of 128B-swizzled 16-row panels.
+__device__ __forceinline__ uint32_t panel_off(int row, int x) {
+  const int u = (x & 63) >> 3;
+  return (x >> 6) * PANEL_BYTES + row * 128 + ((u ^ (row & 7)) << 4) + (x & 7) * 2;
+}
+
+// Pages [first, end) of sequence n that split s owns.
+__device__ __forceinline__ void split_pages(const DecodeParams& p, int L, int s, int& first, int& end) {
+  const int pages = (L + PAGE - 1) / PAGE;
+  int span = p.split_pages;
+  if (span <= 0) span = (pages + p.num_splits - 1) / p.num_splits;
+  first = s * span;
+  end = first + span < pages ? first + span : pages;
+  if (span <= 0 || first > pages) first = end = pages;
+}
+
+template <int D, int NW, int NS>
+__global__ void __launch_bounds__(NW * 32)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                        const DecodeParams p) {
+  using L = DLayout<D, NW, NS>;
+  constexpr bool Q_IN_REGS = (D <= 128);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sQ = smem + L::Q_OFF;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int s = blockIdx.x;
+  const int g = blockIdx.y;
+  const int n = blockIdx.z;
+  const int G = p.G;
+  int seq_len = p.seq_lens[n];
+  if (seq_len < 0 || seq_len > p.max_blocks * PAGE) {
+    // a length the block table cannot cover: record it and stay inside the table
+    if (threadIdx.x == 0) set_error(&g_decode_status, kDevBadSplit);
+    seq_len = seq_len < 0 ? 0 : p.max_blocks * PAGE;
+  }
+  int pfirst, pend;
+  split_pages(p, seq_len, s, pfirst, pend);
+  const int npages = pend - pfirst;
+
+  // Q rows of the G heads sharing KV head g (rows >= G are zero), swizzled by 16-byte unit.
+  for (int i = threadIdx.x; i < 16 * (D / 8); i += NW * 32) {
+    const int r = i / (D / 8);
+    const int u = i % (D / 8);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < G)
+      v = *reinterpret_cast<const uint4*>(p.q + ((static_cast<size_t>(n) * p.Hq + g * G + r) * D + u * 8));
+    *reinterpret_cast<uint4*>(sQ + r * (D * 2) + ((u ^ (r & 7)) << 4)) = v;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NW * NS; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  uint8_t* my_stages = smem + L::STAGE_OFF + warp * L::WARP_BYTES;
+  uint64_t* my_bars = bars + warp * NS;
+  const int n_my = npages > warp ? (npages - warp + NW - 1) / NW : 0;
+
+  auto issue = [&](int k) {
+    const int pi = pfirst + warp + k * NW;
+    int pid = p.block_table[static_cast<size_t>(n) * p.max_blocks + pi];
+    if (pid < 0 || pid >= p.num_blocks) {
+      set_error(&g_decode_status, kDevBadPage);
+      pid = 0;
+    }
+    uint8_t* st = my_stages + (k % NS) * L::STAGE_BYTES;
+    uint64_t* bar = &my_bars[k % NS];
+    mbar_arrive_expect_tx(bar, L::STAGE_BYTES);
+#pragma unroll
+    for (int c = 0; c < L::PANELS; ++c) {
+      tma_load_3d(st + c * PANEL_BYTES, &tm_k, bar, c * 64, g, pid * PAGE);
+      tma_load_3d(st + L::KV_BYTES + c * PANEL_BYTES, &tm_v, bar, c * 64, g, pid * PAGE);
+    }
+  };
+
+  if (lane == 0) {
+    for (int k = 0; k < n_my && k < NS; ++k) issue(k);
+  }
+  __syncwarp();
+
+  const uint32_t q_base = smem_u32(sQ);
+  // ldmatrix row addresses for the A (Q) fragments: matrix mi = lane/8
+  const int a_row = ((lane >> 3) & 1) * 8 + (lane & 7);
+  const int a_colh = (lane >> 4) * 8;  // 0 or 8 within the 16-wide k step
+  uint32_t qa[Q_IN_REGS ? D / 16 : 1][4];
+  if constexpr (Q_IN_REGS) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int x = kk * 16 + a_colh;
+      ldsm_x4(q_base + a_row * (D * 2) + (((x >> 3) ^ (a_row & 7)) << 4), qa[kk][0], qa[kk][1], qa[kk][2],
+              qa[kk][3]);
+    }
+  }
+
+  const float c2 = p.scale_log2;
+  float m_a = -INFINITY, m_b = -INFINITY;  // rows lane/4 and lane/4 + 8, raw-score units
+  float l_a = 0.f, l_b = 0.f;              // this lane's share of the row sums
+  float oacc[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+
+  // B-fragment row addresses within a K panel (non-transposed) and a V panel (transposed)
+  const int kb_tok = (lane >> 4) * 8 + (lane & 7);
+  const int kb_colh = ((lane >> 3) & 1) * 8;
+  const int vb_tok = ((lane >> 3) & 1) * 8 + (lane & 7);
+  const int vb_colh = (lane >> 4) * 8;
+
+  bool ok = true;
+  int consumed = 0;
+  for (int k = 0; k < n_my; ++k) {
+    ok = __all_sync(0xffffffffu, mbar_wait(&my_bars[k % NS], (k / NS) & 1));
+    if (!ok) break;
+    consumed = k + 1;
+    uint8_t* st = my_stages + (k % NS) * L::STAGE_BYTES;
+    const uint32_t k_base = smem_u32(st);
+    const uint32_t v_base = k_base + L::KV_BYTES;
+    const int tok0 = (pfirst + warp + k * NW) * PAGE;
+    const int valid = seq_len - tok0 < PAGE ? seq_len - tok0 : PAGE;
+    if (valid < PAGE) {
+      // zero the V rows past the end of the sequence: P is 0 there, but 0 * NaN would not be
+      for (int i = lane; i < (PAGE - valid) * (D / 8); i += 32) {
+        const int r = valid + i / (D / 8);
+        const int x = (i % (D / 8)) * 8;
+        *reinterpret_cast<uint4*>(st + L::KV_BYTES + panel_off(r, x)) = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+    // ---- S = Q K^T (16 heads x 16 tokens)
+    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      uint32_t a[4];
+      if constexpr (Q_IN_REGS) {
+        a[0] = qa[kk][0]; a[1] = qa[kk][1]; a[2] = qa[kk][2]; a[3] = qa[kk][3];
+      } else {
+        const int x = kk * 16 + a_colh;
+        ldsm_x4(q_base + a_row * (D * 2) + (((x >> 3) ^ (a_row & 7)) << 4), a[0], a[1], a[2], a[3]);
+      }
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(k_base + panel_off(kb_tok, kk * 16 + kb_colh), b0, b1, b2, b3);
+      mma_bf16(sacc[0], a, b0, b1);
+      mma_bf16(sacc[1], a, b2, b3);
+    }
+    // ---- mask tokens past seq_len (also hides NaN keys there)
+    const int colq = 2 * (lane & 3);
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (nb * 8 + colq + (e & 1) >= valid) sacc[nb][e] = -INFINITY;
+    // ---- online softmax, rows a = lane/4 and b = lane/4 + 8
+    float mx_a = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
+    float mx_b = fmaxf(fmaxf(sacc[0][2], sacc[0][3]), fmaxf(sacc[1][2], sacc[1][3]));
+    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+    float al_a = 1.f, al_b = 1.f;
+    bool rs = false;
+    if (k == 0) {
+      m_a = mx_a;
+      m_b = mx_b;
+    } else {
+      if ((mx_a - m_a) * c2 > RESCALE_LOG2_THRESHOLD) {
+        al_a = ex2_approx((m_a - mx_a) * c2);
+        l_a *= al_a;
+        m_a = mx_a;
+        rs = true;
+      }
+      if ((mx_b - m_b) * c2 > RESCALE_LOG2_THRESHOLD) {
+        al_b = ex2_approx((m_b - mx_b) * c2);
+        l_b *= al_b;
+        m_b = mx_b;
+        rs = true;
+      }
+    }
+    if (__any_sync(0xffffffffu, rs)) {
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        oacc[i][0] *= al_a; oacc[i][1] *= al_a;
+        oacc[i][2] *= al_b; oacc[i][3] *= al_b;
+      }
+    }
+    const float mb_a = m_a * c2, mb_b = m_b * c2;
+    float pr[2][4];
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) {
+      pr[nb][0] = ex2_approx(fmaf(sacc[nb][0], c2, -mb_a));
+      pr[nb][1] = ex2_approx(fmaf(sacc[nb][1], c2, -mb_a));
+      pr[nb][2] = ex2_approx(fmaf(sacc[nb][2], c2, -mb_b));
+      pr[nb][3] = ex2_approx(fmaf(sacc[nb][3], c2, -mb_b));
+      l_a += pr[nb][0] + pr[nb][1];
+      l_b += pr[nb][2] + pr[nb][3];
+    }
+    uint32_t pa[4];
+    pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+    pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+    pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+    pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+    // ---- O += P V
+#pragma unroll
+    for (int nb = 0; nb < D / 8; nb += 2) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(v_base + panel_off(vb_tok, nb * 8 + vb_colh), b0, b1, b2, b3);
+      mma_bf16(oacc[nb], pa, b0, b1);
+      mma_bf16(oacc[nb + 1], pa, b2, b3);
+    }
+    __syncwarp();
+    if (lane == 0 && k + NS < n_my) {
+      fence_proxy_async_smem();
+      issue(k + NS);
+    }
+    __syncwarp();
+  }
+  if (!ok) {
+    set_error(&g_decode_status, kDevWaitTimeout);
+    // drain copies still in flight before the stage memory is reused
+    if (lane == 0)
+      for (int k = consumed; k < n_my && k < consumed + NS; ++k) mbar_wait(&my_bars[k % NS], (k / NS) & 1);
+  }
+  __syncwarp();
+
+  // ---- per-warp record: m (log2-scaled), l, unnormalised o, rows < 16
+  l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+  l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+  l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+  l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+  float* rec_m = reinterpret_cast<float*>(my_stages);
+  float* rec_l = rec_m + 16;
+  float* rec_o = rec_m + 32;
+  const int ra = lane >> 2, rb = ra + 8;
+  if ((lane & 3) == 0) {
+    const bool any = n_my > 0;
+    rec_m[ra] = any ? m_a * c2 : -INFINITY;
+    rec_m[rb] = any ? m_b * c2 : -INFINITY;
+    rec_l[ra] = any ? l_a : 0.f;
+    rec_l[rb] = any ? l_b : 0.f;
+  }
+#pragma unroll
+  for (int nb = 0; nb < D / 8; ++nb) {
+    const int x = nb * 8 + 2 * (lane & 3);
+    *reinterpret_cast<float2*>(rec_o + ra * D + x) = make_float2(oacc[nb][0], oacc[nb][1]);
+    *reinterpret_cast<float2*>(rec_o + rb * D + x) = make_float2(oacc[nb][2], oacc[nb][3]);
+  }
+  __syncthreads();
+
+  // ---- merge the warps and write the final output or this split's partial
+  const uint8_t* rec0 = smem + L::STAGE_OFF;
+  for (int i = threadIdx.x; i < G * D; i += NW * 32) {
+    const int r = i / D, x = i % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, reinterpret_cast<const float*>(rec0 + w * L::WARP_BYTES)[r]);
+    float Lsum = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float* rm = reinterpret_cast<const float*>(rec0 + w * L::WARP_BYTES);
+        const float wm = rm[r];
+        if (wm == -INFINITY) continue;
+        const float f = ex2_approx(wm - M);
+        Lsum += rm[16 + r] * f;
+        O += rm[32 + r * D + x] * f;
+      }
+    }
+    const int hq = g * G + r;
+    const size_t row = static_cast<size_t>(n) * p.Hq + hq;
+    if (p.write_final) {
+      const float out = (Lsum > 0.f) ? O / Lsum : 0.f;
+      p.o[row * D + x] = __float2bfloat16_rn(out);
+      if (x == 0 && p.lse != nullptr) p.lse[row] = (Lsum > 0.f) ? (M + log2f(Lsum)) * LN2 : -INFINITY;
+    } else {
+      const size_t slot = row * p.splits + s;
+      p.part_o[slot * D + x] = (Lsum > 0.f) ? O / Lsum : 0.f;
+      if (x == 0) {
+        p.part_m[slot] = (Lsum > 0.f) ? M * LN2 : -INFINITY;
+        p.part_l[slot] = Lsum;
+      }
+    }
+  }
+}
+
+// One warp per (sequence, query head): O = sum_i w_i o_i / sum_i w_i, w_i = l_i exp(m_i - M).
+template <int D>
+__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
+                                                      const float* __restrict__ part_m,
+                                                      const float* __restrict__ part_l, int rows, int splits,
+                                                      __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + warp;
+  if (row >= rows) return;
+  const float* pm = part_m + static_cast<size_t>(row) * splits;
+  const float* pl = part_l + static_cast<size_t>(row) * splits;
+  float M = -INFINITY;
+  for (int i = lane; i < splits; i += 32)
+    if (pl[i] > 0.f) M = fmaxf(M, pm[i]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  constexpr int PER = D / 32;  // output columns per lane
+  float acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  float W = 0.f;
+  if (M != -INFINITY) {
+    const float* po = part_o + static_cast<size_t>(row) * splits * D;
+    for (int i = 0; i < splits; ++i) {
+      const float li = pl[i];
+      if (!(li > 0.f)) continue;
+      const float w = li * expf(pm[i] - M);
+      W += w;
+      const float* src = po + static_cast<size_t>(i) * D + lane * PER;
+#pragma unroll
+      for (int e = 0; e < PER; e += 2) {
+        const float2 v = *reinterpret_cast<const float2*>(src + e);
+        acc[e] += w * v.x;
+        acc[e + 1] += w * v.y;
+      }
+    }
+  }
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  __nv_bfloat16* dst = o + static_cast<size_t>(row) * D + lane * PER;
+#pragma unroll
+  for (int e = 0; e < PER; e += 2) {
+    *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+  }
+  if (lse != nullptr && lane == 0) lse[row] = W > 0.f ? M + logf(W) : -INFINITY;
+}
+
+template <int D, int NW, int NS>
+cudaError_t launch_split(const DecodeMaps& m, const DecodeParams& p, cudaStream_t stream) {
+  auto kern = decode_split_kernel<D, NW, NS>;
+  const int smem = DLayout<D, NW, NS>::ALLOC;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.splits, p.Hkv, p.N);
+  kern<<<grid, NW * 32, smem, stream>>>(m.k, m.v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t decode_split_launch(int d, const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream) {
+  if (d == 128) return launch_split<128, 4, 3>(maps, p, stream);
+  if (d == 256) return launch_split<256, 4, 3>(maps, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t combine_launch(int d, const float* part_o, const float* part_m, const float* part_l, int rows,
+                           int splits, void* o, float* lse, cudaStream_t stream) {
+  dim3 grid((rows + 3) / 4);
+  auto* out = static_cast<__nv_bfloat16*>(o);
+  if (d == 128) combine_kernel<128><<<grid, 128, 0, stream>>>(part_o, part_m, part_l, rows, splits, out, lse);
+  else if (d == 256) combine_kernel<256><<<grid, 128, 0, stream>>>(part_o, part_m, part_l, rows, splits, out, lse);
+  else if (d == 64) combine_kernel<64><<<grid, 128, 0, stream>>>(part_o, part_m, part_l, rows, splits, out, lse);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t decode_status(uint32_t* out, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_decode_status, sizeof(uint32_t));
+  if (e == cudaSuccess && clear) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_decode_status, &zero, sizeof(uint32_t));
+  }
+  return e;
+}
+
+}  // namespace attn

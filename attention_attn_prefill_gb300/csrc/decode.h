@@ -1,0 +1,42 @@
+// Internal interface between the C-ABI layer and the decode kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace attn {
+
+// TMA descriptors of the paged caches: 3-D maps {d, Hkv, num_blocks*page},
+// 64-element x 1-head x 16-token boxes, 128-byte swizzle.
+struct DecodeMaps {
+  CUtensorMap k, v;
+};
+
+struct DecodeParams {
+  const __nv_bfloat16* q;      // [N][Hq][d]
+  const int32_t* block_table;  // [N][max_blocks]
+  const int32_t* seq_lens;     // [N]
+  __nv_bfloat16* o;            // [N][Hq][d]    (write_final)
+  float* lse;                  // [N][Hq] or null (write_final)
+  float* part_o;               // [N][Hq][splits][d]
+  float* part_m;               // [N][Hq][splits]
+  float* part_l;               // [N][Hq][splits]
+  int N, Hq, Hkv, G;
+  int max_blocks, num_blocks;
+  int splits;       // grid extent along splits (partial slots per row)
+  int split_pages;  // > 0: pages per split; 0: ceil(pages / num_splits) per sequence
+  int num_splits;
+  float scale;
+  float scale_log2;
+  int write_final;  // 1: write o / lse directly (one split)
+};
+
+cudaError_t decode_split_launch(int d, const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream);
+cudaError_t combine_launch(int d, const float* part_o, const float* part_m, const float* part_l, int rows,
+                           int splits, void* o, float* lse, cudaStream_t stream);
+cudaError_t decode_status(uint32_t* out, bool clear);
+
+}  // namespace attn

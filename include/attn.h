@@ -1,0 +1,160 @@
+/*
+ * attn.h -- C ABI of libattn.so: exact tiled attention with an online softmax
+ * on NVIDIA GB300 (sm_103a).
+ *
+ * The operations (definitions from the pages this library implements):
+ *
+ *   attention of a query row over the keys it may see --
+ *     "Why your local LLM feels dumber than it is" (Part 3.14), section
+ *     "What attention is trying to calculate": score_t = scale * dot(q, k_t),
+ *     weights exp(score_t) normalised over the visible tokens, output the
+ *     weighted sum of the values.
+ *
+ *   tiled prefill with a running max and running sum --
+ *     "Streaming process -- How the SM works inside a transformer", Steps 3-8
+ *     and its code snippet.
+ *
+ *   split-KV decode over a paged cache and the merge of per-group partials --
+ *     "GPU Datapath: Where Every Byte Moves in One LLM Inference Step",
+ *     section D "Paged decode attention -- the zero-reuse stream", and
+ *     "Why your local LLM feels dumber than it is", sections "Why the
+ *     calculation is split into groups" and "Backend names expand into four
+ *     decode algorithms".
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers (CUDA global memory of the current
+ *     device), 16-byte aligned, densely packed in the layout stated.  bf16 is
+ *     IEEE bfloat16 (2 bytes); LSE values are float32 natural logarithms of
+ *     the sum of exp(scaled scores).
+ *   - `stream` is a cudaStream_t passed as an opaque pointer (NULL = legacy
+ *     default stream).  Kernels are enqueued on it and run asynchronously;
+ *     outputs are valid once the stream reaches that point.
+ *   - The caller owns all memory.  The library allocates nothing on the
+ *     device and keeps no per-call state.  Argument errors are detected on the host before
+ *     anything is enqueued and leave the outputs untouched.
+ *   - Grouped-query attention: Hq must be a multiple of Hkv; query head h uses
+ *     KV head h / (Hq / Hkv).
+ *   - Return value: ATTN_OK, or one of the error codes below.  No exception
+ *     crosses the ABI.  Errors detected by a kernel while it runs (a wait that
+ *     timed out, a block-table entry out of range) are recorded in a device
+ *     status word that attn_device_status() reads.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null pointer, bad shape, misalignment, Hq % Hkv != 0 */
+  ATTN_ERR_UNSUPPORTED = 2, /* a head dim or option this build has no kernel for */
+  ATTN_ERR_WORKSPACE = 3,   /* decode workspace missing or too small */
+  ATTN_ERR_CUDA = 4,        /* a CUDA runtime/driver call or kernel launch failed */
+  ATTN_ERR_DEVICE = 5       /* a kernel recorded an error (see attn_device_status) */
+} attn_status_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* attn_status_string(attn_status_t status);
+
+/*
+ * Prefill forward.
+ *   q   [B, S, Hq,  d] bf16      k, v [B, S, Hkv, d] bf16
+ *   o   [B, S, Hq,  d] bf16 (output)
+ *   lse [B, Hq, S]     f32 (output, may be NULL)
+ *   d in {64, 128}; B, S >= 1; Hq, Hkv >= 1 with Hq % Hkv == 0.
+ *   scale: multiplier of q.k (for example 1/sqrt(d)).
+ *   causal != 0: row i sees keys 0..i (itself included); causal == 0: all S keys.
+ * Row i of o is sum_j softmax_j(scale * q_i.k_j) v_j over the visible keys;
+ * lse[b, h, i] = ln sum_j exp(scale * q_i.k_j).
+ * Arithmetic: bf16 inputs, f32 scores and accumulators, the probabilities
+ * rounded to bf16 for P.V while the normaliser sums the unrounded f32 values,
+ * output rounded to bf16 (nearest even).
+ */
+attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                           int Hkv, int S, int d, float scale, int causal, void* stream);
+
+/*
+ * Number of partial slots per (sequence, query head) that attn_decode_paged
+ * uses for the given split settings (1 means the split kernel writes the
+ * output directly and needs no workspace).
+ *   split_tokens > 0: groups of split_tokens tokens (must be a multiple of
+ *     page_size); slots = ceil(max_blocks_per_seq * page_size / split_tokens).
+ *   split_tokens == 0: num_splits (>= 1) groups per sequence.
+ * Returns 0 for invalid arguments.
+ */
+int attn_decode_num_slots(int max_blocks_per_seq, int page_size, int num_splits, int split_tokens);
+
+/*
+ * Bytes of workspace attn_decode_paged needs: num_seqs * Hq * slots * (d + 2)
+ * floats when slots > 1, else 0.
+ */
+size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d, int slots);
+
+/*
+ * Single-token decode over a paged KV cache, split over the context.
+ *   q            [num_seqs, Hq, d] bf16
+ *   k_cache,
+ *   v_cache      [num_blocks, page_size, Hkv, d] bf16: physical pages of
+ *                page_size consecutive token rows
+ *   block_table  [num_seqs, max_blocks_per_seq] int32: physical page of each
+ *                logical page (entries past a sequence's last page are ignored)
+ *   seq_lens     [num_seqs] int32, 0 <= len <= max_blocks_per_seq * page_size
+ *   o            [num_seqs, Hq, d] bf16 (output)
+ *   lse          [num_seqs, Hq] f32 (output, may be NULL)
+ *   d in {128, 256}; page_size == 16.
+ *   Splits: contiguous, page-aligned groups of tokens -- split_tokens per
+ *   group if split_tokens > 0, else ceil(pages / num_splits) pages per group.
+ *   Each group gives a partial (normalised f32 output, max, sum); when there
+ *   is more than one slot the partials go to `workspace` and a second kernel
+ *   merges them (same arithmetic as attn_combine).
+ *   workspace: device buffer of at least attn_decode_workspace_bytes(...)
+ *   bytes (may be NULL when that is 0).
+ * The query sees all seq_len tokens.  A sequence with seq_len == 0 gets o = 0
+ * and lse = -inf.  Tokens of the last page past seq_len are never used, even
+ * if they hold NaN.  A block-table entry outside [0, num_blocks) is recorded
+ * as ATTN_ERR_DEVICE (page 0 is read instead).
+ */
+attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                                const int32_t* seq_lens, void* o, float* lse, int num_seqs, int Hq, int Hkv, int d,
+                                int page_size, int max_blocks_per_seq, int num_blocks, int num_splits,
+                                int split_tokens, float scale, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/*
+ * Merge per-group partials ("Why your local LLM feels dumber than it is",
+ * section "Backend names expand into four decode algorithms": normalised
+ * group outputs merged by their log-sum statistics).
+ *   part_o [rows, num_splits, d] f32: normalised output of each group
+ *   part_m [rows, num_splits]    f32: max scaled score of the group (-inf if empty)
+ *   part_l [rows, num_splits]    f32: sum of exp(score - part_m) (0 if empty)
+ *   rows = num_seqs * Hq.
+ *   o   [rows, d] bf16 = sum_i w_i part_o_i / sum_i w_i, w_i = part_l_i exp(part_m_i - M),
+ *       M = max over non-empty groups; groups with part_l <= 0 carry no weight.
+ *   lse [rows] f32 (may be NULL) = M + ln sum_i w_i.  A row with no
+ *       non-empty group gets o = 0 and lse = -inf.
+ *   d in {64, 128, 256}.
+ */
+attn_status_t attn_combine(const float* part_o, const float* part_m, const float* part_l, int rows,
+                           int num_splits, int d, void* o, float* lse, void* stream);
+
+/*
+ * Device-side status: waits for all work on the current device, then stores
+ * the first error code any kernel of this library recorded since the last
+ * clear (0 = none; 1 = a pipeline wait timed out; 2 = block-table entry out of
+ * range; 3 = inconsistent split geometry) and, if `clear` != 0, resets it.
+ */
+attn_status_t attn_device_status(uint32_t* code, int clear);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

@@ -84,6 +84,17 @@ def prefill(q, k, v, scale: float, causal: bool = True, *, heads=None, rows=None
     return o, lse
 
 
+class _PageView:
+    """Indexing a cache page by page, widening each page to float64 on access."""
+
+    def __init__(self, cache):
+        self.cache = cache
+        self.shape = tuple(cache.shape)
+
+    def __getitem__(self, p):
+        return f64(self.cache[p])
+
+
 def gather_pages(cache, block_table_row, seq_len: int, page: int) -> np.ndarray:
     """Logical tokens [seq_len, Hkv, d] of one sequence, read through its block table."""
     npages = (seq_len + page - 1) // page
@@ -102,16 +113,18 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale: float, *,
     seq_lens [N].  Returns o [N,Hq,d] and lse [N,Hq] in float64.
     """
     q = f64(q)
-    kc, vc = f64(k_cache), f64(v_cache)
     bt = np.asarray(block_table.cpu() if isinstance(block_table, torch.Tensor) else block_table)
     lens = [int(x) for x in (seq_lens.tolist() if isinstance(seq_lens, torch.Tensor) else seq_lens)]
     N, Hq, d = q.shape
-    page, Hkv = kc.shape[1], kc.shape[2]
-    o = np.full((N, Hq, vc.shape[3]), np.nan)
+    page, Hkv, dv = k_cache.shape[1], k_cache.shape[2], v_cache.shape[3]
+    o = np.full((N, Hq, dv), np.nan)
     lse = np.full((N, Hq), np.nan)
     for n in (range(N) if seqs is None else seqs):
-        keys = gather_pages(kc, bt[n], lens[n], page)
-        vals = gather_pages(vc, bt[n], lens[n], page)
+        if lens[n] == 0:
+            continue                     # no key: the result is undefined
+        # widen only this sequence's pages (the caches can be large)
+        keys = gather_pages(_PageView(k_cache), bt[n], lens[n], page)
+        vals = gather_pages(_PageView(v_cache), bt[n], lens[n], page)
         for hq in range(Hq):
             g = kv_head_of(hq, Hq, Hkv)
             on, ln = attend(q[n, hq][None, :], keys[:, g, :], vals[:, g, :], scale)

@@ -1,0 +1,170 @@
+"""Paged split-KV decode and combine parity against the float64 oracle (through the C ABI)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.attention as oa
+from parity import check_lse, check_o, to_np
+from workloads import LONGCTX, PAGED, decode_inputs_for, make_decode_inputs
+from workloads.teaching import teaching_scores_values
+
+pytestmark = pytest.mark.gpu
+
+
+def run_decode(attn, x, scale, dev, **kw):
+    args = [t.to(dev) for t in (x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens)]
+    o, lse = attn.decode_paged(*args, scale=scale, **kw)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def compare(attn, x, scale, dev, what, seqs=None, **kw):
+    o, lse = run_decode(attn, x, scale, dev, **kw)
+    wo, wl = oa.decode_paged(x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens, scale, seqs=seqs)
+    sel = list(range(x.q.shape[0])) if seqs is None else list(seqs)
+    check_o(to_np(o)[sel], wo[sel], what)
+    check_lse(to_np(lse)[sel], wl[sel], what)
+    return o, lse
+
+
+@pytest.mark.parametrize("kw", [dict(num_splits=1), dict(num_splits=4), dict(num_splits=16),
+                                dict(num_splits=3), dict(split_tokens=16), dict(split_tokens=48)],
+                         ids=lambda k: "-".join(f"{a}{b}" for a, b in k.items()))
+def test_paged_d128_gqa4(attn, gpu, kw):
+    """Ragged lengths (1..700), NaN in unused page tails and in unused pages."""
+    lens = [1, 15, 16, 17, 31, 64, 100, 129, 255, 256, 257, 500, 700]
+    x = make_decode_inputs(lens, Hq=32, Hkv=8, d=128, seed=51, nan_tail=True, extra_blocks=5)
+    compare(attn, x, 1.0 / math.sqrt(128), gpu, f"d128 {kw}", **kw)
+
+
+@pytest.mark.parametrize("kw", [dict(num_splits=1), dict(num_splits=5), dict(split_tokens=64),
+                                dict(split_tokens=512)],
+                         ids=lambda k: "-".join(f"{a}{b}" for a, b in k.items()))
+def test_paged_d256_gqa8(attn, gpu, kw):
+    lens = [1, 33, 200, 513, 1000, 1300]
+    x = make_decode_inputs(lens, Hq=16, Hkv=2, d=256, seed=52, nan_tail=True, extra_blocks=3)
+    compare(attn, x, 2.0 ** -4, gpu, f"d256 {kw}", **kw)
+
+
+@pytest.mark.parametrize("hq_hkv", [(1, 1), (16, 1), (6, 3)])
+def test_group_sizes(attn, gpu, hq_hkv):
+    Hq, Hkv = hq_hkv
+    x = make_decode_inputs([40, 77, 300], Hq=Hq, Hkv=Hkv, d=128, seed=53)
+    compare(attn, x, 0.1, gpu, f"G={Hq // Hkv}", num_splits=2)
+
+
+def test_empty_sequence(attn, gpu):
+    """seq_len 0 gives o = 0 and lse = -inf; its neighbours are unaffected."""
+    lens = [0, 20, 0, 33]
+    x = make_decode_inputs(lens, Hq=4, Hkv=1, d=128, seed=54)
+    for kw in (dict(num_splits=1), dict(num_splits=4)):
+        o, lse = run_decode(attn, x, 0.1, gpu, **kw)
+        o, lse = o.cpu(), lse.cpu()
+        assert torch.all(o[[0, 2]] == 0) and torch.all(torch.isneginf(lse[[0, 2]]))
+        wo, wl = oa.decode_paged(x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens, 0.1, seqs=[1, 3])
+        check_o(to_np(o)[[1, 3]], wo[[1, 3]], f"neighbours {kw}")
+        check_lse(to_np(lse)[[1, 3]], wl[[1, 3]], f"neighbours {kw}")
+
+
+def test_single_token_returns_value(attn, gpu):
+    x = make_decode_inputs([1, 1], Hq=8, Hkv=2, d=128, seed=55)
+    o, lse = run_decode(attn, x, 0.3, gpu, num_splits=1)
+    o = o.cpu()
+    for n in range(2):
+        pid = int(x.block_table[n, 0])
+        for h in range(8):
+            assert torch.equal(o[n, h], x.v_cache[pid, 0, h // 4])
+
+
+def test_split_counts_agree(attn, gpu):
+    """Different split geometries agree within the bf16 tolerance (not bit-exactly)."""
+    x = make_decode_inputs([3000, 1234, 4096], Hq=32, Hkv=8, d=128, seed=56)
+    outs = [run_decode(attn, x, 0.09, gpu, **kw) for kw in (dict(num_splits=1), dict(num_splits=16),
+                                                           dict(split_tokens=256))]
+    for o, lse in outs[1:]:
+        check_o(to_np(o), to_np(outs[0][0]), "split vs unsplit")
+        check_lse(to_np(lse), to_np(outs[0][1]), "split vs unsplit")
+
+
+def test_bad_page_is_reported(attn, gpu):
+    """A block-table entry outside [0, num_blocks) is recorded as a device error, not read."""
+    x = make_decode_inputs([40], Hq=4, Hkv=1, d=128, seed=57)
+    bt = x.block_table.clone()
+    bt[0, 1] = x.num_blocks + 1000
+    args = [t.to(gpu) for t in (x.q, x.k_cache, x.v_cache, bt, x.seq_lens)]
+    attn.decode_paged(*args, scale=0.1, num_splits=1)
+    assert attn.device_status(clear=True) == 2
+
+
+def test_worked_example_on_gpu(attn, gpu):
+    """The 27,525-token teaching input: one-hot query, k_t = score_t e_0, v_t = value_t.
+
+    The exact output is 1.325056137248; the bf16 result must be one of its two
+    bf16 neighbours, 1.3203125 or 1.328125 ("Plugging in actual numbers").
+    """
+    s, v = teaching_scores_values()
+    L, d = len(s), 128
+    x = make_decode_inputs([L], Hq=1, Hkv=1, d=d, seed=58)
+    x.q.zero_()
+    x.q[0, 0, 0] = 1.0
+    kc = torch.zeros_like(x.k_cache)
+    vc = torch.zeros_like(x.v_cache)
+    pids = x.block_table[0].tolist()
+    st = torch.tensor(s, dtype=torch.bfloat16)
+    vt = torch.tensor(v, dtype=torch.bfloat16)
+    assert torch.equal(st.double(), torch.tensor(s, dtype=torch.float64))   # exact in bf16
+    for p, pid in enumerate(pids):
+        a, b = 16 * p, min(16 * p + 16, L)
+        kc[pid, :b - a, 0, 0] = st[a:b]
+        vc[pid, :b - a, 0, :] = vt[a:b, None]
+    x.k_cache, x.v_cache = kc, vc
+    for kw in (dict(num_splits=1), dict(num_splits=54), dict(split_tokens=448), dict(split_tokens=320)):
+        o, lse = run_decode(attn, x, 1.0, gpu, **kw)
+        vals = set(o[0, 0].float().cpu().tolist())
+        assert len(vals) == 1 and vals.pop() in (1.3203125, 1.328125), kw
+
+
+def test_paged_config_full_size(attn, gpu):
+    """64 sequences, lengths U[512, 8192], GQA 32:8, d=128; 16 sampled sequences checked per split count."""
+    x = decode_inputs_for(PAGED)
+    seqs = list(range(0, 64, 4))
+    for ns in PAGED.num_splits:
+        compare(attn, x, PAGED.scale, gpu, f"paged ns={ns}", seqs=seqs, num_splits=ns)
+
+
+@pytest.mark.parametrize("span", LONGCTX.split_tokens)
+def test_longctx_config_full_size(attn, gpu, span):
+    """8 sequences up to 122,863 tokens, Hq=16, Hkv=2, d=256, scale 2^-4; two sequences checked."""
+    x = decode_inputs_for(LONGCTX)
+    compare(attn, x, LONGCTX.scale, gpu, f"longctx span={span}", seqs=[2, 7], split_tokens=span)
+
+
+# ------------------------------------------------------------------ combine
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_combine_matches_oracle(attn, gpu, d):
+    rng = np.random.default_rng(d)
+    rows, splits = 37, 9
+    po = rng.standard_normal((rows, splits, d)).astype(np.float32)
+    pm = (rng.standard_normal((rows, splits)) * 20).astype(np.float32)
+    pl = rng.uniform(0.5, 300, (rows, splits)).astype(np.float32)
+    empty = rng.random((rows, splits)) < 0.2
+    empty[3, :] = False
+    pm[empty], pl[empty], po[empty] = -np.inf, 0.0, 0.0
+    empty_row = 5
+    pm[empty_row], pl[empty_row], po[empty_row] = -np.inf, 0.0, 0.0
+    t = lambda a: torch.from_numpy(a).to(gpu)
+    o, lse = attn.combine(t(po), t(pm), t(pl))
+    torch.cuda.synchronize()
+    o, lse = to_np(o), to_np(lse)
+    for r in range(rows):
+        if r == empty_row:
+            assert np.all(o[r] == 0) and np.isneginf(lse[r])
+            continue
+        wo, wl = oa.combine(po[r].astype(np.float64), pm[r].astype(np.float64), pl[r].astype(np.float64))
+        # bf16 rounding of O: half an ulp relative, plus f32 accumulation
+        assert np.all(np.abs(o[r] - wo) <= 2.0 ** -8 * np.abs(wo) + 1e-5), r
+        assert abs(lse[r] - wl) <= 1e-4 * (1 + abs(wl)), r

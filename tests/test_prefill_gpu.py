@@ -1,0 +1,136 @@
+"""Prefill parity: the tcgen05/TMA kernel (through the C ABI) against the float64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.attention as oa
+from parity import check_lse, check_o, to_np
+from workloads import LLAMA8B, SWEEP, TINY, make_prefill_inputs, prefill_inputs_for
+
+pytestmark = pytest.mark.gpu
+
+
+def run_prefill(attn, x, scale, causal, dev):
+    q, k, v = (t.to(dev) for t in (x.q, x.k, x.v))
+    o, lse = attn.prefill(q, k, v, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def full_compare(attn, x, scale, causal, dev, what):
+    o, lse = run_prefill(attn, x, scale, causal, dev)
+    wo, wl = oa.prefill(x.q, x.k, x.v, scale, causal=causal)
+    e = check_o(to_np(o), wo, what)
+    check_lse(to_np(lse), wl, what)
+    return e
+
+
+def test_tiny_config(attn, gpu):
+    """B=1, Hq=Hkv=1, S=128, d=64, scale=1/8: every output and LSE."""
+    x = prefill_inputs_for(TINY)
+    full_compare(attn, x, TINY.scale, True, gpu, "tiny")
+
+
+@pytest.mark.parametrize("S", [1, 7, 128, 129, 255, 256, 257, 300, 511, 640])
+@pytest.mark.parametrize("d", [64, 128])
+def test_ragged_lengths_causal(attn, gpu, S, d):
+    """Several Q/KV tiles with a ragged tail, GQA 4:2, two batch elements."""
+    x = make_prefill_inputs(2, 4, 2, S, d, seed=1000 + S + d)
+    full_compare(attn, x, 1.0 / math.sqrt(d), True, gpu, f"S={S} d={d}")
+
+
+@pytest.mark.parametrize("S", [1, 100, 128, 300, 513])
+@pytest.mark.parametrize("d", [64, 128])
+def test_noncausal(attn, gpu, S, d):
+    x = make_prefill_inputs(1, 2, 1, S, d, seed=2000 + S + d)
+    full_compare(attn, x, 1.0 / math.sqrt(d), False, gpu, f"noncausal S={S} d={d}")
+
+
+def test_mqa_and_mha(attn, gpu):
+    for Hq, Hkv in ((8, 1), (3, 3)):
+        x = make_prefill_inputs(1, Hq, Hkv, 200, 128, seed=30 + Hq)
+        full_compare(attn, x, 0.09, True, gpu, f"Hq={Hq} Hkv={Hkv}")
+
+
+def test_large_scores_running_max_jumps(attn, gpu):
+    """Keys scaled so the running max jumps by far more than the lazy-rescale threshold."""
+    x = make_prefill_inputs(1, 2, 1, 700, 128, seed=44)
+    k = x.k.clone()
+    k[:, 129::97] *= 8
+    k[:, 400:] *= 2
+    x.k = k
+    full_compare(attn, x, 1.0 / math.sqrt(128), True, gpu, "max jumps")
+
+
+def test_row0_returns_v0_exactly(attn, gpu):
+    """Causal row 0 sees only key 0, so O[0] = v0 bit-exactly and LSE[0] = scale * q0.k0."""
+    x = make_prefill_inputs(2, 4, 2, 130, 128, seed=5)
+    o, lse = run_prefill(attn, x, 0.1, True, gpu)
+    o = o.cpu()
+    for h in range(4):
+        assert torch.equal(o[:, 0, h], x.v[:, 0, h // 2]), "row 0 must equal v0"
+
+
+def test_outputs_stay_in_bounds(attn, gpu):
+    """Writes stay inside o / lse: guard regions filled with NaN remain NaN."""
+    B, S, Hq, Hkv, d = 1, 200, 2, 1, 128
+    x = make_prefill_inputs(B, Hq, Hkv, S, d, seed=6)
+    q, k, v = (t.to(gpu) for t in (x.q, x.k, x.v))
+    n = B * S * Hq * d
+    big = torch.full((n + 4096,), float("nan"), dtype=torch.bfloat16, device=gpu)
+    o = big[:n].view(B, S, Hq, d)
+    lbig = torch.full((B * Hq * S + 1024,), float("nan"), dtype=torch.float32, device=gpu)
+    lse = lbig[:B * Hq * S].view(B, Hq, S)
+    attn.prefill(q, k, v, scale=0.1, causal=True, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.isnan(big[n:]).all() and torch.isnan(lbig[B * Hq * S:]).all()
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+def test_deterministic_and_stream(attn, gpu):
+    x = make_prefill_inputs(1, 4, 1, 384, 128, seed=7)
+    q, k, v = (t.to(gpu) for t in (x.q, x.k, x.v))
+    o1, l1 = attn.prefill(q, k, v, scale=0.08)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o2, l2 = attn.prefill(q, k, v, scale=0.08, stream=s)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_lse_optional(attn, gpu):
+    x = make_prefill_inputs(1, 2, 2, 64, 64, seed=8)
+    q, k, v = (t.to(gpu) for t in (x.q, x.k, x.v))
+    o, lse = attn.prefill(q, k, v, scale=0.125, return_lse=False)
+    torch.cuda.synchronize()
+    assert lse is None
+    wo, _ = oa.prefill(x.q, x.k, x.v, 0.125)
+    check_o(to_np(o), wo, "no lse")
+
+
+def _sampled(attn, gpu, cfg, heads, nrows, seed):
+    """Full-size config, sampled rows (first, last, tile edges, random) of a few heads."""
+    x = prefill_inputs_for(cfg)
+    o, lse = run_prefill(attn, x, cfg.scale, True, gpu)
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, cfg.S - 129, cfg.S - 1],
+                                     rng.integers(0, cfg.S, nrows)]))
+    on, ln = to_np(o), to_np(lse)
+    for b in range(cfg.B):
+        wo, wl = oa.prefill(x.q, x.k, x.v, cfg.scale, causal=True, heads=heads, rows=rows, batches=[b])
+        for h in heads:
+            check_o(on[b, rows, h], wo[b, rows, h], f"{cfg.name} b={b} h={h}")
+            check_lse(ln[b, h, rows], wl[b, h, rows], f"{cfg.name} b={b} h={h}")
+    assert np.isfinite(on).all() and np.isfinite(ln).all()
+
+
+def test_llama8b_full_size_sampled(attn, gpu):
+    _sampled(attn, gpu, LLAMA8B, heads=[0, 5, 17, 31], nrows=48, seed=1)
+
+
+@pytest.mark.parametrize("cfg", SWEEP, ids=lambda c: c.name)
+def test_sweep_full_size_sampled(attn, gpu, cfg):
+    _sampled(attn, gpu, cfg, heads=[0, 13, 31], nrows=24, seed=cfg.seed)
