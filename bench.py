@@ -1,0 +1,472 @@
+#!/usr/bin/env python
+"""Throughput of the attention hot path on one GB300 (per rank), one JSON line.
+
+One step = the whole hot path over one batch of synthetic input:
+  * causal prefill of the Llama-3.1-8B-shaped workload (B=1, Hq=32, Hkv=8,
+    S=2048, d=128, bf16) -- one kernel launch;
+  * paged split-KV decode of 64 sequences (lengths U[512, 8192], GQA 32:8,
+    d=128, 16-token shuffled pages) -- the split kernel and the combine kernel.
+L2 is flushed (a 256 MiB write) before every step; each launch is bracketed by
+CUDA events on the stream it runs on.
+
+Headline value: prefill TFLOP/s (4*B*Hq*d*S(S+1)/2 causal flops / kernel
+time); the decode GB/s rides along in "decode".  `e2e` repeats the prefill
+metric through the public API with pinned host buffers, host->device copies
+of q/k/v and device->host copies of o/lse inside the timed region.
+
+`--impl reference` times the float64 CPU oracle instead (the reference arm:
+there is no reference implementation, only the pages' formulas), on a bounded
+sample of the same workload, on the host cores.
+
+Multi-GPU: ranks run independent replicas of the workload (no collective on
+the data path); value = total work of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from workloads import LLAMA8B, PAGED, decode_inputs_for, decode_lens_for, decode_min_bytes, prefill_inputs_for  # noqa
+
+METRIC = "prefill TFLOP/s & decode KV GB/s on 1 GB300, as % of bf16 TC peak / HBM peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DECODE_SPLITS = 4
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def shard(n_units: int, rank: int, world: int) -> range:
+    """Contiguous share of n_units for this rank (used when a workload is split over ranks)."""
+    base, extra = divmod(n_units, world)
+    start = rank * base + min(rank, extra)
+    return range(start, start + base + (1 if rank < extra else 0))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        exe = shutil.which("nvidia-smi")
+        if exe:
+            self.proc = subprocess.Popen(
+                [exe, "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_record(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except Exception:
+        return None
+    if not rec:
+        return None
+    from attention_attn_prefill_gb300.build import CSRC
+    import hashlib
+    h = hashlib.sha256()
+    for name in rec.get("sources", []):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return rec["bytes_per_launch"] if h.hexdigest() == rec.get("sha256") else None
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from attention_attn_prefill_gb300.build import build
+    build()
+    import attention_attn_prefill_gb300 as attn
+
+    peaks, peak_src = load_peaks()
+    cfg = LLAMA8B
+    x = prefill_inputs_for(cfg)
+    q, k, v = (t.to(dev) for t in (x.q, x.k, x.v))
+    o = torch.empty_like(q)
+    lse = torch.empty((cfg.B, cfg.Hq, cfg.S), dtype=torch.float32, device=dev)
+
+    dcfg = PAGED
+    lens = decode_lens_for(dcfg)
+    dx = decode_inputs_for(dcfg)
+    dq, kc, vc, bt, sl = (t.to(dev) for t in (dx.q, dx.k_cache, dx.v_cache, dx.block_table, dx.seq_lens))
+    do = torch.empty_like(dq)
+    dl = torch.empty((dcfg.N, dcfg.Hq), dtype=torch.float32, device=dev)
+    slots = attn.decode_num_slots(dx.max_blocks, num_splits=args.decode_splits)
+    ws = torch.empty(max(1, attn.decode_workspace_bytes(dcfg.N, dcfg.Hq, dcfg.d, slots)), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def prefill():
+        attn.prefill(q, k, v, scale=cfg.scale, causal=True, out=o, lse=lse, stream=stream)
+
+    def decode():
+        attn.decode_paged(dq, kc, vc, bt, sl, scale=dcfg.scale, num_splits=args.decode_splits, out=do, lse=dl,
+                          workspace=ws, stream=stream)
+
+    def step(record):
+        flush.zero_()
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        prefill()
+        e1.record(stream)
+        decode()
+        e2.record(stream)
+        record.append((e0, e1, e2))
+
+    warm = []
+    for _ in range(args.warmup):
+        step(warm)
+    torch.cuda.synchronize()
+    assert attn.device_status(clear=True) == 0
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    rec = []
+    with ClockSampler(local) as clocks:
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step(rec)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    pre_ms = [a.elapsed_time(b) for a, b, _ in rec]
+    dec_ms = [b.elapsed_time(c) for _, b, c in rec]
+    pre_mean, dec_mean = statistics.mean(pre_ms), statistics.mean(dec_ms)
+    step_ms = pre_mean + dec_mean
+    if world > 1:
+        t = torch.tensor([pre_mean, dec_mean, step_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        pre_mean, dec_mean, step_ms = t.tolist()
+
+    flops = cfg.causal_flops
+    tflops = world * flops / (pre_mean * 1e-3) / 1e12
+    dbytes = decode_min_bytes(lens, dcfg.Hq, dcfg.Hkv, dcfg.d)
+    gbs = world * dbytes / (dec_mean * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers (prefill metric)
+    hq, hk, hv = (t.pin_memory() for t in (x.q, x.k, x.v))
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        prefill()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = t.item()
+    e2e_tflops = world * flops / (e2e_ms * 1e-3) / 1e12
+    status = attn.device_status(clear=True)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    achieved = flops / (statistics.mean(pre_ms) * 1e-3) / 1e12
+    peak_tc = peaks["bf16_tflops"]
+    dec_achieved = dbytes / (statistics.mean(dec_ms) * 1e-3) / 1e9
+    launches_per_step = 1 + 1 + (1 if slots > 1 else 0)
+    line = {
+        "metric": METRIC,
+        "value": round(tflops, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16; shapes of the pages' workloads)",
+        "config": {
+            "workload": "causal prefill B=1 Hq=32 Hkv=8 S=2048 d=128 + paged decode N=64 len~U[512,8192] "
+                        f"Hq=32 Hkv=8 d=128 num_splits={args.decode_splits}",
+            "prefill": {"B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "S": cfg.S, "d": cfg.d, "causal": True,
+                        "seed": cfg.seed, "flops_per_step": flops},
+            "decode": {"N": dcfg.N, "Hq": dcfg.Hq, "Hkv": dcfg.Hkv, "d": dcfg.d, "page": 16,
+                       "num_splits": args.decode_splits, "slots": slots, "sum_len": int(sum(lens)),
+                       "seed": dcfg.seed, "bytes_per_step": dbytes},
+            "l2": "flushed between steps (256 MiB write, outside the timed events)",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "tensor", "kernel": "prefill_fwd_kernel<128>", "achieved": round(achieved, 2),
+            "peak": peak_tc, "unit": "TFLOP/s", "frac": round(achieved / peak_tc, 4),
+            "peak_source": f"{peak_src} bf16 dense (burst)", "traffic": traffic_record("prefill_fwd_kernel<128>"),
+            "algorithmic_bytes": cfg.min_bytes,
+        },
+        "decode": {
+            "value": round(gbs, 1), "unit": "GB/s", "ms": round(dec_mean, 4),
+            "roofline": {"bound": "hbm", "kernel": "decode_split_kernel<128,4,3> + combine_kernel<128>",
+                         "achieved": round(dec_achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(dec_achieved / peaks["hbm_gbs"], 4),
+                         "frac_of_8tbs": round(dec_achieved / 8000.0, 4),
+                         "peak_source": f"{peak_src} HBM copy",
+                         "traffic": traffic_record("decode_split_kernel<128,4,3>")},
+        },
+        "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms": round(e2e_ms, 4)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+        "wall_s_timed": round(wall, 3),
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+
+def oracle_prefill_sample(heads: int):
+    """Time the float64 oracle on `heads` query heads of the prefill workload (all rows)."""
+    import oracle.attention as oa
+    cfg = LLAMA8B
+    x = prefill_inputs_for(cfg)
+    t0 = time.perf_counter()
+    oa.prefill(x.q, x.k, x.v, cfg.scale, causal=True, heads=range(heads))
+    dt = time.perf_counter() - t0
+    flops = cfg.causal_flops * heads / cfg.Hq
+    return flops / dt / 1e12, dt, flops
+
+
+def cpu_baseline(min_seconds: float):
+    """Oracle on whole query heads of the prefill workload, repeated until about min_seconds of work."""
+    import oracle.attention as oa
+    cfg = LLAMA8B
+    x = prefill_inputs_for(cfg)
+    heads, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < min_seconds and heads < 4 * cfg.Hq:
+        oa.prefill(x.q, x.k, x.v, cfg.scale, causal=True, heads=[heads % cfg.Hq])
+        heads += 1
+    dt = time.perf_counter() - t0
+    flops = cfg.causal_flops * heads / cfg.Hq
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"float64 numpy oracle, causal prefill B=1 S=2048 d=128: {heads} query-head passes "
+                      f"(all 2048 rows each) in {dt:.2f} s, {flops / 1e9:.1f} GFLOP counted causally; "
+                      "numpy BLAS threads = host cores"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_prefill_sample(1)
+    vals, times = [], []
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        tf, dt, _ = oracle_prefill_sample(args.ref_heads)
+        vals.append(tf)
+        times.append(dt)
+    total = time.perf_counter() - t_all
+    value = args.steps * LLAMA8B.causal_flops * args.ref_heads / LLAMA8B.Hq / total / 1e12
+    line = {
+        "metric": METRIC, "impl": "reference", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16 inputs widened to float64)",
+        "config": {"workload": "causal prefill B=1 Hq=32 Hkv=8 S=2048 d=128 (sample of query heads per step)",
+                   "heads_per_step": args.ref_heads},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{args.ref_heads} of 32 query heads per step, all 2048 rows"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_case(args):
+    """One kernel family on one named workload, for profiling: prints a short JSON line.
+
+    prefill:<name>            name in {tiny, llama8b_prefill, sweep_s1024, sweep_s2048, sweep_s4096}
+    decode:<name>:<splits>    name in {paged_decode, longctx_decode}; splits = num_splits,
+                              or t<N> for split_tokens = N
+    """
+    from workloads import DECODE_CONFIGS, PREFILL_CONFIGS
+    from attention_attn_prefill_gb300.build import build
+    build()
+    import attention_attn_prefill_gb300 as attn
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    kind, name, *rest = args.case.split(":")
+    if kind == "prefill":
+        cfg = {c.name: c for c in PREFILL_CONFIGS}[name]
+        x = prefill_inputs_for(cfg)
+        q, k, v = (t.to(dev) for t in (x.q, x.k, x.v))
+        o = torch.empty_like(q)
+        lse = torch.empty((cfg.B, cfg.Hq, cfg.S), dtype=torch.float32, device=dev)
+        work, unit = cfg.causal_flops / 1e12, "TFLOP/s"
+
+        def launch():
+            attn.prefill(q, k, v, scale=cfg.scale, causal=True, out=o, lse=lse, stream=stream)
+    else:
+        cfg = {c.name: c for c in DECODE_CONFIGS}[name]
+        spec = rest[0] if rest else "1"
+        kw = dict(split_tokens=int(spec[1:])) if spec.startswith("t") else dict(num_splits=int(spec))
+        lens = decode_lens_for(cfg)
+        x = decode_inputs_for(cfg)
+        dq, kc, vc, bt, sl = (t.to(dev) for t in (x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens))
+        do = torch.empty_like(dq)
+        dl = torch.empty((cfg.N, cfg.Hq), dtype=torch.float32, device=dev)
+        slots = attn.decode_num_slots(x.max_blocks, **kw)
+        ws = torch.empty(max(1, attn.decode_workspace_bytes(cfg.N, cfg.Hq, cfg.d, slots)), dtype=torch.uint8,
+                         device=dev)
+        work, unit = decode_min_bytes(lens, cfg.Hq, cfg.Hkv, cfg.d) / 1e9, "GB/s"
+
+        def launch():
+            attn.decode_paged(dq, kc, vc, bt, sl, scale=cfg.scale, out=do, lse=dl, workspace=ws, stream=stream,
+                              **kw)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        launch()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        launch()
+        b.record(stream)
+        ms.append((a, b))
+    torch.cuda.synchronize()
+    t = [a.elapsed_time(b) for a, b in ms]
+    status = attn.device_status(clear=True)
+    print(json.dumps({"case": args.case, "ms_mean": statistics.mean(t), "ms_min": min(t),
+                      "value": work / (statistics.mean(t) * 1e-3), "best": work / (min(t) * 1e-3), "unit": unit,
+                      "device_status": status}), flush=True)
+    if status:
+        sys.exit(3)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--decode-splits", type=int, default=DECODE_SPLITS)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-heads", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default="", help="profile one kernel on one workload (see run_case)")
+    args = ap.parse_args()
+    if args.case:
+        return run_case(args)
+    args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
