@@ -7,21 +7,31 @@
 //
 // How (the tiled flow of "Streaming process -- How the SM works inside a
 // transformer", Steps 3-8 and its code snippet, redesigned for tcgen05):
-//   * one CTA owns two 128-row Q tiles of one (batch, query head); TMA loads
-//     each Q tile once (Step 3);
-//   * a producer warp streams 128-key K and V tiles through a two-stage
-//     shared-memory ring with mbarrier full/empty pairs (Step 6);
-//   * one thread of the MMA warp issues S = Q K^T into TMEM (Step 4) and, once
-//     softmax has written P, O += P V with P read straight from TMEM (Step 7);
-//   * eight softmax warps (one thread per query row, one warpgroup per Q tile)
-//     read S from TMEM, mask, take the running max, exponentiate with ex2 and
-//     keep the running sum (Step 5); O is rescaled only when the max has grown
-//     by more than 2^8 since it was last applied (exact either way, because
-//     O and l always share the same reference max);
-//   * the epilogue divides by l, rounds to bf16, stages the tile in shared
-//     memory and stores it with TMA; LSE = m*scale + ln(l) (Step 8).
-// The two Q tiles ping-pong: while one warpgroup runs softmax on its S, the
-// tensor core works on the other tile's S or P.V.
+//   * one CTA owns one 128-row Q tile of one (batch, query head); TMA loads it
+//     once (Step 3);
+//   * two producer threads stream 128-key K and V tiles through shared-memory
+//     rings (two K stages, three V stages) with mbarrier full/empty pairs
+//     (Step 6);
+//   * one thread issues S_j = Q K_j^T into TMEM (Step 4).  S is triple-buffered
+//     in TMEM, so the tensor core computes S two steps ahead of softmax.  A
+//     second thread, in another warp, issues O += P_j V_j with P (bf16, over
+//     the first 64 columns of S_j's buffer) read straight from TMEM once
+//     softmax has written it (Step 7).  tcgen05.mma blocks its issuing thread
+//     while the tensor core's queue is full, so two issuers let one of them
+//     wait on a barrier while the other keeps the queue fed;
+//   * eight softmax warps share every row: warpgroup h takes key columns
+//     64h..64h+63.  Each thread reads its 64 scores from TMEM, masks, takes the
+//     row max (the two halves of a row exchange theirs through shared memory),
+//     exponentiates with ex2 and keeps its share of the running sum (Step 5).
+//     O is rescaled only when the row max has grown by more than 2^8 since it
+//     was last applied -- exact either way, because O and l always refer to
+//     the same max;
+//   * the epilogue adds the two halves of l, divides, rounds to bf16, stages
+//     the tile in shared memory (128B swizzle) and stores it with TMA; LSE =
+//     m*scale + ln(l) (Step 8).
+// The per-step critical path is max(softmax, P.V + S on the tensor core):
+// softmax of step j never waits for the tensor core, because S_j was issued
+// two P.V products earlier.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -37,14 +47,17 @@ __device__ uint32_t g_prefill_status;
 
 namespace {
 
-constexpr int BM = 128;          // query rows per Q tile (TMEM lanes)
+constexpr int BM = 128;          // query rows per CTA (TMEM lanes)
 constexpr int BN = 128;          // keys per K/V tile
-constexpr int NQT = 2;           // Q tiles per CTA
-constexpr int KV_STAGES = 2;
-constexpr int NUM_THREADS = 320; // 8 softmax warps, 1 TMA warp, 1 MMA warp
+constexpr int NSB = 3;           // S buffers in TMEM
+constexpr int K_STAGES = 2;       // K_j is free as soon as S_j is done, long before it is reloaded
+constexpr int V_STAGES = 3;       // V_j is held until P_j V_j is done
+constexpr int NUM_THREADS = 352; // 8 softmax warps, 1 TMA warp, 2 MMA warps
 constexpr int PRODUCER_WARP = 8;
-constexpr int MMA_WARP = 9;
+constexpr int MMA_WARP = 9;      // issues S = Q K^T, owns the TMEM allocation
+constexpr int PV_WARP = 10;      // issues O += P V
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t O_COL = NSB * 128;  // O accumulator columns start here
 constexpr float RESCALE_LOG2_THRESHOLD = 8.0f;
 constexpr int CHUNK_BYTES = 128 * 128;   // 128 rows x 128 B (64 bf16): one 128B-swizzle panel
 
@@ -53,14 +66,17 @@ struct Layout {
   static constexpr int CHUNKS = D / 64;
   static constexpr int TILE_BYTES = 128 * D * 2;
   static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + NQT * TILE_BYTES;
-  static constexpr int V_OFF = K_OFF + KV_STAGES * TILE_BYTES;
-  static constexpr int BAR_OFF = V_OFF + KV_STAGES * TILE_BYTES;
-  static constexpr int NUM_BARS = 17;
+  static constexpr int K_OFF = Q_OFF + TILE_BYTES;
+  static constexpr int V_OFF = K_OFF + K_STAGES * TILE_BYTES;
+  static constexpr int RED_OFF = V_OFF + V_STAGES * TILE_BYTES;  // row-max exchange [2 steps][2 halves][128]
+  static constexpr int BAR_OFF = RED_OFF + 2 * 2 * 128 * 4;
+  // q_full, k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[3], p_full[3], pv_done[3], o_full, mma_done[2]
+  static constexpr int NUM_BARS = 1 + 7 * 3 + 3;
   static constexpr int SLOT_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int USED = SLOT_OFF + 16;
-  // + 1 KB for aligning the base; never below ~114 KB so that one CTA holds an SM
+  // + 1 KB for aligning the base; never below ~114 KB, so one CTA (and its 512 TMEM columns) holds an SM
   static constexpr int ALLOC = (USED + 1024) > 116 * 1024 ? (USED + 1024) : 116 * 1024;
+  static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -78,45 +94,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* sQ = smem + L::Q_OFF;
   uint8_t* sK = smem + L::K_OFF;
   uint8_t* sV = smem + L::V_OFF;
+  float* red = reinterpret_cast<float*>(smem + L::RED_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 2;
+  uint64_t* k_full = bars + 1;
   uint64_t* k_empty = bars + 4;
-  uint64_t* v_full = bars + 6;
-  uint64_t* v_empty = bars + 8;
-  uint64_t* s_full = bars + 10;
-  uint64_t* p_full = bars + 12;
-  uint64_t* o_full = bars + 14;
-  uint64_t* mma_done = bars + 16;
+  uint64_t* v_full = bars + 7;
+  uint64_t* v_empty = bars + 10;
+  uint64_t* s_full = bars + 13;
+  uint64_t* p_full = bars + 16;
+  uint64_t* pv_done = bars + 19;   // [3]: P_j V_j done, per S buffer
+  uint64_t* o_full = bars + 22;
+  uint64_t* mma_done = bars + 23;  // [2]: each issuer's last MMA done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::SLOT_OFF);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int hq = blockIdx.x;
-  const int qb = p.num_qblocks - 1 - static_cast<int>(blockIdx.y);  // longest causal rows first
+  const int qt = p.num_qblocks - 1 - static_cast<int>(blockIdx.y);  // longest causal rows first
   const int b = blockIdx.z;
   const int g = hq / (p.Hq / p.Hkv);
-  const int q0 = qb * (NQT * BM);
-  const int ntiles = (q0 + BM < p.S) ? 2 : 1;
-  int nkv[NQT];
-#pragma unroll
-  for (int t = 0; t < NQT; ++t) nkv[t] = p.causal ? ((q0 + t * BM) / BN + 1) : p.n_kv_total;
-  const int nkv_max = nkv[ntiles - 1];
+  const int q0 = qt * BM;
+  const int nkv = p.causal ? (qt + 1) : p.n_kv_total;  // KV tiles this Q tile visits
 
   if (threadIdx.x == 0) {
-    for (int t = 0; t < NQT; ++t) {
-      mbar_init(&q_full[t], 1);
-      mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], BM);
-      mbar_init(&o_full[t], 1);
-    }
-    for (int s = 0; s < KV_STAGES; ++s) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 3; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 256);
+      mbar_init(&pv_done[s], 1);
     }
-    mbar_init(mma_done, 1);
+    mbar_init(o_full, 1);
+    mbar_init(&mma_done[0], 1);
+    mbar_init(&mma_done[1], 1);
     fence_mbar_init();
   }
   if (warp == MMA_WARP) {
@@ -129,207 +143,236 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == PRODUCER_WARP) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      tma_prefetch_desc(&tm_o);
-      for (int t = 0; t < ntiles; ++t) {
-        mbar_arrive_expect_tx(&q_full[t], L::TILE_BYTES);
-        for (int c = 0; c < L::CHUNKS; ++c)
-          tma_load_3d(sQ + t * L::TILE_BYTES + c * CHUNK_BYTES, &tm_q, &q_full[t], hq * D + c * 64, q0 + t * BM, b);
+    // ------------------------------------------------------------ TMA producers
+    // Lane 0 loads Q and the K tiles, lane 1 the V tiles; each waits only on its own ring.
+    if (lane < 2) {
+      const bool is_k = lane == 0;
+      const int nst = is_k ? K_STAGES : V_STAGES;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      uint8_t* ring = is_k ? sK : sV;
+      const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+      if (is_k) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_o);
+        mbar_arrive_expect_tx(q_full, L::TILE_BYTES);
+        for (int c = 0; c < L::CHUNKS; ++c) tma_load_3d(sQ + c * CHUNK_BYTES, &tm_q, q_full, hq * D + c * 64, q0, b);
+      } else {
+        tma_prefetch_desc(&tm_v);
       }
-      int nk = 0, nv = 0;  // K and V tiles issued
-      for (int j = 0; j < nkv_max; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(&k_empty[st], ph ^ 1)) { set_error(&g_prefill_status, kDevWaitTimeout); break; }
-        mbar_arrive_expect_tx(&k_full[st], L::TILE_BYTES);
+      int issued = 0;
+      for (int j = 0; j < nkv; ++j) {
+        const int st = j % nst;
+        if (!mbar_wait(&empty[st], ((j / nst) & 1) ^ 1)) {
+          set_error(&g_prefill_status, kDevWaitTimeout);
+          break;
+        }
+        mbar_arrive_expect_tx(&full[st], L::TILE_BYTES);
         for (int c = 0; c < L::CHUNKS; ++c)
-          tma_load_3d(sK + st * L::TILE_BYTES + c * CHUNK_BYTES, &tm_k, &k_full[st], g * D + c * 64, j * BN, b);
-        nk = j + 1;
-        if (!mbar_wait(&v_empty[st], ph ^ 1)) { set_error(&g_prefill_status, kDevWaitTimeout); break; }
-        mbar_arrive_expect_tx(&v_full[st], L::TILE_BYTES);
-        for (int c = 0; c < L::CHUNKS; ++c)
-          tma_load_3d(sV + st * L::TILE_BYTES + c * CHUNK_BYTES, &tm_v, &v_full[st], g * D + c * 64, j * BN, b);
-        nv = j + 1;
+          tma_load_3d(ring + st * L::TILE_BYTES + c * CHUNK_BYTES, map, &full[st], g * D + c * 64, j * BN, b);
+        issued = j + 1;
       }
-      // Drain: every copy this warp started must have landed before the CTA exits.
-      // The last KV_STAGES copies are the newest in their stages, so their phases are current.
-      for (int j = (nk > KV_STAGES ? nk - KV_STAGES : 0); j < nk; ++j) mbar_wait(&k_full[j & 1], (j >> 1) & 1);
-      for (int j = (nv > KV_STAGES ? nv - KV_STAGES : 0); j < nv; ++j) mbar_wait(&v_full[j & 1], (j >> 1) & 1);
-      for (int t = 0; t < ntiles; ++t) mbar_wait(&q_full[t], 0);
+      // Drain: every copy started here must have landed before the CTA exits.  The newest
+      // copy of each stage is the one whose phase is current.
+      for (int j = (issued > nst ? issued - nst : 0); j < issued; ++j) mbar_wait(&full[j % nst], (j / nst) & 1);
+      if (is_k) mbar_wait(q_full, 0);
     }
   } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ MMA issue
+    // ------------------------------------------------------------ S = Q K^T issue
+    // S_j goes to TMEM buffer j % 3, which held P_{j-3}: wait until P_{j-3} V_{j-3} is done.
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0);   // Q (K-major) x K (K-major)
-      constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 1);    // P (TMEM)   x V (MN-major)
-      bool ok = true;
-      for (int t = 0; t < ntiles && ok; ++t) ok = mbar_wait(&q_full[t], 0);
-      tc_fence_after();
-      for (int j = 0; ok && j <= nkv_max; ++j) {
-        for (int t = 0; t < ntiles; ++t) {
-          const uint32_t s_tmem = tmem + t * 256;
-          const uint32_t o_tmem = tmem + t * 256 + 128;
-          if (j >= 1 && j - 1 < nkv[t]) {
-            // O_t += P_t(j-1) V(j-1)
-            const int jj = j - 1;
-            const int st = jj & 1;
-            if (!mbar_wait(&p_full[t], jj & 1) || !mbar_wait(&v_full[st], (jj >> 1) & 1)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t vbase = smem_u32(sV + st * L::TILE_BYTES);
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              // 16 keys = two 8-row swizzle atoms; d panels are BN*128 bytes apart
-              const uint64_t bdesc = smem_desc_sw128(vbase + kk * 16 * 128, BN * 128, 1024);
-              umma_ts(o_tmem, s_tmem + kk * 8, bdesc, IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
-            }
-            if (jj == nkv[t] - 1) umma_commit(&o_full[t]);
-            if (t == ntiles - 1) umma_commit(&v_empty[st]);
-          }
-          if (j < nkv[t]) {
-            // S_t(j) = Q_t K(j)^T
-            const int st = j & 1;
-            if (!mbar_wait(&k_full[st], (j >> 1) & 1)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t qbase = smem_u32(sQ + t * L::TILE_BYTES);
-            const uint32_t kbase = smem_u32(sK + st * L::TILE_BYTES);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t koff = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
-              const uint64_t adesc = smem_desc_sw128(qbase + koff, 16, 1024);
-              const uint64_t bdesc = smem_desc_sw128(kbase + koff, 16, 1024);
-              umma_ss(s_tmem, adesc, bdesc, IDESC_S, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(&s_full[t]);
-            if (t == ntiles - 1) umma_commit(&k_empty[st]);
-          }
+      const uint32_t qbase = smem_u32(sQ);
+      bool ok = mbar_wait(q_full, 0);
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int sb = j % NSB;
+        const int st = j % K_STAGES;
+        if ((j >= NSB && !mbar_wait(&pv_done[sb], ((j - NSB) / NSB) & 1)) ||
+            !mbar_wait(&k_full[st], (j / K_STAGES) & 1)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        const uint32_t kbase = smem_u32(sK + st * L::TILE_BYTES);
+        const uint32_t s_tmem = tmem + sb * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
+          umma_ss(s_tmem, smem_desc_sw128(qbase + koff, 16, 1024), smem_desc_sw128(kbase + koff, 16, 1024), IDESC_S,
+                  kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[sb]);
+        umma_commit(&k_empty[st]);
       }
       if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
-      umma_commit(mma_done);
-      if (!mbar_wait(mma_done, 0)) set_error(&g_prefill_status, kDevWaitTimeout);
+      umma_commit(&mma_done[0]);
+      if (!mbar_wait(&mma_done[0], 0)) set_error(&g_prefill_status, kDevWaitTimeout);
+    }
+  } else if (warp == PV_WARP) {
+    // ------------------------------------------------------------ O += P V issue
+    if (lane == 0) {
+      constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 1);    // P (TMEM) x V (MN-major)
+      const uint32_t o_tmem = tmem + O_COL;
+      bool ok = true;
+      for (int j = 0; j < nkv; ++j) {
+        const int sb = j % NSB;
+        const int st = j % V_STAGES;
+        if (!mbar_wait(&p_full[sb], (j / NSB) & 1) || !mbar_wait(&v_full[st], (j / V_STAGES) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t vbase = smem_u32(sV + st * L::TILE_BYTES);
+        const uint32_t p_tmem = tmem + sb * 128;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          // 16 keys = two 8-row swizzle atoms; d panels are BN*128 bytes apart
+          umma_ts(o_tmem, p_tmem + kk * 8, smem_desc_sw128(vbase + kk * 16 * 128, BN * 128, 1024), IDESC_O,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&pv_done[sb]);
+        umma_commit(&v_empty[st]);
+        if (j == nkv - 1) umma_commit(o_full);
+      }
+      if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
+      umma_commit(&mma_done[1]);
+      if (!mbar_wait(&mma_done[1], 0)) set_error(&g_prefill_status, kDevWaitTimeout);
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int t = warp >> 2;
-    if (t < ntiles) {
-      const int row = (warp & 3) * 32 + lane;
-      const int q = q0 + t * BM + row;
-      const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-      const uint32_t s_tmem = tmem + lane_base + t * 256;
-      const uint32_t o_tmem = s_tmem + 128;
-      const float c2 = p.scale_log2;
-      float m_used = -FLT_MAX;  // raw-score max the current O and l refer to
-      float l = 0.f;
-      bool ok = true;
-      for (int j = 0; j < nkv[t]; ++j) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1));
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(s_tmem + c4 * 32, sr[c4]);
-        tmem_ld_wait();
-        const bool need_mask = (p.causal && j == nkv[t] - 1) || (j == p.n_kv_total - 1 && (p.S % BN) != 0);
-        if (need_mask) {
-          const int key0 = j * BN;
-#pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const int key = key0 + c;
-            if ((p.causal && key > q) || key >= p.S) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
-          }
-        }
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          mx0 = fmaxf(mx0, __uint_as_float(sr[0][c]));
-          mx1 = fmaxf(mx1, __uint_as_float(sr[1][c]));
-          mx2 = fmaxf(mx2, __uint_as_float(sr[2][c]));
-          mx3 = fmaxf(mx3, __uint_as_float(sr[3][c]));
-        }
-        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-        float alpha = 1.f;
-        bool rescale_o = false;
-        if (j == 0) {
-          m_used = mx;
-        } else if ((mx - m_used) * c2 > RESCALE_LOG2_THRESHOLD) {
-          alpha = ex2_approx((m_used - mx) * c2);
-          l *= alpha;
-          rescale_o = true;
-          m_used = mx;
-        }
-        const float mb = (m_used == -INFINITY) ? 0.f : m_used * c2;
-        float rs0 = 0.f, rs1 = 0.f;
-        uint32_t pk[2][32];
+    const int h = warp >> 2;                  // which half of the key columns / of O
+    const int row = (warp & 3) * 32 + lane;   // TMEM lane = query row within the tile
+    const int q = q0 + row;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t o_half = tmem + lane_base + O_COL + h * (D / 2);
+    const float c2 = p.scale_log2;
+    const uint64_t c2x2 = f2_pack(c2, c2);
+    float m_used = -INFINITY;  // raw-score max that O and l currently refer to
+    float l_part = 0.f;        // this half's share of the row sum
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int sb = j % NSB;
+      const uint32_t s_tmem = tmem + lane_base + sb * 128;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j / NSB) & 1));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[2][32];
+      tmem_ld32(s_tmem + h * 64, sr[0]);
+      tmem_ld32(s_tmem + h * 64 + 32, sr[1]);
+      tmem_ld_wait();
+      const bool need_mask = (p.causal && j == nkv - 1) || (j == p.n_kv_total - 1 && (p.S % BN) != 0);
+      if (need_mask) {
+        const int key0 = j * BN + h * 64;
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          const float x0 = __uint_as_float(sr[(2 * c) >> 5][(2 * c) & 31]);
-          const float x1 = __uint_as_float(sr[(2 * c + 1) >> 5][(2 * c + 1) & 31]);
-          const float p0 = ex2_approx(fmaf(x0, c2, -mb));
-          const float p1 = ex2_approx(fmaf(x1, c2, -mb));
-          rs0 += p0;
-          rs1 += p1;
-          pk[c >> 5][c & 31] = pack_bf16x2(p0, p1);
+          const int key = key0 + c;
+          if ((p.causal && key > q) || key >= p.S) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
         }
-        l += rs0 + rs1;
-        // P (bf16, two per column) overwrites the first 64 columns of S
-        tmem_st32(s_tmem, pk[0]);
-        tmem_st32(s_tmem + 32, pk[1]);
-        if (__any_sync(0xffffffffu, rescale_o)) {
-          // P.V of the previous tile has completed: S of this tile was issued after it.
-#pragma unroll 1
-          for (int c4 = 0; c4 < D / 32; ++c4) {
-            uint32_t r[32];
-            tmem_ld32(o_tmem + c4 * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-            tmem_st32(o_tmem + c4 * 32, r);
-          }
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&p_full[t]);
       }
-      // ---- epilogue: O / l -> bf16 -> smem (128B-swizzled, the Q tile's panels) -> TMA store
-      if (ok) ok = mbar_wait(&o_full[t], 0);
-      ok = __all_sync(0xffffffffu, ok);
-      uint8_t* stage = sQ + t * L::TILE_BYTES;
-      if (ok) {
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        mx0 = fmax3(mx0, __uint_as_float(sr[0][2 * c]), __uint_as_float(sr[0][2 * c + 1]));
+        mx1 = fmax3(mx1, __uint_as_float(sr[1][2 * c]), __uint_as_float(sr[1][2 * c + 1]));
+      }
+      // exchange the half-row maxima (both halves have read S, so P may overwrite it afterwards)
+      float* xr = red + (j & 1) * 256;
+      xr[h * 128 + row] = fmaxf(mx0, mx1);
+      named_barrier_sync(1, 256);
+      const float mx = fmaxf(xr[row], xr[128 + row]);
+      float alpha = 1.f;
+      bool rescale_o = false;
+      if (j == 0) {
+        m_used = mx;
+      } else if ((mx - m_used) * c2 > RESCALE_LOG2_THRESHOLD) {
+        alpha = ex2_approx((m_used - mx) * c2);
+        l_part *= alpha;
+        rescale_o = true;
+        m_used = mx;
+      }
+      const float mb = (m_used == -INFINITY) ? 0.f : m_used * c2;
+      const uint64_t nmb2 = f2_pack(-mb, -mb);
+      // p = 2^(s*scale*log2e - m*scale*log2e) in f32x2 pairs; P (bf16, two per column) goes to
+      // columns 32h..32h+31 of this S buffer
+      uint64_t acc0 = 0ull, acc1 = 0ull;
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int e = 2 * c;
+        const uint64_t xy = f2_fma(f2_pack(__uint_as_float(sr[e >> 5][e & 31]), __uint_as_float(sr[e >> 5][(e & 31) + 1])),
+                                   c2x2, nmb2);
+        float x0, x1;
+        f2_unpack(xy, x0, x1);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        if (c & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
+        else acc0 = f2_add(acc0, f2_pack(p0, p1));
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      {
+        float a0, a1;
+        f2_unpack(f2_add(acc0, acc1), a0, a1);
+        l_part += a0 + a1;
+      }
+      tmem_st32(s_tmem + h * 32, pk);
+      if (__any_sync(0xffffffffu, rescale_o)) {
+        // O must hold P_{j-1} V_{j-1} before it is rescaled
+        ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(j - 1) % NSB], ((j - 1) / NSB) & 1));
+        if (!ok) break;
         tc_fence_after();
-        const float inv_l = 1.f / l;
 #pragma unroll 1
-        for (int c4 = 0; c4 < D / 32; ++c4) {
+        for (int c4 = 0; c4 < D / 64; ++c4) {
           uint32_t r[32];
-          tmem_ld32(o_tmem + c4 * 32, r);
+          tmem_ld32(o_half + c4 * 32, r);
           tmem_ld_wait();
-          uint8_t* panel = stage + (c4 >> 1) * CHUNK_BYTES + row * 128;
-          const int u0 = (c4 & 1) * 4;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(r[8 * u + 0]) * inv_l, __uint_as_float(r[8 * u + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(r[8 * u + 2]) * inv_l, __uint_as_float(r[8 * u + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(r[8 * u + 4]) * inv_l, __uint_as_float(r[8 * u + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(r[8 * u + 6]) * inv_l, __uint_as_float(r[8 * u + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(panel + (((u0 + u) ^ (row & 7)) << 4)) = w;
-          }
+          for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+          tmem_st32(o_half + c4 * 32, r);
         }
-        if (p.lse != nullptr && q < p.S)
-          p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.S + q] = m_used * p.scale + logf(l);
-        fence_proxy_async_smem();
-      } else {
-        set_error(&g_prefill_status, kDevWaitTimeout);
       }
-      named_barrier_sync(1 + t, BM);
-      if (ok && row == 0) {
-        for (int c = 0; c < L::CHUNKS; ++c) tma_store_3d(&tm_o, stage + c * CHUNK_BYTES, hq * D + c * 64, q0 + t * BM, b);
-        tma_store_commit();
-        tma_store_wait0();
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full[sb]);
+    }
+    // ---- epilogue: l = both halves; O / l -> bf16 -> smem (the Q tile's 128B-swizzled panels) -> TMA
+    if (ok) ok = mbar_wait(o_full, 0);
+    ok = __all_sync(0xffffffffu, ok);
+    red[256 + h * 128 + row] = l_part;   // the exchange buffer of odd steps is idle by now
+    named_barrier_sync(1, 256);
+    const float l = red[256 + row] + red[384 + row];
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+#pragma unroll 1
+      for (int c4 = 0; c4 < D / 64; ++c4) {
+        uint32_t r[32];
+        tmem_ld32(o_half + c4 * 32, r);
+        tmem_ld_wait();
+        const int col0 = h * (D / 2) + c4 * 32;   // first output column of this chunk
+        uint8_t* panel = sQ + (col0 >> 6) * CHUNK_BYTES + row * 128;
+        const int u0 = (col0 & 63) >> 3;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(r[8 * u + 0]) * inv_l, __uint_as_float(r[8 * u + 1]) * inv_l);
+          w.y = pack_bf16x2(__uint_as_float(r[8 * u + 2]) * inv_l, __uint_as_float(r[8 * u + 3]) * inv_l);
+          w.z = pack_bf16x2(__uint_as_float(r[8 * u + 4]) * inv_l, __uint_as_float(r[8 * u + 5]) * inv_l);
+          w.w = pack_bf16x2(__uint_as_float(r[8 * u + 6]) * inv_l, __uint_as_float(r[8 * u + 7]) * inv_l);
+          *reinterpret_cast<uint4*>(panel + (((u0 + u) ^ (row & 7)) << 4)) = w;
+        }
       }
+      if (h == 0 && p.lse != nullptr && q < p.S)
+        p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.S + q] = m_used * p.scale + logf(l);
+      fence_proxy_async_smem();
+    } else {
+      set_error(&g_prefill_status, kDevWaitTimeout);
+    }
+    named_barrier_sync(1, 256);
+    if (ok && threadIdx.x == 0) {
+      for (int c = 0; c < L::CHUNKS; ++c) tma_store_3d(&tm_o, sQ + c * CHUNK_BYTES, hq * D + c * 64, q0, b);
+      tma_store_commit();
+      tma_store_wait0();
     }
   }
 
@@ -355,7 +398,7 @@ cudaError_t launch(const PrefillMaps& m, const PrefillParams& p, cudaStream_t st
 
 }  // namespace
 
-int prefill_rows_per_cta() { return NQT * BM; }
+int prefill_rows_per_cta() { return BM; }
 int prefill_tile_rows() { return BM; }
 
 cudaError_t prefill_launch(int d, const PrefillMaps& maps, const PrefillParams& p, cudaStream_t stream) {
