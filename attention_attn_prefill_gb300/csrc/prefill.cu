@@ -7,11 +7,12 @@
 //
 // How (the tiled flow of "Streaming process -- How the SM works inside a
 // transformer", Steps 3-8 and its code snippet, redesigned for tcgen05):
-//   * one CTA owns one 128-row Q tile of one (batch, query head); TMA loads it
-//     once (Step 3);
-//   * two producer threads stream 128-key K and V tiles through shared-memory
-//     rings (two K stages, three V stages) with mbarrier full/empty pairs
-//     (Step 6);
+//   * the kernel is persistent: one CTA per SM walks a list of work tiles
+//     (one 128-row Q tile of one (batch, query head) each), longest causal
+//     tiles first, and keeps its pipelines running across tile boundaries;
+//   * two producer threads stream Q (once per tile, Step 3) and 128-key K and
+//     V tiles through shared-memory rings (two K stages, three V stages) with
+//     mbarrier full/empty pairs (Step 6);
 //   * one thread issues S_j = Q K_j^T into TMEM (Step 4).  S is triple-buffered
 //     in TMEM, so the tensor core computes S two steps ahead of softmax.  A
 //     second thread, in another warp, issues O += P_j V_j with P (bf16, over
@@ -27,11 +28,8 @@
 //     was last applied -- exact either way, because O and l always refer to
 //     the same max;
 //   * the epilogue adds the two halves of l, divides, rounds to bf16, stages
-//     the tile in shared memory (128B swizzle) and stores it with TMA; LSE =
-//     m*scale + ln(l) (Step 8).
-// The per-step critical path is max(softmax, P.V + S on the tensor core):
-// softmax of step j never waits for the tensor core, because S_j was issued
-// two P.V products earlier.
+//     the tile in shared memory (128B swizzle) and stores it with TMA while
+//     the next tile starts; LSE = m*scale + ln(l) (Step 8).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -47,11 +45,11 @@ __device__ uint32_t g_prefill_status;
 
 namespace {
 
-constexpr int BM = 128;          // query rows per CTA (TMEM lanes)
+constexpr int BM = 128;          // query rows per work tile (TMEM lanes)
 constexpr int BN = 128;          // keys per K/V tile
 constexpr int NSB = 3;           // S buffers in TMEM
-constexpr int K_STAGES = 2;       // K_j is free as soon as S_j is done, long before it is reloaded
-constexpr int V_STAGES = 3;       // V_j is held until P_j V_j is done
+constexpr int K_STAGES = 2;      // K_j is free as soon as S_j is done, long before it is reloaded
+constexpr int V_STAGES = 3;      // V_j is held until P_j V_j is done
 constexpr int NUM_THREADS = 352; // 8 softmax warps, 1 TMA warp, 2 MMA warps
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;      // issues S = Q K^T, owns the TMEM allocation
@@ -68,19 +66,32 @@ struct Layout {
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + TILE_BYTES;
   static constexpr int V_OFF = K_OFF + K_STAGES * TILE_BYTES;
-  static constexpr int RED_OFF = V_OFF + V_STAGES * TILE_BYTES;  // row-max exchange [2 steps][2 halves][128]
+  static constexpr int OST_OFF = V_OFF + V_STAGES * TILE_BYTES;   // output staging tile
+  static constexpr int RED_OFF = OST_OFF + TILE_BYTES;            // [2 buffers][2 halves][128] floats
   static constexpr int BAR_OFF = RED_OFF + 2 * 2 * 128 * 4;
-  // q_full, k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[3], p_full[3], pv_done[3], o_full, mma_done[2]
-  static constexpr int NUM_BARS = 1 + 7 * 3 + 3;
+  // q_full, q_empty, k_full[2], k_empty[2], v_full[3], v_empty[3], s_full[3], p_full[3], pv_done[3],
+  // o_full, o_free, mma_done[2]
+  static constexpr int NUM_BARS = 2 + 2 * 2 + 5 * 3 + 4;
   static constexpr int SLOT_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int USED = SLOT_OFF + 16;
-  // + 1 KB for aligning the base; never below ~114 KB, so one CTA (and its 512 TMEM columns) holds an SM
-  static constexpr int ALLOC = (USED + 1024) > 116 * 1024 ? (USED + 1024) : 116 * 1024;
+  // The dynamic shared memory window starts 1 KB-aligned (checked at run time); never below
+  // ~114 KB, so that one CTA (and its 512 TMEM columns) holds an SM.
+  static constexpr int ALLOC = USED > 116 * 1024 ? USED : 116 * 1024;
   static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+// Work tile number k of this CTA: a longest-first order dealt out in a zigzag over the CTAs.
+__device__ __forceinline__ bool tile_of(const PrefillParams& p, int k, int& b, int& hq, int& qt) {
+  const int G = gridDim.x;
+  const int c = blockIdx.x;
+  const int idx = k * G + ((k & 1) ? (G - 1 - c) : c);
+  const int per_qt = p.B * p.Hq;
+  if (idx >= p.num_qblocks * per_qt) return false;
+  qt = p.num_qblocks - 1 - idx / per_qt;
+  const int rem = idx % per_qt;
+  hq = rem % p.Hq;
+  b = rem / p.Hq;
+  return true;
 }
 
 template <int D>
@@ -89,39 +100,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                        const PrefillParams p) {
   using L = Layout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if ((smem_u32(smem) & 1023u) != 0) {  // 128B-swizzled tiles need 1 KB alignment
+    if (threadIdx.x == 0) set_error(&g_prefill_status, kDevMisaligned);
+    return;
+  }
   uint8_t* sQ = smem + L::Q_OFF;
   uint8_t* sK = smem + L::K_OFF;
   uint8_t* sV = smem + L::V_OFF;
+  uint8_t* sO = smem + L::OST_OFF;
   float* red = reinterpret_cast<float*>(smem + L::RED_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;
   uint64_t* k_empty = bars + 4;
-  uint64_t* v_full = bars + 7;
-  uint64_t* v_empty = bars + 10;
-  uint64_t* s_full = bars + 13;
-  uint64_t* p_full = bars + 16;
-  uint64_t* pv_done = bars + 19;   // [3]: P_j V_j done, per S buffer
-  uint64_t* o_full = bars + 22;
+  uint64_t* v_full = bars + 6;
+  uint64_t* v_empty = bars + 9;
+  uint64_t* s_full = bars + 12;
+  uint64_t* p_full = bars + 15;
+  uint64_t* pv_done = bars + 18;   // [3]: P_j V_j done, per S buffer
+  uint64_t* o_full = bars + 21;
+  uint64_t* o_free = bars + 22;    // the epilogue has read O out of TMEM
   uint64_t* mma_done = bars + 23;  // [2]: each issuer's last MMA done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::SLOT_OFF);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int hq = blockIdx.x;
-  const int qt = p.num_qblocks - 1 - static_cast<int>(blockIdx.y);  // longest causal rows first
-  const int b = blockIdx.z;
-  const int g = hq / (p.Hq / p.Hkv);
-  const int q0 = qt * BM;
-  const int nkv = p.causal ? (qt + 1) : p.n_kv_total;  // KV tiles this Q tile visits
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < 3; ++s) {
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < K_STAGES; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < 3; ++s) {
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
@@ -129,6 +143,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&pv_done[s], 1);
     }
     mbar_init(o_full, 1);
+    mbar_init(o_free, 256);
     mbar_init(&mma_done[0], 1);
     mbar_init(&mma_done[1], 1);
     fence_mbar_init();
@@ -141,10 +156,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int G = p.Hq / p.Hkv;
+  auto tile_nkv = [&](int qt) { return p.causal ? (qt + 1) : p.n_kv_total; };
 
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ TMA producers
     // Lane 0 loads Q and the K tiles, lane 1 the V tiles; each waits only on its own ring.
+    // Counters run across work tiles, so the rings never drain between tiles.
     if (lane < 2) {
       const bool is_k = lane == 0;
       const int nst = is_k ? K_STAGES : V_STAGES;
@@ -152,58 +170,74 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint64_t* empty = is_k ? k_empty : v_empty;
       uint8_t* ring = is_k ? sK : sV;
       const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+      tma_prefetch_desc(map);
       if (is_k) {
         tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_o);
-        mbar_arrive_expect_tx(q_full, L::TILE_BYTES);
-        for (int c = 0; c < L::CHUNKS; ++c) tma_load_3d(sQ + c * CHUNK_BYTES, &tm_q, q_full, hq * D + c * 64, q0, b);
-      } else {
-        tma_prefetch_desc(&tm_v);
       }
-      int issued = 0;
-      for (int j = 0; j < nkv; ++j) {
-        const int st = j % nst;
-        if (!mbar_wait(&empty[st], ((j / nst) & 1) ^ 1)) {
-          set_error(&g_prefill_status, kDevWaitTimeout);
-          break;
+      bool ok = true;
+      int issued = 0, nq = 0;
+      int b, hq, qt;
+      for (int k = 0; ok && tile_of(p, k, b, hq, qt); ++k) {
+        const int g = hq / G;
+        if (is_k) {
+          // Q of this tile replaces the previous one once all of its S = Q K^T products are done
+          if (k > 0 && !mbar_wait(q_empty, (k - 1) & 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(q_full, L::TILE_BYTES);
+          for (int c = 0; c < L::CHUNKS; ++c)
+            tma_load_3d(sQ + c * CHUNK_BYTES, &tm_q, q_full, hq * D + c * 64, qt * BM, b);
+          nq = k + 1;
         }
-        mbar_arrive_expect_tx(&full[st], L::TILE_BYTES);
-        for (int c = 0; c < L::CHUNKS; ++c)
-          tma_load_3d(ring + st * L::TILE_BYTES + c * CHUNK_BYTES, map, &full[st], g * D + c * 64, j * BN, b);
-        issued = j + 1;
+        const int nkv = tile_nkv(qt);
+        for (int j = 0; j < nkv; ++j) {
+          const int st = issued % nst;
+          if (!mbar_wait(&empty[st], ((issued / nst) & 1) ^ 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[st], L::TILE_BYTES);
+          for (int c = 0; c < L::CHUNKS; ++c)
+            tma_load_3d(ring + st * L::TILE_BYTES + c * CHUNK_BYTES, map, &full[st], g * D + c * 64, j * BN, b);
+          ++issued;
+        }
       }
+      if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
       // Drain: every copy started here must have landed before the CTA exits.  The newest
       // copy of each stage is the one whose phase is current.
-      for (int j = (issued > nst ? issued - nst : 0); j < issued; ++j) mbar_wait(&full[j % nst], (j / nst) & 1);
-      if (is_k) mbar_wait(q_full, 0);
+      for (int i = (issued > nst ? issued - nst : 0); i < issued; ++i) mbar_wait(&full[i % nst], (i / nst) & 1);
+      if (nq > 0) mbar_wait(q_full, (nq - 1) & 1);
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ S = Q K^T issue
-    // S_j goes to TMEM buffer j % 3, which held P_{j-3}: wait until P_{j-3} V_{j-3} is done.
+    // S of global step gs goes to TMEM buffer gs % 3, which held P of step gs - 3: wait until
+    // that P.V is done.
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0);   // Q (K-major) x K (K-major)
       const uint32_t qbase = smem_u32(sQ);
-      bool ok = mbar_wait(q_full, 0);
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int sb = j % NSB;
-        const int st = j % K_STAGES;
-        if ((j >= NSB && !mbar_wait(&pv_done[sb], ((j - NSB) / NSB) & 1)) ||
-            !mbar_wait(&k_full[st], (j / K_STAGES) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t kbase = smem_u32(sK + st * L::TILE_BYTES);
-        const uint32_t s_tmem = tmem + sb * 128;
+      bool ok = true;
+      int gs = 0;
+      int b, hq, qt;
+      for (int k = 0; ok && tile_of(p, k, b, hq, qt); ++k) {
+        if (!mbar_wait(q_full, k & 1)) { ok = false; break; }
+        const int nkv = tile_nkv(qt);
+        for (int j = 0; j < nkv; ++j, ++gs) {
+          const int sb = gs % NSB;
+          const int st = gs % K_STAGES;
+          if ((gs >= NSB && !mbar_wait(&pv_done[sb], ((gs - NSB) / NSB) & 1)) ||
+              !mbar_wait(&k_full[st], (gs / K_STAGES) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t kbase = smem_u32(sK + st * L::TILE_BYTES);
+          const uint32_t s_tmem = tmem + sb * 128;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
-          umma_ss(s_tmem, smem_desc_sw128(qbase + koff, 16, 1024), smem_desc_sw128(kbase + koff, 16, 1024), IDESC_S,
-                  kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
+            umma_ss(s_tmem, smem_desc_sw128(qbase + koff, 16, 1024), smem_desc_sw128(kbase + koff, 16, 1024),
+                    IDESC_S, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&s_full[sb]);
+          umma_commit(&k_empty[st]);
         }
-        umma_commit(&s_full[sb]);
-        umma_commit(&k_empty[st]);
+        umma_commit(q_empty);  // Q may be replaced once this tile's products are done
       }
       if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
       umma_commit(&mma_done[0]);
@@ -215,25 +249,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 1);    // P (TMEM) x V (MN-major)
       const uint32_t o_tmem = tmem + O_COL;
       bool ok = true;
-      for (int j = 0; j < nkv; ++j) {
-        const int sb = j % NSB;
-        const int st = j % V_STAGES;
-        if (!mbar_wait(&p_full[sb], (j / NSB) & 1) || !mbar_wait(&v_full[st], (j / V_STAGES) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t vbase = smem_u32(sV + st * L::TILE_BYTES);
-        const uint32_t p_tmem = tmem + sb * 128;
+      int gs = 0;
+      int b, hq, qt;
+      for (int k = 0; ok && tile_of(p, k, b, hq, qt); ++k) {
+        // the first product of a tile overwrites O: the previous tile's epilogue must have read it
+        if (k > 0 && !mbar_wait(o_free, (k - 1) & 1)) { ok = false; break; }
+        const int nkv = tile_nkv(qt);
+        for (int j = 0; j < nkv; ++j, ++gs) {
+          const int sb = gs % NSB;
+          const int st = gs % V_STAGES;
+          if (!mbar_wait(&p_full[sb], (gs / NSB) & 1) || !mbar_wait(&v_full[st], (gs / V_STAGES) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t vbase = smem_u32(sV + st * L::TILE_BYTES);
+          const uint32_t p_tmem = tmem + sb * 128;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // 16 keys = two 8-row swizzle atoms; d panels are BN*128 bytes apart
-          umma_ts(o_tmem, p_tmem + kk * 8, smem_desc_sw128(vbase + kk * 16 * 128, BN * 128, 1024), IDESC_O,
-                  (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            // 16 keys = two 8-row swizzle atoms; d panels are BN*128 bytes apart
+            umma_ts(o_tmem, p_tmem + kk * 8, smem_desc_sw128(vbase + kk * 16 * 128, BN * 128, 1024), IDESC_O,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&pv_done[sb]);
+          umma_commit(&v_empty[st]);
+          if (j == nkv - 1) umma_commit(o_full);
         }
-        umma_commit(&pv_done[sb]);
-        umma_commit(&v_empty[st]);
-        if (j == nkv - 1) umma_commit(o_full);
       }
       if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
       umma_commit(&mma_done[1]);
@@ -243,137 +284,148 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ softmax + epilogue
     const int h = warp >> 2;                  // which half of the key columns / of O
     const int row = (warp & 3) * 32 + lane;   // TMEM lane = query row within the tile
-    const int q = q0 + row;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t o_half = tmem + lane_base + O_COL + h * (D / 2);
     const float c2 = p.scale_log2;
     const uint64_t c2x2 = f2_pack(c2, c2);
-    float m_used = -INFINITY;  // raw-score max that O and l currently refer to
-    float l_part = 0.f;        // this half's share of the row sum
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int sb = j % NSB;
-      const uint32_t s_tmem = tmem + lane_base + sb * 128;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j / NSB) & 1));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[2][32];
-      tmem_ld32(s_tmem + h * 64, sr[0]);
-      tmem_ld32(s_tmem + h * 64 + 32, sr[1]);
-      tmem_ld_wait();
-      const bool need_mask = (p.causal && j == nkv - 1) || (j == p.n_kv_total - 1 && (p.S % BN) != 0);
-      if (need_mask) {
-        const int key0 = j * BN + h * 64;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const int key = key0 + c;
-          if ((p.causal && key > q) || key >= p.S) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
-        }
-      }
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        mx0 = fmax3(mx0, __uint_as_float(sr[0][2 * c]), __uint_as_float(sr[0][2 * c + 1]));
-        mx1 = fmax3(mx1, __uint_as_float(sr[1][2 * c]), __uint_as_float(sr[1][2 * c + 1]));
-      }
-      // exchange the half-row maxima (both halves have read S, so P may overwrite it afterwards)
-      float* xr = red + (j & 1) * 256;
-      xr[h * 128 + row] = fmaxf(mx0, mx1);
-      named_barrier_sync(1, 256);
-      const float mx = fmaxf(xr[row], xr[128 + row]);
-      float alpha = 1.f;
-      bool rescale_o = false;
-      if (j == 0) {
-        m_used = mx;
-      } else if ((mx - m_used) * c2 > RESCALE_LOG2_THRESHOLD) {
-        alpha = ex2_approx((m_used - mx) * c2);
-        l_part *= alpha;
-        rescale_o = true;
-        m_used = mx;
-      }
-      const float mb = (m_used == -INFINITY) ? 0.f : m_used * c2;
-      const uint64_t nmb2 = f2_pack(-mb, -mb);
-      // p = 2^(s*scale*log2e - m*scale*log2e) in f32x2 pairs; P (bf16, two per column) goes to
-      // columns 32h..32h+31 of this S buffer
-      uint64_t acc0 = 0ull, acc1 = 0ull;
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int e = 2 * c;
-        const uint64_t xy = f2_fma(f2_pack(__uint_as_float(sr[e >> 5][e & 31]), __uint_as_float(sr[e >> 5][(e & 31) + 1])),
-                                   c2x2, nmb2);
-        float x0, x1;
-        f2_unpack(xy, x0, x1);
-        const float p0 = ex2_approx(x0);
-        const float p1 = ex2_approx(x1);
-        if (c & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
-        else acc0 = f2_add(acc0, f2_pack(p0, p1));
-        pk[c] = pack_bf16x2(p0, p1);
-      }
-      {
-        float a0, a1;
-        f2_unpack(f2_add(acc0, acc1), a0, a1);
-        l_part += a0 + a1;
-      }
-      tmem_st32(s_tmem + h * 32, pk);
-      if (__any_sync(0xffffffffu, rescale_o)) {
-        // O must hold P_{j-1} V_{j-1} before it is rescaled
-        ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(j - 1) % NSB], ((j - 1) / NSB) & 1));
+    int gs = 0;
+    int b, hq, qt;
+    for (int k = 0; ok && tile_of(p, k, b, hq, qt); ++k) {
+      const int q0 = qt * BM;
+      const int q = q0 + row;
+      const int nkv = tile_nkv(qt);
+      float m_used = -INFINITY;  // raw-score max that O and l currently refer to
+      float l_part = 0.f;        // this half's share of the row sum
+      for (int j = 0; j < nkv; ++j, ++gs) {
+        const int sb = gs % NSB;
+        const uint32_t s_tmem = tmem + lane_base + sb * 128;
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (gs / NSB) & 1));
         if (!ok) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int c4 = 0; c4 < D / 64; ++c4) {
-          uint32_t r[32];
-          tmem_ld32(o_half + c4 * 32, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-          tmem_st32(o_half + c4 * 32, r);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&p_full[sb]);
-    }
-    // ---- epilogue: l = both halves; O / l -> bf16 -> smem (the Q tile's 128B-swizzled panels) -> TMA
-    if (ok) ok = mbar_wait(o_full, 0);
-    ok = __all_sync(0xffffffffu, ok);
-    red[256 + h * 128 + row] = l_part;   // the exchange buffer of odd steps is idle by now
-    named_barrier_sync(1, 256);
-    const float l = red[256 + row] + red[384 + row];
-    if (ok) {
-      tc_fence_after();
-      const float inv_l = 1.f / l;
-#pragma unroll 1
-      for (int c4 = 0; c4 < D / 64; ++c4) {
-        uint32_t r[32];
-        tmem_ld32(o_half + c4 * 32, r);
+        uint32_t sr[2][32];
+        tmem_ld32(s_tmem + h * 64, sr[0]);
+        tmem_ld32(s_tmem + h * 64 + 32, sr[1]);
         tmem_ld_wait();
+        const bool need_mask = (p.causal && j == nkv - 1) || (j == p.n_kv_total - 1 && (p.S % BN) != 0);
+        if (need_mask) {
+          const int key0 = j * BN + h * 64;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const int key = key0 + c;
+            if ((p.causal && key > q) || key >= p.S) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+          }
+        }
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          mx0 = fmax3(mx0, __uint_as_float(sr[0][2 * c]), __uint_as_float(sr[0][2 * c + 1]));
+          mx1 = fmax3(mx1, __uint_as_float(sr[1][2 * c]), __uint_as_float(sr[1][2 * c + 1]));
+        }
+        // exchange the half-row maxima (both halves have read S, so P may overwrite it afterwards)
+        float* xr = red + (gs & 1) * 256;
+        xr[h * 128 + row] = fmaxf(mx0, mx1);
+        named_barrier_sync(1, 256);
+        const float mx = fmaxf(xr[row], xr[128 + row]);
+        float alpha = 1.f;
+        bool rescale_o = false;
+        if (j == 0) {
+          m_used = mx;
+        } else if ((mx - m_used) * c2 > RESCALE_LOG2_THRESHOLD) {
+          alpha = ex2_approx((m_used - mx) * c2);
+          l_part *= alpha;
+          rescale_o = true;
+          m_used = mx;
+        }
+        const float mb = (m_used == -INFINITY) ? 0.f : m_used * c2;
+        const uint64_t nmb2 = f2_pack(-mb, -mb);
+        // p = 2^(s*scale*log2e - m*scale*log2e) in f32x2 pairs; P (bf16, two per column) goes to
+        // columns 32h..32h+31 of this S buffer
+        uint64_t acc0 = 0ull, acc1 = 0ull;
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int e = 2 * c;
+          const uint64_t xy = f2_fma(
+              f2_pack(__uint_as_float(sr[e >> 5][e & 31]), __uint_as_float(sr[e >> 5][(e & 31) + 1])), c2x2, nmb2);
+          float x0, x1;
+          f2_unpack(xy, x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          if (c & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
+          else acc0 = f2_add(acc0, f2_pack(p0, p1));
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        {
+          float a0, a1;
+          f2_unpack(f2_add(acc0, acc1), a0, a1);
+          l_part += a0 + a1;
+        }
+        tmem_st32(s_tmem + h * 32, pk);
+        if (__any_sync(0xffffffffu, rescale_o)) {
+          // O must hold P V of the previous step before it is rescaled
+          ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(gs - 1) % NSB], ((gs - 1) / NSB) & 1));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c4 = 0; c4 < D / 64; ++c4) {
+            uint32_t r[32];
+            tmem_ld32(o_half + c4 * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+            tmem_st32(o_half + c4 * 32, r);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full[sb]);
+      }
+      if (!ok) break;
+      // ---- epilogue: l = both halves; O / l -> bf16 -> staging smem (128B swizzle) -> TMA store
+      ok = __all_sync(0xffffffffu, mbar_wait(o_full, k & 1));
+      if (!ok) break;
+      tc_fence_after();
+      // the l exchange uses the buffer the next step will use; the staging barrier below
+      // separates it from that step's writes
+      float* xl = red + (gs & 1) * 256;
+      xl[h * 128 + row] = l_part;
+      uint32_t ov[D / 64][32];
+#pragma unroll
+      for (int c4 = 0; c4 < D / 64; ++c4) tmem_ld32(o_half + c4 * 32, ov[c4]);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(o_free);  // the next tile's first P.V may overwrite O now
+      if (threadIdx.x == 0) tma_store_wait_read0();  // the previous tile's store has read the staging tile
+      named_barrier_sync(1, 256);
+      const float l = xl[row] + xl[128 + row];
+      const float inv_l = 1.f / l;
+#pragma unroll
+      for (int c4 = 0; c4 < D / 64; ++c4) {
         const int col0 = h * (D / 2) + c4 * 32;   // first output column of this chunk
-        uint8_t* panel = sQ + (col0 >> 6) * CHUNK_BYTES + row * 128;
+        uint8_t* panel = sO + (col0 >> 6) * CHUNK_BYTES + row * 128;
         const int u0 = (col0 & 63) >> 3;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(r[8 * u + 0]) * inv_l, __uint_as_float(r[8 * u + 1]) * inv_l);
-          w.y = pack_bf16x2(__uint_as_float(r[8 * u + 2]) * inv_l, __uint_as_float(r[8 * u + 3]) * inv_l);
-          w.z = pack_bf16x2(__uint_as_float(r[8 * u + 4]) * inv_l, __uint_as_float(r[8 * u + 5]) * inv_l);
-          w.w = pack_bf16x2(__uint_as_float(r[8 * u + 6]) * inv_l, __uint_as_float(r[8 * u + 7]) * inv_l);
+          w.x = pack_bf16x2(__uint_as_float(ov[c4][8 * u + 0]) * inv_l, __uint_as_float(ov[c4][8 * u + 1]) * inv_l);
+          w.y = pack_bf16x2(__uint_as_float(ov[c4][8 * u + 2]) * inv_l, __uint_as_float(ov[c4][8 * u + 3]) * inv_l);
+          w.z = pack_bf16x2(__uint_as_float(ov[c4][8 * u + 4]) * inv_l, __uint_as_float(ov[c4][8 * u + 5]) * inv_l);
+          w.w = pack_bf16x2(__uint_as_float(ov[c4][8 * u + 6]) * inv_l, __uint_as_float(ov[c4][8 * u + 7]) * inv_l);
           *reinterpret_cast<uint4*>(panel + (((u0 + u) ^ (row & 7)) << 4)) = w;
         }
       }
       if (h == 0 && p.lse != nullptr && q < p.S)
         p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.S + q] = m_used * p.scale + logf(l);
       fence_proxy_async_smem();
-    } else {
-      set_error(&g_prefill_status, kDevWaitTimeout);
+      named_barrier_sync(1, 256);
+      if (threadIdx.x == 0) {
+        for (int c = 0; c < L::CHUNKS; ++c) tma_store_3d(&tm_o, sO + c * CHUNK_BYTES, hq * D + c * 64, q0, b);
+        tma_store_commit();
+      }
     }
-    named_barrier_sync(1, 256);
-    if (ok && threadIdx.x == 0) {
-      for (int c = 0; c < L::CHUNKS; ++c) tma_store_3d(&tm_o, sQ + c * CHUNK_BYTES, hq * D + c * 64, q0, b);
-      tma_store_commit();
-      tma_store_wait0();
-    }
+    if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
+    if (threadIdx.x == 0) tma_store_wait0();
   }
 
   __syncwarp();  // single-lane roles rejoin their warps before the CTA barrier
@@ -385,13 +437,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+int g_num_sms = 0;
+
 template <int D>
 cudaError_t launch(const PrefillMaps& m, const PrefillParams& p, cudaStream_t stream) {
   auto kern = prefill_fwd_kernel<D>;
   const int smem = Layout<D>::ALLOC;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.Hq, p.num_qblocks, p.B);
+  if (g_num_sms == 0) {
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  }
+  const long long tiles = static_cast<long long>(p.num_qblocks) * p.B * p.Hq;
+  const int grid = static_cast<int>(tiles < g_num_sms ? tiles : g_num_sms);
   kern<<<grid, NUM_THREADS, smem, stream>>>(m.q, m.k, m.v, m.o, p);
   return cudaGetLastError();
 }

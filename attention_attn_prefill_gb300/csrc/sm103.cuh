@@ -24,6 +24,7 @@ enum DeviceError : uint32_t {
   kDevWaitTimeout = 1,       // an mbarrier wait ran out of time
   kDevBadPage = 2,           // block_table entry outside [0, num_blocks)
   kDevBadSplit = 3,          // split geometry inconsistent with the launch
+  kDevMisaligned = 4,        // dynamic shared memory not 1 KB-aligned
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

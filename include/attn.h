@@ -146,7 +146,8 @@ attn_status_t attn_combine(const float* part_o, const float* part_m, const float
  * Device-side status: waits for all work on the current device, then stores
  * the first error code any kernel of this library recorded since the last
  * clear (0 = none; 1 = a pipeline wait timed out; 2 = block-table entry out of
- * range; 3 = inconsistent split geometry) and, if `clear` != 0, resets it.
+ * range; 3 = a seq_len the block table cannot cover; 4 = shared memory not
+ * 1 KB-aligned) and, if `clear` != 0, resets it.
  */
 attn_status_t attn_device_status(uint32_t* code, int clear);
 
