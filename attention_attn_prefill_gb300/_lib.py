@@ -44,6 +44,7 @@ _SIGNATURES = {
     "attn_decode_workspace_bytes": (c_size_t, [c_int] * 4),
     "attn_decode_paged": (c_int, [c_void_p] * 7 + [c_int] * 9 + [c_float, c_void_p, c_size_t, c_void_p]),
     "attn_combine": (c_int, [c_void_p] * 3 + [c_int] * 3 + [c_void_p, c_void_p, c_void_p]),
+    "attn_decode_paged_noalloc": (c_int, [c_void_p] * 7 + [c_int] * 9 + [c_float, c_void_p]),
     "attn_device_status": (c_int, [c_u32_p, c_int]),
 }
 
@@ -161,6 +162,30 @@ def decode_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, 
         N, Hq, Hkv, d, page, max_blocks, num_blocks, num_splits, split_tokens, float(scale), ws_ptr, ws_bytes,
         _stream_handle(stream))
     _check(st, "attn_decode_paged")
+    return out, lse
+
+
+def decode_paged_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
+                         seq_lens: torch.Tensor, scale: float | None = None, num_splits: int = 1,
+                         split_tokens: int = 0, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                         return_lse: bool = True, stream=None):
+    """decode_paged without a workspace: the partials use the library's fixed device array."""
+    N, Hq, d = q.shape
+    num_blocks, page, Hkv, _ = k_cache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((N, Hq), dtype=torch.float32, device=q.device)
+    st = lib().attn_decode_paged_noalloc(
+        _dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.bfloat16, "k_cache"),
+        _dev(v_cache, torch.bfloat16, "v_cache"), _dev(block_table, torch.int32, "block_table"),
+        _dev(seq_lens, torch.int32, "seq_lens"), _dev(out, torch.bfloat16, "out"),
+        _dev(lse, torch.float32, "lse") if lse is not None else None,
+        N, Hq, Hkv, d, page, block_table.shape[1], num_blocks, num_splits, split_tokens, float(scale),
+        _stream_handle(stream))
+    _check(st, "attn_decode_paged_noalloc")
     return out, lse
 
 

@@ -126,6 +126,34 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
                                 void* stream);
 
 /*
+ * Paged decode that allocates nothing.  The pages have no counterpart to
+ * this entry point: it exists for callers that cannot provide a workspace,
+ * such as a plugin inside a host framework that owns all device memory and
+ * hands out no scratch buffers, or a serving loop that forbids device
+ * allocations once it has started.
+ *   Arguments, layouts, results and errors are those of attn_decode_paged,
+ *   without workspace / workspace_bytes: the per-split partials live in a
+ *   fixed array of ATTN_DECODE_NOALLOC_SCRATCH_BYTES inside the library's own
+ *   device memory, present on every device that loads the library until the
+ *   process exits.  No cudaMalloc, cudaFree or other allocating call is made.
+ *   If the partials need more than that (num_seqs * Hq * slots * (d + 2) * 4
+ *   bytes with slots > 1), the call returns ATTN_ERR_WORKSPACE and enqueues
+ *   nothing.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.
+ *   All calls share the array: calls whose work overlaps on the GPU (other
+ *   streams, other host threads) race on it.  Every partial a call reads was
+ *   written earlier in the same call, so leftovers of earlier calls are
+ *   harmless.
+ */
+#define ATTN_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_table, const int32_t* seq_lens, void* o, float* lse,
+                                        int num_seqs, int Hq, int Hkv, int d, int page_size, int max_blocks_per_seq,
+                                        int num_blocks, int num_splits, int split_tokens, float scale, void* stream);
+
+/*
  * Merge per-group partials ("Why your local LLM feels dumber than it is",
  * section "Backend names expand into four decode algorithms": normalised
  * group outputs merged by their log-sum statistics).
