@@ -45,6 +45,9 @@ from workloads import LLAMA8B, PAGED, decode_inputs_for, decode_lens_for, decode
 METRIC = "prefill TFLOP/s & decode KV GB/s on 1 GB300, as % of bf16 TC peak / HBM peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DECODE_SPLITS = 4
+# "GPU Datapath: Where Every Byte Moves in One LLM Inference Step", section C: FA3 on H100 runs this
+# exact prefill cell (causal, GQA 32:8, S=2048, d=128) in 87.7 us -> 34.38 GFLOP / 87.7 us.
+PAGES_H100_TFLOPS = 34.376515584e9 / 87.7e-6 / 1e12
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -73,60 +76,92 @@ def shard(n_units: int, rank: int, world: int) -> range:
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    """SM clock and throttle reasons sampled every few ms while the timed region runs.
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    Reads NVML through ctypes (no Python package needed); falls back to a
+    `nvidia-smi -lms` loop if NVML cannot be loaded.  Reading clocks changes
+    nothing on the GPU.
+    """
 
-    def __init__(self, index: int):
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap"}
+
+    def __init__(self, index: int, period_s: float = 0.002):
         self.index = index
-        self.proc = None
-        self.lines = []
+        self.period = period_s
+        self.samples = []          # (sm_mhz, reasons_mask)
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._nvml = None
+        self._proc = None
+
+    def _open_nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(1), ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        self._nvml = (lib, h, ctypes)
+
+    def _loop(self):
+        lib, h, ct = self._nvml
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, ct.c_int(1), ct.byref(clk)) == 0:
+                r = rs.value if get_reasons(h, ct.byref(rs)) == 0 else 0
+                self.samples.append((float(clk.value), int(r)))
+            time.sleep(self.period)
 
     def __enter__(self):
-        exe = shutil.which("nvidia-smi")
-        if exe:
-            self.proc = subprocess.Popen(
-                [exe, "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
-            time.sleep(0.3)
+        try:
+            self._open_nvml()
+            self._thread = threading.Thread(target=self._loop, daemon=True)
+            self._thread.start()
+        except Exception:
+            exe = shutil.which("nvidia-smi")
+            if exe:
+                self._proc = subprocess.Popen(
+                    [exe, "-i", str(self.index), "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "20"], stdout=subprocess.PIPE,
+                    stderr=subprocess.DEVNULL, text=True)
+                self._thread = threading.Thread(target=self._read_smi, daemon=True)
+                self._thread.start()
+        time.sleep(0.01)
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def _read_smi(self):
+        for line in self._proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            try:
+                self.max_mhz = float(parts[1])
+                self.samples.append((float(parts[0]), int(parts[2], 16)))
+            except (ValueError, IndexError):
+                continue
 
     def __exit__(self, *exc):
-        if self.proc:
-            time.sleep(0.2)
-            self.proc.terminate()
+        self._stop.set()
+        if self._proc:
+            self._proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._proc.wait(timeout=5)
             except Exception:
-                self.proc.kill()
+                self._proc.kill()
+        if hasattr(self, "_thread"):
+            self._thread.join(timeout=2)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[4:8]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"]}
+        reasons = sorted({name for _, r in self.samples for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples)}
 
 
 def traffic_record(kernel: str):
@@ -281,7 +316,8 @@ def run_gpu(args):
         "ms_per_step": round(step_ms, 4),
         "higher_is_better": True,
         "scaling": "weak",
-        "vs_baseline": None,
+        "vs_baseline": round(tflops / PAGES_H100_TFLOPS, 3),
+        "vs_baseline_ref": f"{PAGES_H100_TFLOPS:.1f} TFLOP/s: FA3 on H100, 87.7 us for this prefill cell (pages)",
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16; shapes of the pages' workloads)",
         "config": {
@@ -326,18 +362,6 @@ def run_gpu(args):
 
 # ---------------------------------------------------------------------------- CPU oracle
 
-def oracle_prefill_sample(heads: int):
-    """Time the float64 oracle on `heads` query heads of the prefill workload (all rows)."""
-    import oracle.attention as oa
-    cfg = LLAMA8B
-    x = prefill_inputs_for(cfg)
-    t0 = time.perf_counter()
-    oa.prefill(x.q, x.k, x.v, cfg.scale, causal=True, heads=range(heads))
-    dt = time.perf_counter() - t0
-    flops = cfg.causal_flops * heads / cfg.Hq
-    return flops / dt / 1e12, dt, flops
-
-
 def cpu_baseline(min_seconds: float):
     """Oracle on whole query heads of the prefill workload, repeated until about min_seconds of work."""
     import oracle.attention as oa
@@ -356,17 +380,23 @@ def cpu_baseline(min_seconds: float):
 
 
 def run_reference(args):
+    """The float64 oracle on the host cores: each step is `ref_heads` query heads of the prefill workload."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    for _ in range(args.warmup):
-        oracle_prefill_sample(1)
-    vals, times = [], []
+    import oracle.attention as oa
+    cfg = LLAMA8B
+    x = prefill_inputs_for(cfg)
+
+    def step(i):
+        heads = [(i * args.ref_heads + h) % cfg.Hq for h in range(args.ref_heads)]
+        oa.prefill(x.q, x.k, x.v, cfg.scale, causal=True, heads=heads)
+
+    for i in range(args.warmup):
+        step(i)
     t_all = time.perf_counter()
-    for _ in range(args.steps):
-        tf, dt, _ = oracle_prefill_sample(args.ref_heads)
-        vals.append(tf)
-        times.append(dt)
+    for i in range(args.steps):
+        step(i)
     total = time.perf_counter() - t_all
     value = args.steps * LLAMA8B.causal_flops * args.ref_heads / LLAMA8B.Hq / total / 1e12
     line = {
