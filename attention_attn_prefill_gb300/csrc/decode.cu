@@ -21,7 +21,10 @@
 // warps' states are merged in shared memory; the CTA writes either the final
 // bf16 output + LSE (one split) or its partial.
 //
-// Combine kernel: one warp per (sequence, query head) merges the partials.
+// Combine kernel: one warp per (sequence, query head) merges the partials.  It is
+// launched as a programmatic dependent of the split kernel: its CTAs may start
+// while the split kernel's last wave runs and wait (griddepcontrol.wait) until
+// every partial is written and visible, which hides the second launch.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -117,6 +120,8 @@ __global__ void __launch_bounds__(NW * 32)
   const int g = blockIdx.y;
   const int n = blockIdx.z;
   const int G = p.G;
+  // let a dependent combine launch start early; it waits for this grid to finish before reading
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int seq_len = p.seq_lens[n];
   if (seq_len < 0 || seq_len > p.max_blocks * PAGE) {
     // a length the block table cannot cover: record it and stay inside the table
@@ -376,6 +381,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
                                                       const float* __restrict__ part_m,
                                                       const float* __restrict__ part_l, int rows, int splits,
                                                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+  // the partials come from the preceding kernel in the stream: wait until they are all visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + warp;
   if (row >= rows) return;
@@ -437,13 +444,24 @@ cudaError_t decode_split_launch(int d, const DecodeMaps& maps, const DecodeParam
 
 cudaError_t combine_launch(int d, const float* part_o, const float* part_m, const float* part_l, int rows,
                            int splits, void* o, float* lse, cudaStream_t stream) {
-  dim3 grid((rows + 3) / 4);
   auto* out = static_cast<__nv_bfloat16*>(o);
-  if (d == 128) combine_kernel<128><<<grid, 128, 0, stream>>>(part_o, part_m, part_l, rows, splits, out, lse);
-  else if (d == 256) combine_kernel<256><<<grid, 128, 0, stream>>>(part_o, part_m, part_l, rows, splits, out, lse);
-  else if (d == 64) combine_kernel<64><<<grid, 128, 0, stream>>>(part_o, part_m, part_l, rows, splits, out, lse);
+  void (*kern)(const float*, const float*, const float*, int, int, __nv_bfloat16*, float*) = nullptr;
+  if (d == 128) kern = combine_kernel<128>;
+  else if (d == 256) kern = combine_kernel<256>;
+  else if (d == 64) kern = combine_kernel<64>;
   else return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  // programmatic dependent launch: may begin before the previous kernel in the stream has finished
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((rows + 3) / 4);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, part_o, part_m, part_l, rows, splits, out, lse);
 }
 
 cudaError_t decode_status(uint32_t* out, bool clear) {

@@ -10,9 +10,9 @@
 //   * the kernel is persistent: one CTA per SM walks a list of work tiles
 //     (one 128-row Q tile of one (batch, query head) each), longest causal
 //     tiles first, and keeps its pipelines running across tile boundaries;
-//   * two producer threads stream Q (once per tile, Step 3) and 128-key K and
-//     V tiles through shared-memory rings (two K stages, three V stages) with
-//     mbarrier full/empty pairs (Step 6);
+//   * two producer threads, in two warps, stream Q (once per tile, Step 3)
+//     and 128-key K and V tiles through shared-memory rings (two K stages,
+//     three V stages) with mbarrier full/empty pairs (Step 6);
 //   * one thread issues S_j = Q K_j^T into TMEM (Step 4).  S is triple-buffered
 //     in TMEM, so the tensor core computes S two steps ahead of softmax.  A
 //     second thread, in another warp, issues O += P_j V_j with P (bf16, over
@@ -50,8 +50,9 @@ constexpr int BN = 128;          // keys per K/V tile
 constexpr int NSB = 3;           // S buffers in TMEM
 constexpr int K_STAGES = 2;      // K_j is free as soon as S_j is done, long before it is reloaded
 constexpr int V_STAGES = 3;      // V_j is held until P_j V_j is done
-constexpr int NUM_THREADS = 352; // 8 softmax warps, 1 TMA warp, 2 MMA warps
-constexpr int PRODUCER_WARP = 8;
+constexpr int NUM_THREADS = 384; // 8 softmax warps, 2 TMA warps, 2 MMA warps
+constexpr int PRODUCER_WARP = 8; // loads Q and streams K
+constexpr int V_WARP = 11;       // streams V
 constexpr int MMA_WARP = 9;      // issues S = Q K^T, owns the TMEM allocation
 constexpr int PV_WARP = 10;      // issues O += P V
 constexpr uint32_t TMEM_COLS = 512;
@@ -159,12 +160,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int G = p.Hq / p.Hkv;
   auto tile_nkv = [&](int qt) { return p.causal ? (qt + 1) : p.n_kv_total; };
 
-  if (warp == PRODUCER_WARP) {
+  if (warp == PRODUCER_WARP || warp == V_WARP) {
     // ------------------------------------------------------------ TMA producers
-    // Lane 0 loads Q and the K tiles, lane 1 the V tiles; each waits only on its own ring.
+    // Warp 8 loads Q and the K tiles, warp 11 the V tiles; each waits only on its own ring.
     // Counters run across work tiles, so the rings never drain between tiles.
-    if (lane < 2) {
-      const bool is_k = lane == 0;
+    if (lane == 0) {
+      const bool is_k = warp == PRODUCER_WARP;
       const int nst = is_k ? K_STAGES : V_STAGES;
       uint64_t* full = is_k ? k_full : v_full;
       uint64_t* empty = is_k ? k_empty : v_empty;
