@@ -42,6 +42,7 @@ _SIGNATURES = {
     "attn_prefill": (c_int, [c_void_p] * 5 + [c_int] * 5 + [c_float, c_int, c_void_p]),
     "attn_decode_num_slots": (c_int, [c_int] * 4),
     "attn_decode_workspace_bytes": (c_size_t, [c_int] * 4),
+    "attn_decode_balanced_workspace_bytes": (c_size_t, [c_int] * 4),
     "attn_decode_paged": (c_int, [c_void_p] * 7 + [c_int] * 9 + [c_float, c_void_p, c_size_t, c_void_p]),
     "attn_combine": (c_int, [c_void_p] * 3 + [c_int] * 3 + [c_void_p, c_void_p, c_void_p]),
     "attn_decode_paged_noalloc": (c_int, [c_void_p] * 7 + [c_int] * 9 + [c_float, c_void_p]),
@@ -128,11 +129,18 @@ def decode_workspace_bytes(num_seqs: int, Hq: int, d: int, slots: int) -> int:
     return int(lib().attn_decode_workspace_bytes(num_seqs, Hq, d, slots))
 
 
+def decode_balanced_workspace_bytes(num_seqs: int, Hq: int, Hkv: int, d: int) -> int:
+    return int(lib().attn_decode_balanced_workspace_bytes(num_seqs, Hq, Hkv, d))
+
+
 def decode_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
                  seq_lens: torch.Tensor, scale: float | None = None, num_splits: int = 1, split_tokens: int = 0,
                  out: torch.Tensor | None = None, lse: torch.Tensor | None = None, return_lse: bool = True,
                  workspace: torch.Tensor | None = None, stream=None):
-    """Paged split-KV decode: q [N,Hq,d]; caches [num_blocks,16,Hkv,d] bf16 -> (o [N,Hq,d], lse [N,Hq])."""
+    """Paged split-KV decode: q [N,Hq,d]; caches [num_blocks,16,Hkv,d] bf16 -> (o [N,Hq,d], lse [N,Hq]).
+
+    num_splits=0 with split_tokens=0 selects balanced mode (equal page shares per worker warp).
+    """
     N, Hq, d = q.shape
     num_blocks, page, Hkv, dk = k_cache.shape
     if dk != d or v_cache.shape != k_cache.shape:
@@ -142,10 +150,15 @@ def decode_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, 
     max_blocks = block_table.shape[1]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    slots = decode_num_slots(max_blocks, num_splits, split_tokens, page)
-    if slots < 1:
-        raise AttnError(1, "attn_decode_num_slots")
-    need = decode_workspace_bytes(N, Hq, d, slots)
+    if num_splits == 0 and split_tokens == 0:
+        need = int(lib().attn_decode_balanced_workspace_bytes(N, Hq, Hkv, d))   # balanced mode
+        if need == 0:
+            raise AttnError(1, "attn_decode_balanced_workspace_bytes")
+    else:
+        slots = decode_num_slots(max_blocks, num_splits, split_tokens, page)
+        if slots < 1:
+            raise AttnError(1, "attn_decode_num_slots")
+        need = decode_workspace_bytes(N, Hq, d, slots)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     if out is None:

@@ -122,6 +122,14 @@ size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d, int slots) {
   return static_cast<size_t>(num_seqs) * Hq * slots * (static_cast<size_t>(d) + 2) * sizeof(float);
 }
 
+size_t attn_decode_balanced_workspace_bytes(int num_seqs, int Hq, int Hkv, int d) {
+  if (num_seqs < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (d != 128 && d != 256)) return 0;
+  const int warps = attn::decode_balanced_warps(d);
+  if (warps <= 0) return 0;
+  return attn::decode_balanced_records(warps, num_seqs, Hkv) * (Hq / Hkv) * (static_cast<size_t>(d) + 2) *
+         sizeof(float);
+}
+
 attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                                 const int32_t* seq_lens, void* o, float* lse, int num_seqs, int Hq, int Hkv, int d,
                                 int page_size, int max_blocks_per_seq, int num_blocks, int num_splits,
@@ -142,6 +150,35 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;  // query heads per KV head fill at most 16 MMA rows
   if (num_seqs > 65535 || Hkv > 65535) return ATTN_ERR_INVALID_ARG;
   if (static_cast<int64_t>(num_blocks) * page_size > (int64_t(1) << 31) - 1) return ATTN_ERR_INVALID_ARG;
+  if (num_splits == 0 && split_tokens == 0) {
+    // balanced mode: equal shares of all pages per worker warp, then a combine
+    attn::BalancedParams bp;
+    bp.warps_total = attn::decode_balanced_warps(d);
+    if (bp.warps_total <= 0) return ATTN_ERR_CUDA;
+    const size_t need = attn_decode_balanced_workspace_bytes(num_seqs, Hq, Hkv, d);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+    attn::DecodeMaps bmaps;
+    const uint64_t brow = static_cast<uint64_t>(Hkv) * d * 2;
+    const uint64_t btokens = static_cast<uint64_t>(num_blocks) * page_size;
+    if (!encode_3d(&bmaps.k, k_cache, d, Hkv, btokens, static_cast<uint64_t>(d) * 2, brow, 64, 1, page_size) ||
+        !encode_3d(&bmaps.v, v_cache, d, Hkv, btokens, static_cast<uint64_t>(d) * 2, brow, 64, 1, page_size))
+      return ATTN_ERR_CUDA;
+    bp.q = static_cast<const __nv_bfloat16*>(q);
+    bp.block_table = block_table;
+    bp.seq_lens = seq_lens;
+    bp.o = static_cast<__nv_bfloat16*>(o);
+    bp.lse = lse;
+    bp.rec = static_cast<float*>(workspace);
+    bp.N = num_seqs;
+    bp.Hq = Hq;
+    bp.Hkv = Hkv;
+    bp.G = Hq / Hkv;
+    bp.max_blocks = max_blocks_per_seq;
+    bp.num_blocks = num_blocks;
+    bp.scale = scale;
+    bp.scale_log2 = scale * 1.4426950408889634f;
+    return from_cuda(attn::decode_balanced_launch(d, bmaps, bp, static_cast<cudaStream_t>(stream)));
+  }
   const int slots = attn_decode_num_slots(max_blocks_per_seq, page_size, num_splits, split_tokens);
   if (slots < 1 || slots > 65535) return ATTN_ERR_INVALID_ARG;
   const size_t need = attn_decode_workspace_bytes(num_seqs, Hq, d, slots);

@@ -423,6 +423,432 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
   if (lse != nullptr && lane == 0) lse[row] = W > 0.f ? M + logf(W) : -INFINITY;
 }
 
+// ----------------------------------------------------------------------------
+// Balanced decode.  The pages of all sequences, for every KV head, form one
+// list ordered by (sequence, KV head, page); worker warp u of the persistent
+// grid takes the contiguous share [u W / Wp, (u+1) W / Wp) of its W pages, so
+// every warp streams the same number of bytes whatever the length mix.  With
+// the KV head inside the sequence, warps running side by side read the other
+// heads' slices of the same physical pages.  A warp writes one partial record
+// per (sequence n, KV head g) its share touches, at index u + n Hkv + g
+// (distinct for all warps, because shares are contiguous and ordered).  The
+// combine finds the warps covering (n, g) arithmetically.
+// ----------------------------------------------------------------------------
+
+__device__ __forceinline__ int pages_of(const int32_t* lens, int n, int max_blocks) {
+  int L = lens[n];
+  L = L < 0 ? 0 : (L > max_blocks * PAGE ? max_blocks * PAGE : L);
+  return (L + PAGE - 1) / PAGE;
+}
+
+__device__ __forceinline__ int clamped_len(const int32_t* lens, int n, int max_blocks) {
+  const int L = lens[n];
+  return L < 0 ? 0 : (L > max_blocks * PAGE ? max_blocks * PAGE : L);
+}
+
+// Warp-wide: total pages per KV head, and (if want >= 0) the first sequence n whose
+// inclusive page prefix exceeds `want`, with the prefix before it.  All lanes get the results.
+__device__ __forceinline__ void page_scan(const int32_t* lens, int N, int max_blocks, int lane, long long want,
+                                          long long& total, int& n_at, long long& before, int mult = 1) {
+  total = 0;
+  n_at = N;
+  before = 0;
+  for (int base = 0; base < N; base += 32) {
+    const int n = base + lane;
+    const int pg = n < N ? mult * pages_of(lens, n, max_blocks) : 0;
+    int incl = pg;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += t;
+    }
+    const long long excl_g = total + incl - pg;  // pages before sequence n
+    if (n_at == N && want >= 0) {
+      const unsigned hit = __ballot_sync(0xffffffffu, n < N && pg > 0 && excl_g <= want && want < excl_g + pg);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        n_at = base + src;
+        before = __shfl_sync(0xffffffffu, excl_g, src);
+      }
+    }
+    total += __shfl_sync(0xffffffffu, incl, 31);
+  }
+}
+
+// Walks the (sequence, KV head, page) list, skipping empty sequences.
+struct PageCursor {
+  int n, g, p, np;  // sequence, KV head, page within it, pages of that sequence
+  __device__ __forceinline__ void advance(const int32_t* lens, int N, int Hkv, int max_blocks) {
+    if (++p < np) return;
+    p = 0;
+    if (++g < Hkv) return;
+    g = 0;
+    do {
+      if (++n == N) n = 0;  // only reached past the end of the list, where nothing is read
+      np = pages_of(lens, n, max_blocks);
+    } while (np == 0);
+  }
+};
+
+template <int D, int NW, int NS>
+struct BLayout {
+  static constexpr int PANELS = D / 64;
+  static constexpr int KV_BYTES = PANELS * PANEL_BYTES;
+  static constexpr int STAGE_BYTES = 2 * KV_BYTES;
+  static constexpr int WARP_BYTES = NS * STAGE_BYTES;
+  static constexpr int Q_BYTES = 16 * D * 2;  // one warp's Q rows
+  static constexpr int Q_OFF = NW * WARP_BYTES;
+  static constexpr int BAR_OFF = Q_OFF + NW * Q_BYTES;
+  static constexpr int ALLOC = BAR_OFF + NW * NS * 8;  // the dynamic window is 1 KB-aligned (checked)
+};
+
+template <int D, int NW, int NS>
+__global__ void __launch_bounds__(NW * 32)
+    decode_balanced_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                           const BalancedParams p) {
+  using L = BLayout<D, NW, NS>;
+  constexpr bool Q_IN_REGS = (D <= 128);
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) set_error(&g_decode_status, kDevMisaligned);
+    return;
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NW * NS; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < p.N; i += NW * 32)
+      if (p.seq_lens[i] < 0 || p.seq_lens[i] > p.max_blocks * PAGE) set_error(&g_decode_status, kDevBadSplit);
+  __syncthreads();
+
+  const int N = p.N, G = p.G;
+  const int u = blockIdx.x * NW + warp;
+  long long W, dummy_before;
+  int dummy_n;
+  page_scan(p.seq_lens, N, p.max_blocks, lane, -1, W, dummy_n, dummy_before, p.Hkv);
+  const long long lo = static_cast<long long>(u) * W / p.warps_total;
+  const long long hi = static_cast<long long>(u + 1) * W / p.warps_total;
+  const int npg = static_cast<int>(hi - lo);
+  if (npg <= 0) return;  // nothing to stream (warps never sync with each other after the setup)
+
+  // cursor at the first page of this warp's share
+  PageCursor cur;
+  {
+    long long tot, before;
+    int n_at;
+    page_scan(p.seq_lens, N, p.max_blocks, lane, lo, tot, n_at, before, p.Hkv);
+    cur.n = n_at;
+    cur.np = pages_of(p.seq_lens, n_at, p.max_blocks);
+    const int r = static_cast<int>(lo - before);
+    cur.g = r / cur.np;
+    cur.p = r % cur.np;
+  }
+  PageCursor icur = cur;  // the issuing lane's cursor runs NS pages ahead
+
+  uint8_t* my_stages = smem + warp * L::WARP_BYTES;
+  uint64_t* my_bars = bars + warp * NS;
+  uint8_t* sQ = smem + L::Q_OFF + warp * L::Q_BYTES;
+  const uint32_t q_base = smem_u32(sQ);
+
+  int nissued = 0;  // pages this warp's lane 0 has requested
+  auto issue = [&](int k) {
+    nissued = k + 1;
+    int pid = p.block_table[static_cast<size_t>(icur.n) * p.max_blocks + icur.p];
+    if (pid < 0 || pid >= p.num_blocks) {
+      set_error(&g_decode_status, kDevBadPage);
+      pid = 0;
+    }
+    uint8_t* st = my_stages + (k % NS) * L::STAGE_BYTES;
+    uint64_t* bar = &my_bars[k % NS];
+    mbar_arrive_expect_tx(bar, L::STAGE_BYTES);
+#pragma unroll
+    for (int c = 0; c < L::PANELS; ++c) {
+      tma_load_3d(st + c * PANEL_BYTES, &tm_k, bar, c * 64, icur.g, pid * PAGE);
+      tma_load_3d(st + L::KV_BYTES + c * PANEL_BYTES, &tm_v, bar, c * 64, icur.g, pid * PAGE);
+    }
+    icur.advance(p.seq_lens, N, p.Hkv, p.max_blocks);
+  };
+  if (lane == 0)
+    for (int k = 0; k < npg && k < NS; ++k) issue(k);
+  __syncwarp();
+
+  const int a_row = ((lane >> 3) & 1) * 8 + (lane & 7);
+  const int a_colh = (lane >> 4) * 8;
+  const int kb_tok = (lane >> 4) * 8 + (lane & 7);
+  const int kb_colh = ((lane >> 3) & 1) * 8;
+  const int vb_tok = ((lane >> 3) & 1) * 8 + (lane & 7);
+  const int vb_colh = (lane >> 4) * 8;
+  const float c2 = p.scale_log2;
+  const size_t R = static_cast<size_t>(p.warps_total) + static_cast<size_t>(p.Hkv) * N;
+
+  uint32_t qa[Q_IN_REGS ? D / 16 : 1][4];
+  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+  float oacc[D / 8][4];
+  int seg_g = -1, seg_n = -1, seg_len = 0;
+  bool first = true;
+
+  // finish the current (g, n) segment: partial record = normalised o, max (natural units), sum
+  auto flush = [&]() {
+    float la = l_a, lb = l_b;
+    la += __shfl_xor_sync(0xffffffffu, la, 1);
+    la += __shfl_xor_sync(0xffffffffu, la, 2);
+    lb += __shfl_xor_sync(0xffffffffu, lb, 1);
+    lb += __shfl_xor_sync(0xffffffffu, lb, 2);
+    const size_t idx = static_cast<size_t>(u) + static_cast<size_t>(seg_n) * p.Hkv + seg_g;
+    const int ra = lane >> 2, rb = ra + 8;
+    float* ro = p.rec + idx * G * D;
+    const float ia = la > 0.f ? 1.f / la : 0.f, ib = lb > 0.f ? 1.f / lb : 0.f;
+#pragma unroll
+    for (int nb = 0; nb < D / 8; ++nb) {
+      const int x = nb * 8 + 2 * (lane & 3);
+      if (ra < G) *reinterpret_cast<float2*>(ro + ra * D + x) = make_float2(oacc[nb][0] * ia, oacc[nb][1] * ia);
+      if (rb < G) *reinterpret_cast<float2*>(ro + rb * D + x) = make_float2(oacc[nb][2] * ib, oacc[nb][3] * ib);
+    }
+    if ((lane & 3) == 0) {
+      float* rm = p.rec + R * G * D + idx * G;
+      float* rl = rm + R * G;
+      if (ra < G) { rm[ra] = la > 0.f ? m_a * p.scale : -INFINITY; rl[ra] = la; }
+      if (rb < G) { rm[rb] = lb > 0.f ? m_b * p.scale : -INFINITY; rl[rb] = lb; }
+    }
+  };
+
+  bool ok = true;
+  int consumed = 0;
+  for (int k = 0; k < npg; ++k) {
+    ok = __all_sync(0xffffffffu, mbar_wait(&my_bars[k % NS], (k / NS) & 1));
+    if (!ok) break;
+    consumed = k + 1;
+    if (cur.g != seg_g || cur.n != seg_n) {
+      if (seg_g >= 0) flush();
+      seg_g = cur.g;
+      seg_n = cur.n;
+      seg_len = clamped_len(p.seq_lens, seg_n, p.max_blocks);
+      // Q rows of the G heads of KV head g for sequence n (rows >= G zero), 16-byte units swizzled
+      for (int i = lane; i < 16 * (D / 8); i += 32) {
+        const int r = i / (D / 8);
+        const int c = i % (D / 8);
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r < G)
+          v = *reinterpret_cast<const uint4*>(p.q + ((static_cast<size_t>(seg_n) * p.Hq + seg_g * G + r) * D + c * 8));
+        *reinterpret_cast<uint4*>(sQ + r * (D * 2) + ((c ^ (r & 7)) << 4)) = v;
+      }
+      __syncwarp();
+      if constexpr (Q_IN_REGS) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int x = kk * 16 + a_colh;
+          ldsm_x4(q_base + a_row * (D * 2) + (((x >> 3) ^ (a_row & 7)) << 4), qa[kk][0], qa[kk][1], qa[kk][2],
+                  qa[kk][3]);
+        }
+      }
+      m_a = m_b = -INFINITY;
+      l_a = l_b = 0.f;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+      first = true;
+    }
+    uint8_t* st = my_stages + (k % NS) * L::STAGE_BYTES;
+    const uint32_t k_base = smem_u32(st);
+    const uint32_t v_base = k_base + L::KV_BYTES;
+    const int tok0 = cur.p * PAGE;
+    const int valid = seg_len - tok0 < PAGE ? seg_len - tok0 : PAGE;
+    if (valid < PAGE) {
+      for (int i = lane; i < (PAGE - valid) * (D / 8); i += 32) {
+        const int r = valid + i / (D / 8);
+        const int x = (i % (D / 8)) * 8;
+        *reinterpret_cast<uint4*>(st + L::KV_BYTES + panel_off(r, x)) = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+    // ---- S = Q K^T (16 heads x 16 tokens)
+    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      uint32_t a[4];
+      if constexpr (Q_IN_REGS) {
+        a[0] = qa[kk][0]; a[1] = qa[kk][1]; a[2] = qa[kk][2]; a[3] = qa[kk][3];
+      } else {
+        const int x = kk * 16 + a_colh;
+        ldsm_x4(q_base + a_row * (D * 2) + (((x >> 3) ^ (a_row & 7)) << 4), a[0], a[1], a[2], a[3]);
+      }
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(k_base + panel_off(kb_tok, kk * 16 + kb_colh), b0, b1, b2, b3);
+      mma_bf16(sacc[0], a, b0, b1);
+      mma_bf16(sacc[1], a, b2, b3);
+    }
+    const int colq = 2 * (lane & 3);
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (nb * 8 + colq + (e & 1) >= valid) sacc[nb][e] = -INFINITY;
+    float mx_a = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
+    float mx_b = fmaxf(fmaxf(sacc[0][2], sacc[0][3]), fmaxf(sacc[1][2], sacc[1][3]));
+    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+    float al_a = 1.f, al_b = 1.f;
+    bool rs = false;
+    if (first) {
+      m_a = mx_a;
+      m_b = mx_b;
+      first = false;
+    } else {
+      if ((mx_a - m_a) * c2 > RESCALE_LOG2_THRESHOLD) {
+        al_a = ex2_approx((m_a - mx_a) * c2);
+        l_a *= al_a;
+        m_a = mx_a;
+        rs = true;
+      }
+      if ((mx_b - m_b) * c2 > RESCALE_LOG2_THRESHOLD) {
+        al_b = ex2_approx((m_b - mx_b) * c2);
+        l_b *= al_b;
+        m_b = mx_b;
+        rs = true;
+      }
+    }
+    if (__any_sync(0xffffffffu, rs)) {
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        oacc[i][0] *= al_a; oacc[i][1] *= al_a;
+        oacc[i][2] *= al_b; oacc[i][3] *= al_b;
+      }
+    }
+    const float mb_a = m_a * c2, mb_b = m_b * c2;
+    float pr[2][4];
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) {
+      pr[nb][0] = ex2_approx(fmaf(sacc[nb][0], c2, -mb_a));
+      pr[nb][1] = ex2_approx(fmaf(sacc[nb][1], c2, -mb_a));
+      pr[nb][2] = ex2_approx(fmaf(sacc[nb][2], c2, -mb_b));
+      pr[nb][3] = ex2_approx(fmaf(sacc[nb][3], c2, -mb_b));
+      l_a += pr[nb][0] + pr[nb][1];
+      l_b += pr[nb][2] + pr[nb][3];
+    }
+    uint32_t pa[4];
+    pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+    pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+    pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+    pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+#pragma unroll
+    for (int nb = 0; nb < D / 8; nb += 2) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(v_base + panel_off(vb_tok, nb * 8 + vb_colh), b0, b1, b2, b3);
+      mma_bf16(oacc[nb], pa, b0, b1);
+      mma_bf16(oacc[nb + 1], pa, b2, b3);
+    }
+    __syncwarp();
+    if (lane == 0 && k + NS < npg) {
+      fence_proxy_async_smem();
+      issue(k + NS);
+    }
+    __syncwarp();
+    cur.advance(p.seq_lens, N, p.Hkv, p.max_blocks);
+  }
+  if (!ok) {
+    set_error(&g_decode_status, kDevWaitTimeout);
+    // copies still in flight must land before this warp's stages can be released
+    if (lane == 0)
+      for (int k = consumed; k < nissued; ++k) mbar_wait(&my_bars[k % NS], (k / NS) & 1);
+    return;
+  }
+  flush();
+}
+
+// One warp per (sequence n, query head hq): merge the records of the warps that covered (g, n).
+template <int D>
+__global__ void __launch_bounds__(128) combine_balanced_kernel(const BalancedParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + warp;
+  if (row >= p.N * p.Hq) return;
+  const int n = row / p.Hq, hq = row % p.Hq;
+  const int G = p.G, g = hq / G, r = hq % G;
+  long long Wt, before;
+  int n_at;
+  page_scan(p.seq_lens, p.N, p.max_blocks, lane, -1, Wt, n_at, before, p.Hkv);
+  constexpr int PER = D / 32;
+  float acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  float M = -INFINITY, W = 0.f;
+  const int np = pages_of(p.seq_lens, n, p.max_blocks);
+  if (np > 0) {
+    // pages of the sequences before n (each appears once per KV head in the list)
+    long long pre = 0;
+    for (int base = 0; base < n; base += 32) {
+      const int m2 = base + lane;
+      int pg = m2 < n ? pages_of(p.seq_lens, m2, p.max_blocks) : 0;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) pg += __shfl_xor_sync(0xffffffffu, pg, off);
+      pre += pg;
+    }
+    const long long Wp = p.warps_total;
+    const long long start = static_cast<long long>(p.Hkv) * pre + static_cast<long long>(g) * np, last = start + np - 1;
+    const int u0 = static_cast<int>(((start + 1) * Wp - 1) / Wt);
+    const int u1 = static_cast<int>(((last + 1) * Wp - 1) / Wt);
+    const size_t R = static_cast<size_t>(p.warps_total) + static_cast<size_t>(p.Hkv) * p.N;
+    const size_t j = static_cast<size_t>(n) * p.Hkv + g;
+    const float* rm = p.rec + R * G * D;
+    const float* rl = rm + R * G;
+    // a warp whose share is empty (fewer pages than warps) wrote no record
+    auto has_pages = [&](int uu) { return (uu + 1) * Wt / Wp > uu * Wt / Wp; };
+    for (int uu = u0; uu <= u1; ++uu) {
+      const size_t idx = uu + j;
+      if (has_pages(uu) && rl[idx * G + r] > 0.f) M = fmaxf(M, rm[idx * G + r]);
+    }
+    if (M != -INFINITY) {
+      for (int uu = u0; uu <= u1; ++uu) {
+        if (!has_pages(uu)) continue;
+        const size_t idx = uu + j;
+        const float li = rl[idx * G + r];
+        if (!(li > 0.f)) continue;
+        const float w = li * expf(rm[idx * G + r] - M);
+        W += w;
+        const float* src = p.rec + (idx * G + r) * D + lane * PER;
+#pragma unroll
+        for (int e = 0; e < PER; e += 2) {
+          const float2 v = *reinterpret_cast<const float2*>(src + e);
+          acc[e] += w * v.x;
+          acc[e + 1] += w * v.y;
+        }
+      }
+    }
+  }
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  __nv_bfloat16* dst = p.o + static_cast<size_t>(row) * D + lane * PER;
+#pragma unroll
+  for (int e = 0; e < PER; e += 2)
+    *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+  if (p.lse != nullptr && lane == 0) p.lse[row] = W > 0.f ? M + logf(W) : -INFINITY;
+}
+
+template <int D, int NW, int NS, int CTAS_PER_SM>
+cudaError_t launch_balanced(const DecodeMaps& m, const BalancedParams& p, cudaStream_t stream) {
+  auto kern = decode_balanced_kernel<D, NW, NS>;
+  const int smem = BLayout<D, NW, NS>::ALLOC;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<p.warps_total / NW, NW * 32, smem, stream>>>(m.k, m.v, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.N * p.Hq + 3) / 4);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_balanced_kernel<D>, p);
+}
+
 template <int D, int NW, int NS>
 cudaError_t launch_split(const DecodeMaps& m, const DecodeParams& p, cudaStream_t stream) {
   auto kern = decode_split_kernel<D, NW, NS>;
@@ -462,6 +888,27 @@ cudaError_t combine_launch(int d, const float* part_o, const float* part_m, cons
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, part_o, part_m, part_l, rows, splits, out, lse);
+}
+
+constexpr int BAL_NW = 4;
+
+size_t decode_balanced_records(int warps_total, int N, int Hkv) {
+  return static_cast<size_t>(warps_total) + static_cast<size_t>(Hkv) * N;
+}
+
+int decode_balanced_warps(int d) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  const int ctas_per_sm = d <= 128 ? 2 : 1;  // shared memory: 112 KB per CTA at d = 128, 224 KB at 256
+  return sms * ctas_per_sm * BAL_NW;
+}
+
+cudaError_t decode_balanced_launch(int d, const DecodeMaps& maps, const BalancedParams& p, cudaStream_t stream) {
+  if (p.warps_total % BAL_NW) return cudaErrorInvalidValue;
+  if (d == 128) return launch_balanced<128, BAL_NW, 3, 2>(maps, p, stream);
+  if (d == 256) return launch_balanced<256, BAL_NW, 3, 1>(maps, p, stream);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t decode_status(uint32_t* out, bool clear) {

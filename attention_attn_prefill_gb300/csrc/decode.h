@@ -34,6 +34,27 @@ struct DecodeParams {
   int write_final;  // 1: write o / lse directly (one split)
 };
 
+// Balanced ("stream-K") decode: every warp of a persistent grid takes an equal
+// contiguous share of the flattened (sequence, KV head, page) list and writes
+// one partial record per (sequence, KV head) it touches; a combine merges them.
+struct BalancedParams {
+  const __nv_bfloat16* q;      // [N][Hq][d]
+  const int32_t* block_table;  // [N][max_blocks]
+  const int32_t* seq_lens;     // [N]
+  __nv_bfloat16* o;            // [N][Hq][d]
+  float* lse;                  // [N][Hq] or null
+  float* rec;                  // records: o [R][G][d], then m [R][G], then l [R][G]; R = warps + N*Hkv
+  int N, Hq, Hkv, G;
+  int max_blocks, num_blocks;
+  int warps_total;             // number of worker warps in the split grid
+  float scale;
+  float scale_log2;
+};
+
+size_t decode_balanced_records(int warps_total, int N, int Hkv);
+int decode_balanced_warps(int d);  // worker warps of the split grid on the current device (0 on error)
+cudaError_t decode_balanced_launch(int d, const DecodeMaps& maps, const BalancedParams& p, cudaStream_t stream);
+
 cudaError_t decode_split_launch(int d, const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream);
 cudaError_t combine_launch(int d, const float* part_o, const float* part_m, const float* part_l, int rows,
                            int splits, void* o, float* lse, cudaStream_t stream);

@@ -164,6 +164,14 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.samples)}
 
 
+def decode_ws_bytes(attn, max_blocks, cfg, num_splits=0, split_tokens=0):
+    """Workspace for one paged decode call (num_splits = split_tokens = 0 is balanced mode)."""
+    if num_splits == 0 and split_tokens == 0:
+        return attn.decode_balanced_workspace_bytes(cfg.N, cfg.Hq, cfg.Hkv, cfg.d)
+    slots = attn.decode_num_slots(max_blocks, num_splits=num_splits, split_tokens=split_tokens)
+    return attn.decode_workspace_bytes(cfg.N, cfg.Hq, cfg.d, slots)
+
+
 def traffic_record(kernel: str):
     """DRAM bytes per launch from a committed ncu summary, if it matches the current kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -209,9 +217,9 @@ def run_gpu(args):
     dq, kc, vc, bt, sl = (t.to(dev) for t in (dx.q, dx.k_cache, dx.v_cache, dx.block_table, dx.seq_lens))
     do = torch.empty_like(dq)
     dl = torch.empty((dcfg.N, dcfg.Hq), dtype=torch.float32, device=dev)
-    slots = attn.decode_num_slots(dx.max_blocks, num_splits=args.decode_splits)
-    ws = torch.empty(max(1, attn.decode_workspace_bytes(dcfg.N, dcfg.Hq, dcfg.d, slots)), dtype=torch.uint8,
-                     device=dev)
+    ws = torch.empty(max(1, decode_ws_bytes(attn, dx.max_blocks, dcfg, num_splits=args.decode_splits)),
+                     dtype=torch.uint8, device=dev)
+    slots = attn.decode_num_slots(dx.max_blocks, num_splits=args.decode_splits) if args.decode_splits else 0
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -305,7 +313,7 @@ def run_gpu(args):
     achieved = flops / (statistics.mean(pre_ms) * 1e-3) / 1e12
     peak_tc = peaks["bf16_tflops"]
     dec_achieved = dbytes / (statistics.mean(dec_ms) * 1e-3) / 1e9
-    launches_per_step = 1 + 1 + (1 if slots > 1 else 0)
+    launches_per_step = 1 + 1 + (1 if (slots > 1 or args.decode_splits == 0) else 0)
     line = {
         "metric": METRIC,
         "value": round(tflops, 2),
@@ -446,9 +454,7 @@ def run_case(args):
         dq, kc, vc, bt, sl = (t.to(dev) for t in (x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens))
         do = torch.empty_like(dq)
         dl = torch.empty((cfg.N, cfg.Hq), dtype=torch.float32, device=dev)
-        slots = attn.decode_num_slots(x.max_blocks, **kw)
-        ws = torch.empty(max(1, attn.decode_workspace_bytes(cfg.N, cfg.Hq, cfg.d, slots)), dtype=torch.uint8,
-                         device=dev)
+        ws = torch.empty(max(1, decode_ws_bytes(attn, x.max_blocks, cfg, **kw)), dtype=torch.uint8, device=dev)
         work, unit = decode_min_bytes(lens, cfg.Hq, cfg.Hkv, cfg.d) / 1e9, "GB/s"
 
         def launch():

@@ -96,6 +96,15 @@ int attn_decode_num_slots(int max_blocks_per_seq, int page_size, int num_splits,
 size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d, int slots);
 
 /*
+ * Bytes of workspace attn_decode_paged needs in balanced mode (num_splits == 0
+ * and split_tokens == 0) on the current device:
+ * (worker warps + Hkv * num_seqs) * (Hq / Hkv) * (d + 2) floats, where the
+ * number of worker warps follows the device's SM count.  Returns 0 for
+ * invalid arguments or when no CUDA device can be queried.
+ */
+size_t attn_decode_balanced_workspace_bytes(int num_seqs, int Hq, int Hkv, int d);
+
+/*
  * Single-token decode over a paged KV cache, split over the context.
  *   q            [num_seqs, Hq, d] bf16
  *   k_cache,
@@ -114,6 +123,12 @@ size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d, int slots);
  *   merges them (same arithmetic as attn_combine).
  *   workspace: device buffer of at least attn_decode_workspace_bytes(...)
  *   bytes (may be NULL when that is 0).
+ *   Balanced mode (num_splits == 0 and split_tokens == 0): the pages of all
+ *   sequences and KV heads form one list, and every worker warp of a grid
+ *   sized to the device takes an equal contiguous share of it, whatever the
+ *   mix of lengths; each share yields one partial per (sequence, KV head) it
+ *   touches and a second kernel merges them.  Needs
+ *   attn_decode_balanced_workspace_bytes(...) bytes of workspace.
  * The query sees all seq_len tokens.  A sequence with seq_len == 0 gets o = 0
  * and lse = -inf.  Tokens of the last page past seq_len are never used, even
  * if they hold NaN.  A block-table entry outside [0, num_blocks) is recorded

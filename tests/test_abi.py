@@ -51,7 +51,7 @@ def _decode_args(**over):
 @pytest.mark.parametrize("over,want", [
     (dict(q=None), 1), (dict(bt=FAKE + 2), 1), (dict(N=0), 1), (dict(Hkv=3), 1),
     (dict(page=32), 2), (dict(d=64), 2), (dict(Hq=40, Hkv=2), 2),
-    (dict(ns=0), 1), (dict(st=24), 1),                       # split_tokens not a page multiple
+    (dict(ns=-1), 1), (dict(st=24), 1),                      # bad split count; split_tokens not a page multiple
     (dict(ws=None), 3), (dict(wsb=10), 3), (dict(ws=FAKE + 4), 3),
 ])
 def test_decode_argument_checks(attn, over, want):

@@ -30,7 +30,8 @@ def compare(attn, x, scale, dev, what, seqs=None, **kw):
 
 
 @pytest.mark.parametrize("kw", [dict(num_splits=1), dict(num_splits=4), dict(num_splits=16),
-                                dict(num_splits=3), dict(split_tokens=16), dict(split_tokens=48)],
+                                dict(num_splits=3), dict(split_tokens=16), dict(split_tokens=48),
+                                dict(num_splits=0)],
                          ids=lambda k: "-".join(f"{a}{b}" for a, b in k.items()))
 def test_paged_d128_gqa4(attn, gpu, kw):
     """Ragged lengths (1..700), NaN in unused page tails and in unused pages."""
@@ -40,7 +41,7 @@ def test_paged_d128_gqa4(attn, gpu, kw):
 
 
 @pytest.mark.parametrize("kw", [dict(num_splits=1), dict(num_splits=5), dict(split_tokens=64),
-                                dict(split_tokens=512)],
+                                dict(split_tokens=512), dict(num_splits=0)],
                          ids=lambda k: "-".join(f"{a}{b}" for a, b in k.items()))
 def test_paged_d256_gqa8(attn, gpu, kw):
     lens = [1, 33, 200, 513, 1000, 1300]
@@ -59,7 +60,7 @@ def test_empty_sequence(attn, gpu):
     """seq_len 0 gives o = 0 and lse = -inf; its neighbours are unaffected."""
     lens = [0, 20, 0, 33]
     x = make_decode_inputs(lens, Hq=4, Hkv=1, d=128, seed=54)
-    for kw in (dict(num_splits=1), dict(num_splits=4)):
+    for kw in (dict(num_splits=1), dict(num_splits=4), dict(num_splits=0)):
         o, lse = run_decode(attn, x, 0.1, gpu, **kw)
         o, lse = o.cpu(), lse.cpu()
         assert torch.all(o[[0, 2]] == 0) and torch.all(torch.isneginf(lse[[0, 2]]))
@@ -82,10 +83,21 @@ def test_split_counts_agree(attn, gpu):
     """Different split geometries agree within the bf16 tolerance (not bit-exactly)."""
     x = make_decode_inputs([3000, 1234, 4096], Hq=32, Hkv=8, d=128, seed=56)
     outs = [run_decode(attn, x, 0.09, gpu, **kw) for kw in (dict(num_splits=1), dict(num_splits=16),
-                                                           dict(split_tokens=256))]
+                                                           dict(split_tokens=256), dict(num_splits=0))]
     for o, lse in outs[1:]:
         check_o(to_np(o), to_np(outs[0][0]), "split vs unsplit")
         check_lse(to_np(lse), to_np(outs[0][1]), "split vs unsplit")
+
+
+def test_balanced_many_short_sequences(attn, gpu):
+    """Balanced mode with fewer pages than worker warps (idle warps) and many empty sequences."""
+    lens = [0, 1, 0, 0, 17, 3, 0, 16, 40] * 5
+    x = make_decode_inputs(lens, Hq=8, Hkv=2, d=128, seed=59, nan_tail=True)
+    seqs = [i for i, L in enumerate(lens) if L > 0]
+    compare(attn, x, 0.1, gpu, "balanced short", seqs=seqs, num_splits=0)
+    o, lse = run_decode(attn, x, 0.1, gpu, num_splits=0)
+    empty = [i for i, L in enumerate(lens) if L == 0]
+    assert torch.all(o.cpu()[empty] == 0) and torch.all(torch.isneginf(lse.cpu()[empty]))
 
 
 def test_bad_page_is_reported(attn, gpu):
@@ -120,7 +132,8 @@ def test_worked_example_on_gpu(attn, gpu):
         kc[pid, :b - a, 0, 0] = st[a:b]
         vc[pid, :b - a, 0, :] = vt[a:b, None]
     x.k_cache, x.v_cache = kc, vc
-    for kw in (dict(num_splits=1), dict(num_splits=54), dict(split_tokens=448), dict(split_tokens=320)):
+    for kw in (dict(num_splits=1), dict(num_splits=54), dict(split_tokens=448), dict(split_tokens=320),
+               dict(num_splits=0)):
         o, lse = run_decode(attn, x, 1.0, gpu, **kw)
         vals = set(o[0, 0].float().cpu().tolist())
         assert len(vals) == 1 and vals.pop() in (1.3203125, 1.328125), kw
@@ -130,13 +143,15 @@ def test_paged_config_full_size(attn, gpu):
     """64 sequences, lengths U[512, 8192], GQA 32:8, d=128; 16 sampled sequences checked per split count."""
     x = decode_inputs_for(PAGED)
     seqs = list(range(0, 64, 4))
-    for ns in PAGED.num_splits:
+    for ns in PAGED.num_splits + (0,):
         compare(attn, x, PAGED.scale, gpu, f"paged ns={ns}", seqs=seqs, num_splits=ns)
 
 
-@pytest.mark.parametrize("span", LONGCTX.split_tokens)
+@pytest.mark.parametrize("span", LONGCTX.split_tokens + (0,))
 def test_longctx_config_full_size(attn, gpu, span):
-    """8 sequences up to 122,863 tokens, Hq=16, Hkv=2, d=256, scale 2^-4; two sequences checked."""
+    """8 sequences up to 122,863 tokens, Hq=16, Hkv=2, d=256, scale 2^-4; two sequences checked.
+
+    span 0 is balanced mode."""
     x = decode_inputs_for(LONGCTX)
     compare(attn, x, LONGCTX.scale, gpu, f"longctx span={span}", seqs=[2, 7], split_tokens=span)
 
