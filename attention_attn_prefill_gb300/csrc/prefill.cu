@@ -27,9 +27,15 @@
 //     O is rescaled only when the row max has grown by more than 2^8 since it
 //     was last applied -- exact either way, because O and l always refer to
 //     the same max;
-//   * the epilogue adds the two halves of l, divides, rounds to bf16, stages
-//     the tile in shared memory (128B swizzle) and stores it with TMA while
-//     the next tile starts; LSE = m*scale + ln(l) (Step 8).
+//   * at the end of a tile the softmax warps add the two halves of l, write
+//     LSE = m*scale + ln(l) and hand l to a fourth warpgroup, then go straight
+//     on to the next tile.  That epilogue warpgroup (one thread per row) waits
+//     for the last P_j V_j, reads O out of TMEM, releases it for the next
+//     tile's first product, divides by l, rounds to bf16 and stores the tile
+//     with TMA through a 128B-swizzled staging panel (Step 8).  Tile
+//     boundaries therefore cost the softmax warps almost nothing.
+//   * the first tile's Q, K and V loads are issued by the thread that sets up
+//     the barriers, before the CTA-wide barrier and the TMEM allocation.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -50,11 +56,12 @@ constexpr int BN = 128;          // keys per K/V tile
 constexpr int NSB = 3;           // S buffers in TMEM
 constexpr int K_STAGES = 2;      // K_j is free as soon as S_j is done, long before it is reloaded
 constexpr int V_STAGES = 3;      // V_j is held until P_j V_j is done
-constexpr int NUM_THREADS = 384; // 8 softmax warps, 2 TMA warps, 2 MMA warps
+constexpr int NUM_THREADS = 512; // 8 softmax warps, 2 TMA warps, 2 MMA warps, 4 epilogue warps
 constexpr int PRODUCER_WARP = 8; // loads Q and streams K
 constexpr int V_WARP = 11;       // streams V
 constexpr int MMA_WARP = 9;      // issues S = Q K^T, owns the TMEM allocation
 constexpr int PV_WARP = 10;      // issues O += P V
+constexpr int EPI_WARP0 = 12;    // warps 12..15: epilogue, one thread per row
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t O_COL = NSB * 128;  // O accumulator columns start here
 constexpr float RESCALE_LOG2_THRESHOLD = 8.0f;
@@ -67,12 +74,14 @@ struct Layout {
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + TILE_BYTES;
   static constexpr int V_OFF = K_OFF + K_STAGES * TILE_BYTES;
-  static constexpr int OST_OFF = V_OFF + V_STAGES * TILE_BYTES;   // output staging tile
-  static constexpr int RED_OFF = OST_OFF + TILE_BYTES;            // [2 buffers][2 halves][128] floats
-  static constexpr int BAR_OFF = RED_OFF + 2 * 2 * 128 * 4;
+  static constexpr int OST_OFF = V_OFF + V_STAGES * TILE_BYTES;   // output staging: one 64-column panel
+  static constexpr int RED_OFF = OST_OFF + CHUNK_BYTES;           // row-max exchange [2 buffers][2 halves][128]
+  static constexpr int XL_OFF = RED_OFF + 2 * 2 * 128 * 4;        // row-sum exchange [2 halves][128]
+  static constexpr int LROW_OFF = XL_OFF + 2 * 128 * 4;           // l handed to the epilogue [2 tiles][128]
+  static constexpr int BAR_OFF = LROW_OFF + 2 * 128 * 4;
   // q_full, q_empty, k_full[2], k_empty[2], v_full[3], v_empty[3], s_full[3], p_full[3], pv_done[3],
-  // o_full, o_free, mma_done[2]
-  static constexpr int NUM_BARS = 2 + 2 * 2 + 5 * 3 + 4;
+  // o_full, o_free, mma_done[2], l_full[2], l_empty[2]
+  static constexpr int NUM_BARS = 2 + 2 * 2 + 5 * 3 + 4 + 4;
   static constexpr int SLOT_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int USED = SLOT_OFF + 16;
   // The dynamic shared memory window starts 1 KB-aligned (checked at run time); never below
@@ -111,6 +120,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* sV = smem + L::V_OFF;
   uint8_t* sO = smem + L::OST_OFF;
   float* red = reinterpret_cast<float*>(smem + L::RED_OFF);
+  float* xl = reinterpret_cast<float*>(smem + L::XL_OFF);
+  float* lrow = reinterpret_cast<float*>(smem + L::LROW_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
@@ -124,12 +135,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* o_full = bars + 21;
   uint64_t* o_free = bars + 22;    // the epilogue has read O out of TMEM
   uint64_t* mma_done = bars + 23;  // [2]: each issuer's last MMA done
+  uint64_t* l_full = bars + 25;    // [2]: a tile's row sums are in lrow
+  uint64_t* l_empty = bars + 27;   // [2]: the epilogue has read them
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::SLOT_OFF);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int G = p.Hq / p.Hkv;
+  auto tile_nkv = [&](int qt) { return p.causal ? (qt + 1) : p.n_kv_total; };
+  // loads of the first tile that are issued before the CTA barrier: Q, and as many K and V
+  // tiles as the rings hold
+  auto first_loads = [&](int nst) {
+    int b, hq, qt;
+    if (!tile_of(p, 0, b, hq, qt)) return 0;
+    const int n = tile_nkv(qt);
+    return n < nst ? n : nst;
+  };
 
-  if (threadIdx.x == 0) {
+  if (warp == PRODUCER_WARP && lane == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int s = 0; s < K_STAGES; ++s) {
@@ -144,10 +167,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&pv_done[s], 1);
     }
     mbar_init(o_full, 1);
-    mbar_init(o_free, 256);
+    mbar_init(o_free, 128);
     mbar_init(&mma_done[0], 1);
     mbar_init(&mma_done[1], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&l_full[s], 128);
+      mbar_init(&l_empty[s], 128);
+    }
     fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
+    int b, hq, qt;
+    if (tile_of(p, 0, b, hq, qt)) {
+      const int g = hq / G;
+      mbar_arrive_expect_tx(q_full, L::TILE_BYTES);
+      for (int c = 0; c < L::CHUNKS; ++c) tma_load_3d(sQ + c * CHUNK_BYTES, &tm_q, q_full, hq * D + c * 64, qt * BM, b);
+      const int nk = first_loads(K_STAGES), nv = first_loads(V_STAGES);
+      for (int j = 0; j < nk; ++j) {
+        mbar_arrive_expect_tx(&k_full[j], L::TILE_BYTES);
+        for (int c = 0; c < L::CHUNKS; ++c)
+          tma_load_3d(sK + j * L::TILE_BYTES + c * CHUNK_BYTES, &tm_k, &k_full[j], g * D + c * 64, j * BN, b);
+      }
+      for (int j = 0; j < nv; ++j) {
+        mbar_arrive_expect_tx(&v_full[j], L::TILE_BYTES);
+        for (int c = 0; c < L::CHUNKS; ++c)
+          tma_load_3d(sV + j * L::TILE_BYTES + c * CHUNK_BYTES, &tm_v, &v_full[j], g * D + c * 64, j * BN, b);
+      }
+    }
   }
   if (warp == MMA_WARP) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -157,8 +205,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int G = p.Hq / p.Hkv;
-  auto tile_nkv = [&](int qt) { return p.causal ? (qt + 1) : p.n_kv_total; };
 
   if (warp == PRODUCER_WARP || warp == V_WARP) {
     // ------------------------------------------------------------ TMA producers
@@ -171,26 +217,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint64_t* empty = is_k ? k_empty : v_empty;
       uint8_t* ring = is_k ? sK : sV;
       const CUtensorMap* map = is_k ? &tm_k : &tm_v;
-      tma_prefetch_desc(map);
-      if (is_k) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_o);
-      }
+      const int npre = first_loads(nst);
       bool ok = true;
-      int issued = 0, nq = 0;
+      int issued = npre, nq = 0;
       int b, hq, qt;
       for (int k = 0; ok && tile_of(p, k, b, hq, qt); ++k) {
         const int g = hq / G;
         if (is_k) {
           // Q of this tile replaces the previous one once all of its S = Q K^T products are done
-          if (k > 0 && !mbar_wait(q_empty, (k - 1) & 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(q_full, L::TILE_BYTES);
-          for (int c = 0; c < L::CHUNKS; ++c)
-            tma_load_3d(sQ + c * CHUNK_BYTES, &tm_q, q_full, hq * D + c * 64, qt * BM, b);
+          if (k > 0) {
+            if (!mbar_wait(q_empty, (k - 1) & 1)) { ok = false; break; }
+            mbar_arrive_expect_tx(q_full, L::TILE_BYTES);
+            for (int c = 0; c < L::CHUNKS; ++c)
+              tma_load_3d(sQ + c * CHUNK_BYTES, &tm_q, q_full, hq * D + c * 64, qt * BM, b);
+          }
           nq = k + 1;
         }
         const int nkv = tile_nkv(qt);
-        for (int j = 0; j < nkv; ++j) {
+        for (int j = (k == 0 ? npre : 0); j < nkv; ++j) {
           const int st = issued % nst;
           if (!mbar_wait(&empty[st], ((issued / nst) & 1) ^ 1)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[st], L::TILE_BYTES);
@@ -281,9 +325,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       umma_commit(&mma_done[1]);
       if (!mbar_wait(&mma_done[1], 0)) set_error(&g_prefill_status, kDevWaitTimeout);
     }
-  } else {
-    // ------------------------------------------------------------ softmax + epilogue
-    const int h = warp >> 2;                  // which half of the key columns / of O
+  } else if (warp < PRODUCER_WARP) {
+    // ------------------------------------------------------------ softmax
+    // A wait that runs out of time clears `ok`; the warp then skips its remaining waits but
+    // keeps the named-barrier schedule, so no other warp is left at a barrier.
+    const int h = warp >> 2;                  // which half of the key columns
     const int row = (warp & 3) * 32 + lane;   // TMEM lane = query row within the tile
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t o_half = tmem + lane_base + O_COL + h * (D / 2);
@@ -292,30 +338,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     int gs = 0;
     int b, hq, qt;
-    for (int k = 0; ok && tile_of(p, k, b, hq, qt); ++k) {
-      const int q0 = qt * BM;
-      const int q = q0 + row;
+    for (int k = 0; tile_of(p, k, b, hq, qt); ++k) {
+      const int q = qt * BM + row;
       const int nkv = tile_nkv(qt);
       float m_used = -INFINITY;  // raw-score max that O and l currently refer to
       float l_part = 0.f;        // this half's share of the row sum
       for (int j = 0; j < nkv; ++j, ++gs) {
         const int sb = gs % NSB;
         const uint32_t s_tmem = tmem + lane_base + sb * 128;
-        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (gs / NSB) & 1));
-        if (!ok) break;
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (gs / NSB) & 1));
         tc_fence_after();
         uint32_t sr[2][32];
         tmem_ld32(s_tmem + h * 64, sr[0]);
         tmem_ld32(s_tmem + h * 64 + 32, sr[1]);
         tmem_ld_wait();
-        const bool need_mask = (p.causal && j == nkv - 1) || (j == p.n_kv_total - 1 && (p.S % BN) != 0);
-        if (need_mask) {
-          const int key0 = j * BN + h * 64;
+        // last visible column of this thread's 64 keys: the causal diagonal and the end of the
+        // sequence are the only places where it is below 63
+        const int key0 = j * BN + h * 64;
+        int lim = 63;
+        if (p.causal && j == nkv - 1) lim = q - key0;
+        if (j == p.n_kv_total - 1 && p.S - 1 - key0 < lim) lim = p.S - 1 - key0;
+        if (lim < 63) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const int key = key0 + c;
-            if ((p.causal && key > q) || key >= p.S) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
-          }
+          for (int c = 0; c < 64; ++c)
+            if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
         }
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -365,8 +411,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_st32(s_tmem + h * 32, pk);
         if (__any_sync(0xffffffffu, rescale_o)) {
           // O must hold P V of the previous step before it is rescaled
-          ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(gs - 1) % NSB], ((gs - 1) / NSB) & 1));
-          if (!ok) break;
+          if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(gs - 1) % NSB], ((gs - 1) / NSB) & 1));
           tc_fence_after();
 #pragma unroll 1
           for (int c4 = 0; c4 < D / 64; ++c4) {
@@ -382,51 +427,69 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_before();
         mbar_arrive(&p_full[sb]);
       }
-      if (!ok) break;
-      // ---- epilogue: l = both halves; O / l -> bf16 -> staging smem (128B swizzle) -> TMA store
-      ok = __all_sync(0xffffffffu, mbar_wait(o_full, k & 1));
-      if (!ok) break;
-      tc_fence_after();
-      // the l exchange uses the buffer the next step will use; the staging barrier below
-      // separates it from that step's writes
-      float* xl = red + (gs & 1) * 256;
+      // ---- end of tile: add the halves of l, write LSE, hand l to the epilogue warps.  xl is
+      // next written at the end of the next tile, after at least one more max exchange.
       xl[h * 128 + row] = l_part;
-      uint32_t ov[D / 64][32];
-#pragma unroll
-      for (int c4 = 0; c4 < D / 64; ++c4) tmem_ld32(o_half + c4 * 32, ov[c4]);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(o_free);  // the next tile's first P.V may overwrite O now
-      if (threadIdx.x == 0) tma_store_wait_read0();  // the previous tile's store has read the staging tile
       named_barrier_sync(1, 256);
-      const float l = xl[row] + xl[128 + row];
-      const float inv_l = 1.f / l;
-#pragma unroll
-      for (int c4 = 0; c4 < D / 64; ++c4) {
-        const int col0 = h * (D / 2) + c4 * 32;   // first output column of this chunk
-        uint8_t* panel = sO + (col0 >> 6) * CHUNK_BYTES + row * 128;
-        const int u0 = (col0 & 63) >> 3;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(ov[c4][8 * u + 0]) * inv_l, __uint_as_float(ov[c4][8 * u + 1]) * inv_l);
-          w.y = pack_bf16x2(__uint_as_float(ov[c4][8 * u + 2]) * inv_l, __uint_as_float(ov[c4][8 * u + 3]) * inv_l);
-          w.z = pack_bf16x2(__uint_as_float(ov[c4][8 * u + 4]) * inv_l, __uint_as_float(ov[c4][8 * u + 5]) * inv_l);
-          w.w = pack_bf16x2(__uint_as_float(ov[c4][8 * u + 6]) * inv_l, __uint_as_float(ov[c4][8 * u + 7]) * inv_l);
-          *reinterpret_cast<uint4*>(panel + (((u0 + u) ^ (row & 7)) << 4)) = w;
-        }
-      }
-      if (h == 0 && p.lse != nullptr && q < p.S)
-        p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.S + q] = m_used * p.scale + logf(l);
-      fence_proxy_async_smem();
-      named_barrier_sync(1, 256);
-      if (threadIdx.x == 0) {
-        for (int c = 0; c < L::CHUNKS; ++c) tma_store_3d(&tm_o, sO + c * CHUNK_BYTES, hq * D + c * 64, q0, b);
-        tma_store_commit();
+      if (h == 0) {
+        const float l = xl[row] + xl[128 + row];
+        if (p.lse != nullptr && q < p.S) p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.S + q] = m_used * p.scale + logf(l);
+        const int tb = k & 1;
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&l_empty[tb], ((k >> 1) & 1) ^ 1));
+        lrow[tb * 128 + row] = l;
+        mbar_arrive(&l_full[tb]);
       }
     }
     if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
-    if (threadIdx.x == 0) tma_store_wait0();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // One thread per row: wait for the tile's last P.V, read O out of TMEM (bf16 pairs after
+    // the division by l), release O, then store 64-column panels through the staging buffer.
+    const int row = (warp & 3) * 32 + lane;
+    const int et = threadIdx.x - EPI_WARP0 * 32;
+    const uint32_t o_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + O_COL;
+    bool ok = true;
+    int b, hq, qt;
+    for (int k = 0; tile_of(p, k, b, hq, qt); ++k) {
+      const int tb = k & 1;
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&l_full[tb], (k >> 1) & 1));
+      const float inv_l = 1.f / lrow[tb * 128 + row];
+      mbar_arrive(&l_empty[tb]);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_full, k & 1));
+      tc_fence_after();
+      uint32_t ob[D / 2];
+#pragma unroll
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        uint32_t r[32];
+        tmem_ld32(o_row + c4 * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          ob[c4 * 16 + c] = pack_bf16x2(__uint_as_float(r[2 * c]) * inv_l, __uint_as_float(r[2 * c + 1]) * inv_l);
+      }
+      tc_fence_before();
+      mbar_arrive(o_free);  // the next tile's first P.V may overwrite O now
+      uint8_t* line = sO + row * 128;
+#pragma unroll
+      for (int c = 0; c < L::CHUNKS; ++c) {
+        if (et == 0) tma_store_wait_read0();  // the previous panel's store has read the staging buffer
+        named_barrier_sync(2, 128);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 w = make_uint4(ob[32 * c + 4 * u], ob[32 * c + 4 * u + 1], ob[32 * c + 4 * u + 2],
+                                     ob[32 * c + 4 * u + 3]);
+          *reinterpret_cast<uint4*>(line + ((u ^ (row & 7)) << 4)) = w;
+        }
+        fence_proxy_async_smem();
+        named_barrier_sync(2, 128);
+        if (et == 0) {
+          tma_store_3d(&tm_o, sO, hq * D + c * 64, qt * BM, b);
+          tma_store_commit();
+        }
+      }
+    }
+    if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
+    if (et == 0) tma_store_wait0();
   }
 
   __syncwarp();  // single-lane roles rejoin their warps before the CTA barrier
