@@ -163,16 +163,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 256);
+      mbar_init(&p_full[s], 8);   // one arrival per softmax warp
       mbar_init(&pv_done[s], 1);
     }
     mbar_init(o_full, 1);
-    mbar_init(o_free, 128);
+    mbar_init(o_free, 4);          // one arrival per epilogue warp
     mbar_init(&mma_done[0], 1);
     mbar_init(&mma_done[1], 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&l_full[s], 128);
-      mbar_init(&l_empty[s], 128);
+      mbar_init(&l_full[s], 4);
+      mbar_init(&l_empty[s], 4);
     }
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -425,7 +425,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&p_full[sb]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[sb]);  // one arrival per warp: 256 would queue on the barrier
       }
       // ---- end of tile: add the halves of l, write LSE, hand l to the epilogue warps.  xl is
       // next written at the end of the next tile, after at least one more max exchange.
@@ -437,7 +438,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int tb = k & 1;
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&l_empty[tb], ((k >> 1) & 1) ^ 1));
         lrow[tb * 128 + row] = l;
-        mbar_arrive(&l_full[tb]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&l_full[tb]);
       }
     }
     if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
@@ -454,7 +456,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int tb = k & 1;
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&l_full[tb], (k >> 1) & 1));
       const float inv_l = 1.f / lrow[tb * 128 + row];
-      mbar_arrive(&l_empty[tb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&l_empty[tb]);
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_full, k & 1));
       tc_fence_after();
       uint32_t ob[D / 2];
@@ -468,7 +471,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ob[c4 * 16 + c] = pack_bf16x2(__uint_as_float(r[2 * c]) * inv_l, __uint_as_float(r[2 * c + 1]) * inv_l);
       }
       tc_fence_before();
-      mbar_arrive(o_free);  // the next tile's first P.V may overwrite O now
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);  // the next tile's first P.V may overwrite O now
       uint8_t* line = sO + row * 128;
 #pragma unroll
       for (int c = 0; c < L::CHUNKS; ++c) {
