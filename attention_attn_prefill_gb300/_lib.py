@@ -47,6 +47,8 @@ _SIGNATURES = {
     "attn_combine": (c_int, [c_void_p] * 3 + [c_int] * 3 + [c_void_p, c_void_p, c_void_p]),
     "attn_decode_paged_noalloc": (c_int, [c_void_p] * 7 + [c_int] * 9 + [c_float, c_void_p]),
     "attn_device_status": (c_int, [c_u32_p, c_int]),
+    "attn_split_heuristic": (c_int, [c_int] * 4),
+    "attn_decode_auto_splits": (c_int, [c_int] * 4),
 }
 
 
@@ -129,6 +131,19 @@ def decode_workspace_bytes(num_seqs: int, Hq: int, d: int, slots: int) -> int:
     return int(lib().attn_decode_workspace_bytes(num_seqs, Hq, d, slots))
 
 
+def split_heuristic(units: int, capacity: int, blocks: int, max_splits: int = 128) -> int:
+    """The split-count rule restated in C (host arithmetic only); 0 for invalid arguments."""
+    return int(lib().attn_split_heuristic(units, capacity, blocks, max_splits))
+
+
+def decode_auto_splits(num_seqs: int, Hkv: int, d: int, max_blocks_per_seq: int) -> int:
+    """Split count the rule picks for the split kernel on the current device."""
+    n = int(lib().attn_decode_auto_splits(num_seqs, Hkv, d, max_blocks_per_seq))
+    if n < 1:
+        raise AttnError(1, "attn_decode_auto_splits")
+    return n
+
+
 def decode_balanced_workspace_bytes(num_seqs: int, Hq: int, Hkv: int, d: int) -> int:
     return int(lib().attn_decode_balanced_workspace_bytes(num_seqs, Hq, Hkv, d))
 
@@ -139,7 +154,8 @@ def decode_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, 
                  workspace: torch.Tensor | None = None, stream=None):
     """Paged split-KV decode: q [N,Hq,d]; caches [num_blocks,16,Hkv,d] bf16 -> (o [N,Hq,d], lse [N,Hq]).
 
-    num_splits=0 with split_tokens=0 selects balanced mode (equal page shares per worker warp).
+    num_splits=0 with split_tokens=0 selects balanced mode (equal page shares per worker warp);
+    num_splits="auto" takes the count decode_auto_splits picks.
     """
     N, Hq, d = q.shape
     num_blocks, page, Hkv, dk = k_cache.shape
@@ -150,6 +166,8 @@ def decode_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, 
     max_blocks = block_table.shape[1]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    if num_splits == "auto":
+        num_splits = decode_auto_splits(N, Hkv, d, max_blocks)
     if num_splits == 0 and split_tokens == 0:
         need = int(lib().attn_decode_balanced_workspace_bytes(N, Hq, Hkv, d))   # balanced mode
         if need == 0:

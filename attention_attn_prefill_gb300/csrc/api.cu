@@ -16,6 +16,7 @@ namespace {
 
 constexpr int kVersion = 100;  // 0.1.0
 constexpr int kPage = 16;
+constexpr int kAutoMaxSplits = 128;  // largest split count the automatic choice considers
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -114,6 +115,35 @@ int attn_decode_num_slots(int max_blocks_per_seq, int page_size, int num_splits,
   }
   if (split_tokens < 0 || num_splits < 1) return 0;
   return num_splits < max_blocks_per_seq ? num_splits : max_blocks_per_seq;
+}
+
+int attn_split_heuristic(int units, int capacity, int blocks, int max_splits) {
+  if (units < 1 || capacity < 1 || blocks < 1 || max_splits < 1) return 0;
+  int limit = max_splits < capacity ? max_splits : capacity;
+  if (blocks < limit) limit = blocks;
+  auto per_group = [&](int c) { return (blocks + c - 1) / c; };
+  auto efficiency = [&](int c) {
+    const double w = static_cast<double>(units) * c / capacity;
+    return w / std::ceil(w);
+  };
+  // a count is a candidate only if it changes the number of blocks per group
+  auto candidate = [&](int c) { return c == 1 || per_group(c) != per_group(c - 1); };
+  double best = 0.0;
+  for (int c = 1; c <= limit; ++c)
+    if (candidate(c) && efficiency(c) > best) best = efficiency(c);
+  for (int c = 1; c <= limit; ++c)
+    if (candidate(c) && efficiency(c) >= 0.85 * best) return c;
+  return 1;
+}
+
+int attn_decode_auto_splits(int num_seqs, int Hkv, int d, int max_blocks_per_seq) {
+  if (num_seqs < 1 || Hkv < 1 || max_blocks_per_seq < 1 || (d != 128 && d != 256)) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  const int per_sm = attn::decode_split_ctas_per_sm(d);
+  if (per_sm < 1) return 0;
+  return attn_split_heuristic(num_seqs * Hkv, sms * per_sm, max_blocks_per_seq, kAutoMaxSplits);
 }
 
 size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d, int slots) {

@@ -860,7 +860,23 @@ cudaError_t launch_split(const DecodeMaps& m, const DecodeParams& p, cudaStream_
   return cudaGetLastError();
 }
 
+template <int D, int NW, int NS>
+int split_ctas_per_sm() {
+  auto kern = decode_split_kernel<D, NW, NS>;
+  const int smem = DLayout<D, NW, NS>::ALLOC;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, NW * 32, smem) != cudaSuccess) return 0;
+  return n;
+}
+
 }  // namespace
+
+int decode_split_ctas_per_sm(int d) {
+  if (d == 128) return split_ctas_per_sm<128, 4, 3>();
+  if (d == 256) return split_ctas_per_sm<256, 4, 3>();
+  return 0;
+}
 
 cudaError_t decode_split_launch(int d, const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream) {
   if (d == 128) return launch_split<128, 4, 3>(maps, p, stream);

@@ -56,6 +56,7 @@ int decode_balanced_warps(int d);  // worker warps of the split grid on the curr
 cudaError_t decode_balanced_launch(int d, const DecodeMaps& maps, const BalancedParams& p, cudaStream_t stream);
 
 cudaError_t decode_split_launch(int d, const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream);
+int decode_split_ctas_per_sm(int d);  // resident split-kernel CTAs per SM on the current device (0 on error)
 cudaError_t combine_launch(int d, const float* part_o, const float* part_m, const float* part_l, int rows,
                            int splits, void* o, float* lse, cudaStream_t stream);
 cudaError_t decode_status(uint32_t* out, bool clear);

@@ -90,6 +90,32 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
 int attn_decode_num_slots(int max_blocks_per_seq, int page_size, int num_splits, int split_tokens);
 
 /*
+ * Split-count rule of "Why your local LLM feels dumber than it is" (Part
+ * 3.14), section "Why FlashAttention 2 selects 54, 62, or 87 groups": among
+ * c = 1 .. min(max_splits, capacity, blocks), a count is a candidate when it
+ * changes ceil(blocks / c) compared with c - 1 (c = 1 always is); its
+ * estimated efficiency is w / ceil(w) with w = units * c / capacity; the
+ * smallest candidate whose efficiency is at least 85% of the best one wins.
+ *   units      independent work items per split (sequences x KV heads)
+ *   capacity   work items the device runs at once
+ *   blocks     key/value blocks of the longest sequence
+ * Pure host arithmetic (no CUDA call).  With units = 4, capacity = 2 x SMs and
+ * blocks = 431 it gives the page's 54 / 62 / 87 for 132 / 148 / 188 SMs.
+ * Returns 0 for invalid arguments.
+ */
+int attn_split_heuristic(int units, int capacity, int blocks, int max_splits);
+
+/*
+ * The same rule restated for this library's split kernel on the current
+ * device: units = num_seqs * Hkv, capacity = SMs x resident split-kernel CTAs
+ * per SM, blocks = max_blocks_per_seq (16-token pages), at most 128 splits.
+ * Pass the result as num_splits to attn_decode_paged (and to
+ * attn_decode_num_slots for the workspace size).  Returns 0 for invalid
+ * arguments or when no CUDA device can be queried.
+ */
+int attn_decode_auto_splits(int num_seqs, int Hkv, int d, int max_blocks_per_seq);
+
+/*
  * Bytes of workspace attn_decode_paged needs: num_seqs * Hq * slots * (d + 2)
  * floats when slots > 1, else 0.
  */

@@ -100,6 +100,15 @@ def test_balanced_many_short_sequences(attn, gpu):
     assert torch.all(o.cpu()[empty] == 0) and torch.all(torch.isneginf(lse.cpu()[empty]))
 
 
+def test_auto_split_count(attn, gpu):
+    """num_splits="auto": the split-count rule for this device, then the usual parity."""
+    lens = [3000, 17, 1234, 4096, 640]
+    x = make_decode_inputs(lens, Hq=32, Hkv=8, d=128, seed=60, nan_tail=True)
+    n = attn.decode_auto_splits(len(lens), 8, 128, x.block_table.shape[1])
+    assert 1 <= n <= 128
+    compare(attn, x, 0.09, gpu, f"auto ({n} splits)", num_splits="auto")
+
+
 def test_bad_page_is_reported(attn, gpu):
     """A block-table entry outside [0, num_blocks) is recorded as a device error, not read."""
     x = make_decode_inputs([40], Hq=4, Hkv=1, d=128, seed=57)
