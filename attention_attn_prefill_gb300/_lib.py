@@ -48,6 +48,7 @@ _SIGNATURES = {
     "attn_decode_paged_noalloc": (c_int, [c_void_p] * 7 + [c_int] * 9 + [c_float, c_void_p]),
     "attn_device_status": (c_int, [c_u32_p, c_int]),
     "attn_split_heuristic": (c_int, [c_int] * 4),
+    "attn_prefill_varlen": (c_int, [c_void_p] * 6 + [c_int] * 6 + [c_float, c_int, c_void_p]),
     "attn_decode_auto_splits": (c_int, [c_int] * 4),
 }
 
@@ -119,6 +120,31 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
         _dev(out, torch.bfloat16, "out"), _dev(lse, torch.float32, "lse") if lse is not None else None,
         B, Hq, Hkv, S, d, float(scale), 1 if causal else 0, _stream_handle(stream))
     _check(st, "attn_prefill")
+    return out, lse
+
+
+def prefill_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor, max_seqlen: int,
+                   scale: float | None = None, causal: bool = True, out: torch.Tensor | None = None,
+                   lse: torch.Tensor | None = None, return_lse: bool = True, stream=None):
+    """Packed sequences: q [T,Hq,d], k/v [T,Hkv,d] bf16, cu_seqlens [N+1] int32 -> (o [T,Hq,d], lse [Hq,T])."""
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (T, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [total_tokens, Hkv, d] matching q")
+    if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens must be [num_seqs + 1]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    st = lib().attn_prefill_varlen(
+        _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
+        _dev(out, torch.bfloat16, "out"), _dev(lse, torch.float32, "lse") if lse is not None else None,
+        _dev(cu_seqlens, torch.int32, "cu_seqlens"), cu_seqlens.numel() - 1, int(max_seqlen), T, Hq, Hkv, d,
+        float(scale), 1 if causal else 0, _stream_handle(stream))
+    _check(st, "attn_prefill_varlen")
     return out, lse
 
 

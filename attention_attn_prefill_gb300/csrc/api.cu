@@ -69,41 +69,65 @@ const char* attn_status_string(attn_status_t s) {
 
 int attn_version(void) { return kVersion; }
 
-attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                           int S, int d, float scale, int causal, void* stream) {
+namespace {
+
+// Shared by both prefill entry points: `batch` sequences of `rows` tokens each in the maps (one
+// packed batch of `rows` tokens for packed sequences).
+attn_status_t prefill_common(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int Hq,
+                             int Hkv, int rows, int d, float scale, int causal, const int32_t* cu_seqlens,
+                             int num_seqs, int max_seqlen, void* stream) {
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (batch < 1 || rows < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   // TMA coordinates are int32 and each map dimension must stay below 2^32
-  if (static_cast<int64_t>(Hq) * d > (1 << 30) || S > (1 << 30) || B > 65535 || Hq > 65535)
+  if (static_cast<int64_t>(Hq) * d > (1 << 30) || rows > (1 << 30) || batch > 65535 || Hq > 65535 ||
+      num_seqs > (1 << 24))
     return ATTN_ERR_INVALID_ARG;
 
   attn::PrefillMaps maps;
   const uint64_t q_row = static_cast<uint64_t>(Hq) * d * 2, kv_row = static_cast<uint64_t>(Hkv) * d * 2;
-  const uint32_t rows = static_cast<uint32_t>(attn::prefill_tile_rows());
-  if (!encode_3d(&maps.q, q, static_cast<uint64_t>(Hq) * d, S, B, q_row, q_row * S, 64, rows, 1) ||
-      !encode_3d(&maps.k, k, static_cast<uint64_t>(Hkv) * d, S, B, kv_row, kv_row * S, 64, rows, 1) ||
-      !encode_3d(&maps.v, v, static_cast<uint64_t>(Hkv) * d, S, B, kv_row, kv_row * S, 64, rows, 1) ||
-      !encode_3d(&maps.o, o, static_cast<uint64_t>(Hq) * d, S, B, q_row, q_row * S, 64, rows, 1))
+  const uint32_t box = static_cast<uint32_t>(attn::prefill_tile_rows());
+  if (!encode_3d(&maps.q, q, static_cast<uint64_t>(Hq) * d, rows, batch, q_row, q_row * rows, 64, box, 1) ||
+      !encode_3d(&maps.k, k, static_cast<uint64_t>(Hkv) * d, rows, batch, kv_row, kv_row * rows, 64, box, 1) ||
+      !encode_3d(&maps.v, v, static_cast<uint64_t>(Hkv) * d, rows, batch, kv_row, kv_row * rows, 64, box, 1) ||
+      !encode_3d(&maps.o, o, static_cast<uint64_t>(Hq) * d, rows, batch, q_row, q_row * rows, 64, box, 1))
     return ATTN_ERR_CUDA;
 
   attn::PrefillParams p;
   p.lse = lse;
-  p.B = B;
+  p.o = o;
+  p.cu_seqlens = cu_seqlens;
+  p.B = cu_seqlens != nullptr ? num_seqs : batch;
   p.Hq = Hq;
   p.Hkv = Hkv;
-  p.S = S;
+  p.S = rows;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.causal = causal ? 1 : 0;
   const int per_cta = attn::prefill_rows_per_cta();
-  p.num_qblocks = (S + per_cta - 1) / per_cta;
-  p.n_kv_total = (S + 127) / 128;
+  const int longest = cu_seqlens != nullptr ? max_seqlen : rows;
+  p.num_qblocks = (longest + per_cta - 1) / per_cta;
   if (p.num_qblocks > 65535) return ATTN_ERR_INVALID_ARG;
   return from_cuda(attn::prefill_launch(d, maps, p, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                           int S, int d, float scale, int causal, void* stream) {
+  return prefill_common(q, k, v, o, lse, B, Hq, Hkv, S, d, scale, causal, nullptr, 0, 0, stream);
+}
+
+attn_status_t attn_prefill_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                                  const int32_t* cu_seqlens, int num_seqs, int max_seqlen, int total_tokens, int Hq,
+                                  int Hkv, int d, float scale, int causal, void* stream) {
+  if (cu_seqlens == nullptr || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (num_seqs < 1 || max_seqlen < 1 || total_tokens < 1) return ATTN_ERR_INVALID_ARG;
+  return prefill_common(q, k, v, o, lse, 1, Hq, Hkv, total_tokens, d, scale, causal, cu_seqlens, num_seqs,
+                        max_seqlen, stream);
 }
 
 int attn_decode_num_slots(int max_blocks_per_seq, int page_size, int num_splits, int split_tokens) {

@@ -90,19 +90,49 @@ struct Layout {
   static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
-// Work tile number k of this CTA: a longest-first order dealt out in a zigzag over the CTAs.
-__device__ __forceinline__ bool tile_of(const PrefillParams& p, int k, int& b, int& hq, int& qt) {
-  const int G = gridDim.x;
-  const int c = blockIdx.x;
-  const int idx = k * G + ((k & 1) ? (G - 1 - c) : c);
-  const int per_qt = p.B * p.Hq;
-  if (idx >= p.num_qblocks * per_qt) return false;
-  qt = p.num_qblocks - 1 - idx / per_qt;
-  const int rem = idx % per_qt;
-  hq = rem % p.Hq;
-  b = rem / p.Hq;
-  return true;
-}
+// One work tile: 128 query rows of one (sequence, query head).
+struct WorkTile {
+  int b, hq, qt;  // sequence, query head, query tile within the sequence
+  int base, z;    // row and batch coordinates of the sequence's first token in the maps
+  int len;        // tokens of the sequence
+};
+
+// Walks this CTA's work tiles.  Tiles (query tile, sequence, head) are ordered longest first (the
+// causal cost of a tile grows with its query tile) and dealt out in a zigzag over the CTAs.  A
+// packed sequence shorter than the longest one has no tiles at the top query-tile levels: every role
+// skips those alike, so all roles see the same list.
+struct TileWalk {
+  long long v = 0;
+  __device__ __forceinline__ bool next(const PrefillParams& p, WorkTile& t) {
+    const long long G = gridDim.x, c = blockIdx.x;
+    const long long per_qt = static_cast<long long>(p.B) * p.Hq;
+    const long long total = per_qt * p.num_qblocks;
+    while (true) {
+      const long long idx = v * G + ((v & 1) ? (G - 1 - c) : c);
+      ++v;
+      if (idx >= total) return false;
+      t.qt = p.num_qblocks - 1 - static_cast<int>(idx / per_qt);
+      const long long rem = idx % per_qt;
+      t.hq = static_cast<int>(rem % p.Hq);
+      t.b = static_cast<int>(rem / p.Hq);
+      if (p.cu_seqlens == nullptr) {
+        t.base = 0;
+        t.z = t.b;
+        t.len = p.S;
+        return true;
+      }
+      const int s0 = p.cu_seqlens[t.b], s1 = p.cu_seqlens[t.b + 1];
+      if (s0 < 0 || s1 < s0 || s1 > p.S || s1 - s0 > p.num_qblocks * BM) {
+        set_error(&g_prefill_status, kDevBadSeqlens);
+        continue;  // the sequence is skipped
+      }
+      t.base = s0;
+      t.z = 0;
+      t.len = s1 - s0;
+      if (t.qt * BM < t.len) return true;
+    }
+  }
+};
 
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -142,13 +172,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.Hq / p.Hkv;
-  auto tile_nkv = [&](int qt) { return p.causal ? (qt + 1) : p.n_kv_total; };
+  auto kv_tiles = [&](const WorkTile& t) { return (t.len + BN - 1) / BN; };
+  auto tile_nkv = [&](const WorkTile& t) { return p.causal ? (t.qt + 1) : kv_tiles(t); };
   // loads of the first tile that are issued before the CTA barrier: Q, and as many K and V
   // tiles as the rings hold
   auto first_loads = [&](int nst) {
-    int b, hq, qt;
-    if (!tile_of(p, 0, b, hq, qt)) return 0;
-    const int n = tile_nkv(qt);
+    TileWalk w;
+    WorkTile t;
+    if (!w.next(p, t)) return 0;
+    const int n = tile_nkv(t);
     return n < nst ? n : nst;
   };
 
@@ -179,21 +211,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_o);
-    int b, hq, qt;
-    if (tile_of(p, 0, b, hq, qt)) {
-      const int g = hq / G;
+    TileWalk w;
+    WorkTile t;
+    if (w.next(p, t)) {
+      const int g = t.hq / G;
       mbar_arrive_expect_tx(q_full, L::TILE_BYTES);
-      for (int c = 0; c < L::CHUNKS; ++c) tma_load_3d(sQ + c * CHUNK_BYTES, &tm_q, q_full, hq * D + c * 64, qt * BM, b);
+      for (int c = 0; c < L::CHUNKS; ++c)
+        tma_load_3d(sQ + c * CHUNK_BYTES, &tm_q, q_full, t.hq * D + c * 64, t.base + t.qt * BM, t.z);
       const int nk = first_loads(K_STAGES), nv = first_loads(V_STAGES);
       for (int j = 0; j < nk; ++j) {
         mbar_arrive_expect_tx(&k_full[j], L::TILE_BYTES);
         for (int c = 0; c < L::CHUNKS; ++c)
-          tma_load_3d(sK + j * L::TILE_BYTES + c * CHUNK_BYTES, &tm_k, &k_full[j], g * D + c * 64, j * BN, b);
+          tma_load_3d(sK + j * L::TILE_BYTES + c * CHUNK_BYTES, &tm_k, &k_full[j], g * D + c * 64, t.base + j * BN,
+                      t.z);
       }
       for (int j = 0; j < nv; ++j) {
         mbar_arrive_expect_tx(&v_full[j], L::TILE_BYTES);
         for (int c = 0; c < L::CHUNKS; ++c)
-          tma_load_3d(sV + j * L::TILE_BYTES + c * CHUNK_BYTES, &tm_v, &v_full[j], g * D + c * 64, j * BN, b);
+          tma_load_3d(sV + j * L::TILE_BYTES + c * CHUNK_BYTES, &tm_v, &v_full[j], g * D + c * 64, t.base + j * BN,
+                      t.z);
       }
     }
   }
@@ -220,26 +256,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int npre = first_loads(nst);
       bool ok = true;
       int issued = npre, nq = 0;
-      int b, hq, qt;
-      for (int k = 0; ok && tile_of(p, k, b, hq, qt); ++k) {
-        const int g = hq / G;
+      TileWalk walk;
+      WorkTile t;
+      for (int k = 0; ok && walk.next(p, t); ++k) {
+        const int g = t.hq / G;
         if (is_k) {
           // Q of this tile replaces the previous one once all of its S = Q K^T products are done
           if (k > 0) {
             if (!mbar_wait(q_empty, (k - 1) & 1)) { ok = false; break; }
             mbar_arrive_expect_tx(q_full, L::TILE_BYTES);
             for (int c = 0; c < L::CHUNKS; ++c)
-              tma_load_3d(sQ + c * CHUNK_BYTES, &tm_q, q_full, hq * D + c * 64, qt * BM, b);
+              tma_load_3d(sQ + c * CHUNK_BYTES, &tm_q, q_full, t.hq * D + c * 64, t.base + t.qt * BM, t.z);
           }
           nq = k + 1;
         }
-        const int nkv = tile_nkv(qt);
+        const int nkv = tile_nkv(t);
         for (int j = (k == 0 ? npre : 0); j < nkv; ++j) {
           const int st = issued % nst;
           if (!mbar_wait(&empty[st], ((issued / nst) & 1) ^ 1)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[st], L::TILE_BYTES);
           for (int c = 0; c < L::CHUNKS; ++c)
-            tma_load_3d(ring + st * L::TILE_BYTES + c * CHUNK_BYTES, map, &full[st], g * D + c * 64, j * BN, b);
+            tma_load_3d(ring + st * L::TILE_BYTES + c * CHUNK_BYTES, map, &full[st], g * D + c * 64, t.base + j * BN,
+                        t.z);
           ++issued;
         }
       }
@@ -258,10 +296,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t qbase = smem_u32(sQ);
       bool ok = true;
       int gs = 0;
-      int b, hq, qt;
-      for (int k = 0; ok && tile_of(p, k, b, hq, qt); ++k) {
+      TileWalk walk;
+      WorkTile t;
+      for (int k = 0; ok && walk.next(p, t); ++k) {
         if (!mbar_wait(q_full, k & 1)) { ok = false; break; }
-        const int nkv = tile_nkv(qt);
+        const int nkv = tile_nkv(t);
         for (int j = 0; j < nkv; ++j, ++gs) {
           const int sb = gs % NSB;
           const int st = gs % K_STAGES;
@@ -295,11 +334,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t o_tmem = tmem + O_COL;
       bool ok = true;
       int gs = 0;
-      int b, hq, qt;
-      for (int k = 0; ok && tile_of(p, k, b, hq, qt); ++k) {
+      TileWalk walk;
+      WorkTile t;
+      for (int k = 0; ok && walk.next(p, t); ++k) {
         // the first product of a tile overwrites O: the previous tile's epilogue must have read it
         if (k > 0 && !mbar_wait(o_free, (k - 1) & 1)) { ok = false; break; }
-        const int nkv = tile_nkv(qt);
+        const int nkv = tile_nkv(t);
         for (int j = 0; j < nkv; ++j, ++gs) {
           const int sb = gs % NSB;
           const int st = gs % V_STAGES;
@@ -337,10 +377,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint64_t c2x2 = f2_pack(c2, c2);
     bool ok = true;
     int gs = 0;
-    int b, hq, qt;
-    for (int k = 0; tile_of(p, k, b, hq, qt); ++k) {
-      const int q = qt * BM + row;
-      const int nkv = tile_nkv(qt);
+    TileWalk walk;
+    WorkTile t;
+    for (int k = 0; walk.next(p, t); ++k) {
+      const int q = t.qt * BM + row;  // query row within the sequence
+      const int nkv = tile_nkv(t);
+      const int nkv_all = kv_tiles(t);
       float m_used = -INFINITY;  // raw-score max that O and l currently refer to
       float l_part = 0.f;        // this half's share of the row sum
       for (int j = 0; j < nkv; ++j, ++gs) {
@@ -357,7 +399,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int key0 = j * BN + h * 64;
         int lim = 63;
         if (p.causal && j == nkv - 1) lim = q - key0;
-        if (j == p.n_kv_total - 1 && p.S - 1 - key0 < lim) lim = p.S - 1 - key0;
+        if (j == nkv_all - 1 && t.len - 1 - key0 < lim) lim = t.len - 1 - key0;
         if (lim < 63) {
 #pragma unroll
           for (int c = 0; c < 64; ++c)
@@ -434,7 +476,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       named_barrier_sync(1, 256);
       if (h == 0) {
         const float l = xl[row] + xl[128 + row];
-        if (p.lse != nullptr && q < p.S) p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.S + q] = m_used * p.scale + logf(l);
+        if (p.lse != nullptr && q < t.len)
+          p.lse[(static_cast<size_t>(t.z) * p.Hq + t.hq) * p.S + t.base + q] = m_used * p.scale + logf(l);
         const int tb = k & 1;
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&l_empty[tb], ((k >> 1) & 1) ^ 1));
         lrow[tb * 128 + row] = l;
@@ -447,12 +490,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ epilogue
     // One thread per row: wait for the tile's last P.V, read O out of TMEM (bf16 pairs after
     // the division by l), release O, then store 64-column panels through the staging buffer.
+    // The last tile of a packed sequence that ends inside it is written row by row instead, so
+    // that the rows of the next sequence are left alone.
     const int row = (warp & 3) * 32 + lane;
     const int et = threadIdx.x - EPI_WARP0 * 32;
     const uint32_t o_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + O_COL;
     bool ok = true;
-    int b, hq, qt;
-    for (int k = 0; tile_of(p, k, b, hq, qt); ++k) {
+    TileWalk walk;
+    WorkTile t;
+    for (int k = 0; walk.next(p, t); ++k) {
       const int tb = k & 1;
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&l_full[tb], (k >> 1) & 1));
       const float inv_l = 1.f / lrow[tb * 128 + row];
@@ -473,6 +519,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free);  // the next tile's first P.V may overwrite O now
+      if (p.cu_seqlens != nullptr && t.qt * BM + BM > t.len) {
+        if (t.qt * BM + row < t.len) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
+                                                (static_cast<size_t>(t.base + t.qt * BM + row) * p.Hq + t.hq) * D);
+#pragma unroll
+          for (int u = 0; u < D / 8; ++u) dst[u] = make_uint4(ob[4 * u], ob[4 * u + 1], ob[4 * u + 2], ob[4 * u + 3]);
+        }
+        continue;
+      }
       uint8_t* line = sO + row * 128;
 #pragma unroll
       for (int c = 0; c < L::CHUNKS; ++c) {
@@ -487,7 +542,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         fence_proxy_async_smem();
         named_barrier_sync(2, 128);
         if (et == 0) {
-          tma_store_3d(&tm_o, sO, hq * D + c * 64, qt * BM, b);
+          tma_store_3d(&tm_o, sO, t.hq * D + c * 64, t.base + t.qt * BM, t.z);
           tma_store_commit();
         }
       }

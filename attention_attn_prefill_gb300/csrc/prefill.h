@@ -8,20 +8,25 @@
 
 namespace attn {
 
-// TMA descriptors of one prefill call.  Q/O: [B][S][Hq*d], K/V: [B][S][Hkv*d]
-// (3-D maps, 64-element x 128-row boxes, 128-byte swizzle).
+// TMA descriptors of one prefill call.  Q/O: [B][S][Hq*d], K/V: [B][S][Hkv*d] (B = 1 for packed
+// sequences); 3-D maps, 64-element x 128-row boxes, 128-byte swizzle.
 struct PrefillMaps {
   CUtensorMap q, k, v, o;
 };
 
+// Two layouts share one kernel:
+//   * fixed length (cu_seqlens == null): B sequences of S tokens, maps [B][S][H*d], LSE [B][Hq][S];
+//   * packed (cu_seqlens != null): B sequences of cu_seqlens[n+1] - cu_seqlens[n] tokens stored
+//     back to back, S = total tokens, maps [1][S][H*d], LSE [Hq][S].
 struct PrefillParams {
-  float* lse;        // [B][Hq][S] or null
+  float* lse;                  // LSE (see above) or null
+  void* o;                     // output base (bf16), for the rows of a partial packed tile
+  const int32_t* cu_seqlens;   // [B + 1] or null
   int B, Hq, Hkv, S;
   float scale;       // natural-units score scale
   float scale_log2;  // scale * log2(e)
   int causal;
-  int num_qblocks;   // ceil(S / rows per CTA)
-  int n_kv_total;    // ceil(S / 128)
+  int num_qblocks;   // query tiles of the longest sequence: ceil(S or max_seqlen / 128)
 };
 
 int prefill_rows_per_cta();

@@ -25,6 +25,7 @@ enum DeviceError : uint32_t {
   kDevBadPage = 2,           // block_table entry outside [0, num_blocks)
   kDevBadSplit = 3,          // split geometry inconsistent with the launch
   kDevMisaligned = 4,        // dynamic shared memory not 1 KB-aligned
+  kDevBadSeqlens = 5,        // cu_seqlens not increasing, past the tokens, or longer than max_seqlen
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

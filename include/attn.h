@@ -79,6 +79,31 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
                            int Hkv, int S, int d, float scale, int causal, void* stream);
 
 /*
+ * Prefill forward over packed sequences of different lengths: the varlen
+ * attention call that "GPU Datapath: Where Every Byte Moves in One LLM
+ * Inference Step", section "Measuring the Real Kernels, One at a Time", says
+ * its attention cells dispatch (cumulative sequence offsets, one packed token
+ * dimension).
+ *   q, o       [total_tokens, Hq,  d] bf16 (o is output)
+ *   k, v       [total_tokens, Hkv, d] bf16
+ *   cu_seqlens [num_seqs + 1] int32, DEVICE memory: sequence n holds tokens
+ *              cu_seqlens[n] .. cu_seqlens[n+1]-1; cu_seqlens[0] = 0,
+ *              non-decreasing, cu_seqlens[num_seqs] <= total_tokens.
+ *   max_seqlen upper bound of every sequence length (host value; sizes the
+ *              work list).
+ *   lse        [Hq, total_tokens] f32 (output, may be NULL).
+ * Each sequence is attended on its own, exactly as attn_prefill does for one
+ * batch element (causal positions counted from the sequence's first token).
+ * Rows of o that belong to no sequence are not written.  A zero-length
+ * sequence has no rows.  A cu_seqlens entry that breaks the rules above is
+ * recorded as device status 5 and that sequence is skipped.
+ * d, Hq, Hkv, scale, causal and the arithmetic are as for attn_prefill.
+ */
+attn_status_t attn_prefill_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                                  const int32_t* cu_seqlens, int num_seqs, int max_seqlen, int total_tokens, int Hq,
+                                  int Hkv, int d, float scale, int causal, void* stream);
+
+/*
  * Number of partial slots per (sequence, query head) that attn_decode_paged
  * uses for the given split settings (1 means the split kernel writes the
  * output directly and needs no workspace).
@@ -216,7 +241,8 @@ attn_status_t attn_combine(const float* part_o, const float* part_m, const float
  * the first error code any kernel of this library recorded since the last
  * clear (0 = none; 1 = a pipeline wait timed out; 2 = block-table entry out of
  * range; 3 = a seq_len the block table cannot cover; 4 = shared memory not
- * 1 KB-aligned) and, if `clear` != 0, resets it.
+ * 1 KB-aligned; 5 = cu_seqlens decreasing, past total_tokens or longer than
+ * max_seqlen) and, if `clear` != 0, resets it.
  */
 attn_status_t attn_device_status(uint32_t* code, int clear);
 

@@ -84,6 +84,39 @@ def prefill(q, k, v, scale: float, causal: bool = True, *, heads=None, rows=None
     return o, lse
 
 
+def prefill_varlen(q, k, v, cu_seqlens, scale: float, causal: bool = True, *, heads=None,
+                   seqs=None) -> tuple[np.ndarray, np.ndarray]:
+    """Packed sequences, each attended on its own.
+
+    q [T,Hq,d], k/v [T,Hkv,d]; sequence n is tokens cu_seqlens[n] .. cu_seqlens[n+1]-1 and its
+    causal positions count from its first token.  Returns o [T,Hq,d] and lse [Hq,T] in float64;
+    tokens outside the sampled sequences/heads (or in no sequence) are NaN.  This is the varlen
+    attention call of "GPU Datapath: Where Every Byte Moves in One LLM Inference Step", section
+    "Measuring the Real Kernels, One at a Time", with the per-row definition of "What attention is
+    trying to calculate" ("Why your local LLM feels dumber than it is").
+    """
+    q, k, v = f64(q), f64(k), f64(v)
+    cu = [int(x) for x in (cu_seqlens.tolist() if isinstance(cu_seqlens, torch.Tensor) else cu_seqlens)]
+    T, Hq, _ = q.shape
+    Hkv = k.shape[1]
+    o = np.full((T, Hq, v.shape[2]), np.nan)
+    lse = np.full((Hq, T), np.nan)
+    heads = range(Hq) if heads is None else heads
+    seqs = range(len(cu) - 1) if seqs is None else seqs
+    for n in seqs:
+        s0, s1 = cu[n], cu[n + 1]
+        if s1 <= s0:
+            continue
+        pos = np.arange(s1 - s0)
+        visible = (pos[None, :] <= pos[:, None]) if causal else None
+        for hq in heads:
+            g = kv_head_of(hq, Hq, Hkv)
+            ob, lb = attend(q[s0:s1, hq, :], k[s0:s1, g, :], v[s0:s1, g, :], scale, visible)
+            o[s0:s1, hq, :] = ob
+            lse[hq, s0:s1] = lb
+    return o, lse
+
+
 class _PageView:
     """Indexing a cache page by page, widening each page to float64 on access."""
 

@@ -20,7 +20,7 @@ import scipy.special as sps
 import torch
 
 import oracle.attention as oa
-from workloads import make_decode_inputs, make_prefill_inputs, randn_bf16
+from workloads import make_decode_inputs, make_prefill_inputs, make_varlen_inputs, randn_bf16
 from workloads.teaching import teaching_scores_values
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -264,6 +264,47 @@ def check_brute_force_tiny():
                 assert abs(float(tot.ln()) - lse[0, h, i]) <= 1e-13 * (1 + abs(lse[0, h, i]))
 
 
+def check_varlen_matches_scipy():
+    """Packed sequences: each row against scipy's softmax over its own sequence's keys up to itself."""
+    lens = [5, 1, 0, 9, 3]
+    x = make_varlen_inputs(lens, Hq=4, Hkv=2, d=6, seed=31, extra=2)
+    o, lse = oa.prefill_varlen(x.q, x.k, x.v, x.cu_seqlens, 0.45, causal=True)
+    q, k, v = oa.f64(x.q), oa.f64(x.k), oa.f64(x.v)
+    cu = x.cu_seqlens.tolist()
+    for n in range(len(lens)):
+        for i in range(cu[n], cu[n + 1]):
+            for h in range(4):
+                s = 0.45 * k[cu[n]:i + 1, h // 2] @ q[i, h]
+                _close(o[i, h], sps.softmax(s) @ v[cu[n]:i + 1, h // 2], rtol=1e-12, atol=1e-13, what="varlen o")
+                _close(lse[h, i], sps.logsumexp(s), what="varlen lse")
+    assert np.isnan(o[-2:]).all() and np.isnan(lse[:, -2:]).all()   # tokens in no sequence
+
+
+def check_varlen_single_token_sequences():
+    """A one-token sequence returns its own value row exactly and lse = scale * q.k."""
+    x = make_varlen_inputs([1, 1, 1], Hq=2, Hkv=1, d=8, seed=32)
+    o, lse = oa.prefill_varlen(x.q, x.k, x.v, x.cu_seqlens, 0.7, causal=False)
+    q, k, v = oa.f64(x.q), oa.f64(x.k), oa.f64(x.v)
+    for t in range(3):
+        for h in range(2):
+            assert np.array_equal(o[t, h], v[t, 0])
+            _close(lse[h, t], 0.7 * float(q[t, h] @ k[t, 0]), what="single-token lse")
+
+
+def check_varlen_sequences_isolated():
+    """Changing one sequence's tokens leaves every other sequence bit-identical."""
+    lens = [7, 4, 6]
+    x = make_varlen_inputs(lens, Hq=2, Hkv=2, d=4, seed=33)
+    o0, l0 = oa.prefill_varlen(x.q, x.k, x.v, x.cu_seqlens, 0.5, causal=False)
+    k2, v2 = x.k.clone(), x.v.clone()
+    k2[7:11] = -3 * k2[7:11]
+    v2[7:11] = v2[7:11] + 4
+    o1, l1 = oa.prefill_varlen(x.q, k2, v2, x.cu_seqlens, 0.5, causal=False)
+    keep = np.r_[0:7, 11:17]
+    assert np.array_equal(o1[keep], o0[keep]) and np.array_equal(l1[:, keep], l0[:, keep])
+    assert not np.allclose(o1[7:11], o0[7:11])
+
+
 ALL_CHECKS = [
     check_worked_example_exact,
     check_worked_example_paged,
@@ -280,5 +321,8 @@ ALL_CHECKS = [
     check_decode_equals_contiguous,
     check_split_combine_invariance,
     check_combine_two_groups_closed_form,
+    check_varlen_matches_scipy,
+    check_varlen_single_token_sequences,
+    check_varlen_sequences_isolated,
     check_brute_force_tiny,
 ]

@@ -77,6 +77,36 @@ def combine_ignores_max(parts_o, parts_m, parts_l):
     return o, np.asarray(parts_m)[live].max() + np.log(w.sum())
 
 
+def varlen_positions_from_pack_start(q, k, v, cu_seqlens, scale, causal=True, *, heads=None, seqs=None):
+    """Causal positions counted from token 0 of the whole pack instead of each sequence's start."""
+    q, k, v = oa.f64(q), oa.f64(k), oa.f64(v)
+    cu = [int(x) for x in cu_seqlens.tolist()]
+    T, Hq, _ = q.shape
+    o = np.full((T, Hq, v.shape[2]), np.nan)
+    lse = np.full((Hq, T), np.nan)
+    for n in range(len(cu) - 1):
+        s0, s1 = cu[n], cu[n + 1]
+        if s1 <= s0:
+            continue
+        rows, keys = np.arange(s0, s1), np.arange(0, s1)
+        vis = (keys[None, :] <= rows[:, None]) if causal else None
+        for h in range(Hq):
+            g = oa.kv_head_of(h, Hq, k.shape[1])
+            ob, lb = oa.attend(q[s0:s1, h], k[:s1, g], v[:s1, g], scale, vis)
+            o[s0:s1, h], lse[h, s0:s1] = ob, lb
+    return o, lse
+
+
+def varlen_shifted_slice(q, k, v, cu_seqlens, scale, causal=True, *, heads=None, seqs=None):
+    """Keys and values taken one token late."""
+    q, k, v = oa.f64(q), oa.f64(k), oa.f64(v)
+    k = np.concatenate([k[1:], k[:1]])
+    v = np.concatenate([v[1:], v[:1]])
+    return ORIG_VARLEN(q, k, v, cu_seqlens, scale, causal, heads=heads, seqs=seqs)
+
+
+ORIG_VARLEN = oa.prefill_varlen
+
 MUTANTS = [
     ("attend", attend_no_scale),
     ("attend", attend_wrong_sign),
@@ -87,6 +117,8 @@ MUTANTS = [
     ("kv_head_of", kv_head_modulo),
     ("combine", combine_unweighted),
     ("combine", combine_ignores_max),
+    ("prefill_varlen", varlen_positions_from_pack_start),
+    ("prefill_varlen", varlen_shifted_slice),
 ]
 
 

@@ -139,6 +139,32 @@ def prefill_inputs_for(cfg: PrefillConfig) -> PrefillInputs:
 
 
 @dataclass
+class VarlenInputs:
+    q: torch.Tensor           # [T, Hq, d] bf16, the sequences back to back
+    k: torch.Tensor           # [T, Hkv, d] bf16
+    v: torch.Tensor
+    cu_seqlens: torch.Tensor  # [N + 1] int32 token offsets
+    extra: int = 0            # tokens after the last sequence (belong to none)
+
+    @property
+    def max_seqlen(self) -> int:
+        return int((self.cu_seqlens[1:] - self.cu_seqlens[:-1]).max())
+
+
+def make_varlen_inputs(lens, Hq: int, Hkv: int, d: int, seed: int, extra: int = 0) -> VarlenInputs:
+    """Packed sequences of the given lengths (zero allowed), N(0,1) bf16; ``extra`` trailing tokens
+    that belong to no sequence."""
+    g = _gen(seed)
+    T = int(sum(lens)) + extra
+    q = randn_bf16((T, Hq, d), g)
+    k = randn_bf16((T, Hkv, d), g)
+    v = randn_bf16((T, Hkv, d), g)
+    cu = torch.zeros(len(lens) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
+    return VarlenInputs(q, k, v, cu, extra)
+
+
+@dataclass
 class DecodeInputs:
     q: torch.Tensor            # [N, Hq, d] bf16
     k_cache: torch.Tensor      # [num_blocks, PAGE, Hkv, d] bf16
