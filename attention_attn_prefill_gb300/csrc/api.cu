@@ -81,7 +81,7 @@ attn_status_t prefill_common(const void* q, const void* k, const void* v, void* 
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
   if (batch < 1 || rows < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
   // TMA coordinates are int32 and each map dimension must stay below 2^32
   if (static_cast<int64_t>(Hq) * d > (1 << 30) || rows > (1 << 30) || batch > 65535 || Hq > 65535 ||
       num_seqs > (1 << 24))
@@ -90,9 +90,10 @@ attn_status_t prefill_common(const void* q, const void* k, const void* v, void* 
   attn::PrefillMaps maps;
   const uint64_t q_row = static_cast<uint64_t>(Hq) * d * 2, kv_row = static_cast<uint64_t>(Hkv) * d * 2;
   const uint32_t box = static_cast<uint32_t>(attn::prefill_tile_rows());
+  const uint32_t kv_box = static_cast<uint32_t>(attn::prefill_kv_tile_rows(d));
   if (!encode_3d(&maps.q, q, static_cast<uint64_t>(Hq) * d, rows, batch, q_row, q_row * rows, 64, box, 1) ||
-      !encode_3d(&maps.k, k, static_cast<uint64_t>(Hkv) * d, rows, batch, kv_row, kv_row * rows, 64, box, 1) ||
-      !encode_3d(&maps.v, v, static_cast<uint64_t>(Hkv) * d, rows, batch, kv_row, kv_row * rows, 64, box, 1) ||
+      !encode_3d(&maps.k, k, static_cast<uint64_t>(Hkv) * d, rows, batch, kv_row, kv_row * rows, 64, kv_box, 1) ||
+      !encode_3d(&maps.v, v, static_cast<uint64_t>(Hkv) * d, rows, batch, kv_row, kv_row * rows, 64, kv_box, 1) ||
       !encode_3d(&maps.o, o, static_cast<uint64_t>(Hq) * d, rows, batch, q_row, q_row * rows, 64, box, 1))
     return ATTN_ERR_CUDA;
 

@@ -52,10 +52,7 @@ __device__ uint32_t g_prefill_status;
 namespace {
 
 constexpr int BM = 128;          // query rows per work tile (TMEM lanes)
-constexpr int BN = 128;          // keys per K/V tile
 constexpr int NSB = 3;           // S buffers in TMEM
-constexpr int K_STAGES = 2;      // K_j is free as soon as S_j is done, long before it is reloaded
-constexpr int V_STAGES = 3;      // V_j is held until P_j V_j is done
 constexpr int NUM_THREADS = 512; // 8 softmax warps, 2 TMA warps, 2 MMA warps, 4 epilogue warps
 constexpr int PRODUCER_WARP = 8; // loads Q and streams K
 constexpr int V_WARP = 11;       // streams V
@@ -63,31 +60,44 @@ constexpr int MMA_WARP = 9;      // issues S = Q K^T, owns the TMEM allocation
 constexpr int PV_WARP = 10;      // issues O += P V
 constexpr int EPI_WARP0 = 12;    // warps 12..15: epilogue, one thread per row
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t O_COL = NSB * 128;  // O accumulator columns start here
 constexpr float RESCALE_LOG2_THRESHOLD = 8.0f;
-constexpr int CHUNK_BYTES = 128 * 128;   // 128 rows x 128 B (64 bf16): one 128B-swizzle panel
+constexpr int PANEL_ROW = 128;   // bytes of one 128B-swizzle panel row: 64 bf16
 
+// Tiling and shared-memory layout per head dim.  d <= 128: 128-key K/V tiles, two K and three V
+// stages.  d = 256: 64-key tiles and two stages of each, so that Q and the rings fit in shared
+// memory and O (256 columns) plus three S buffers fit in the 512 TMEM columns.
 template <int D>
 struct Layout {
-  static constexpr int CHUNKS = D / 64;
-  static constexpr int TILE_BYTES = 128 * D * 2;
+  static constexpr int BN = D <= 128 ? 128 : 64;        // keys per K/V tile
+  static constexpr int K_STAGES = 2;                    // K_j is free as soon as S_j is done
+  static constexpr int V_STAGES = D <= 128 ? 3 : 2;     // V_j is held until P_j V_j is done
+  static constexpr int CHUNKS = D / 64;                 // 64-column panels per row
+  static constexpr int Q_PANEL = BM * PANEL_ROW;        // one panel of a Q (or output) tile
+  static constexpr int KV_PANEL = BN * PANEL_ROW;       // one panel of a K or V tile
+  static constexpr int Q_BYTES = CHUNKS * Q_PANEL;
+  static constexpr int KV_BYTES = CHUNKS * KV_PANEL;
+  static constexpr int HALF = BN / 2;                   // keys per softmax thread and step
+  static constexpr uint32_t O_COL = NSB * BN;           // O accumulator columns start here
+  static constexpr int OGRP = D < 128 ? D : 128;        // O columns the epilogue holds at once
   static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + TILE_BYTES;
-  static constexpr int V_OFF = K_OFF + K_STAGES * TILE_BYTES;
-  static constexpr int OST_OFF = V_OFF + V_STAGES * TILE_BYTES;   // output staging: one 64-column panel
-  static constexpr int RED_OFF = OST_OFF + CHUNK_BYTES;           // row-max exchange [2 buffers][2 halves][128]
-  static constexpr int XL_OFF = RED_OFF + 2 * 2 * 128 * 4;        // row-sum exchange [2 halves][128]
-  static constexpr int LROW_OFF = XL_OFF + 2 * 128 * 4;           // l handed to the epilogue [2 tiles][128]
+  static constexpr int K_OFF = Q_OFF + Q_BYTES;
+  static constexpr int V_OFF = K_OFF + K_STAGES * KV_BYTES;
+  static constexpr int OST_OFF = V_OFF + V_STAGES * KV_BYTES;   // output staging: one 64-column panel
+  static constexpr int RED_OFF = OST_OFF + Q_PANEL;             // row-max exchange [2 buffers][2 halves][128]
+  static constexpr int XL_OFF = RED_OFF + 2 * 2 * 128 * 4;      // row-sum exchange [2 halves][128]
+  static constexpr int LROW_OFF = XL_OFF + 2 * 128 * 4;         // l handed to the epilogue [2 tiles][128]
   static constexpr int BAR_OFF = LROW_OFF + 2 * 128 * 4;
-  // q_full, q_empty, k_full[2], k_empty[2], v_full[3], v_empty[3], s_full[3], p_full[3], pv_done[3],
+  // q_full, q_empty, k_full[K], k_empty[K], v_full[V], v_empty[V], s_full[3], p_full[3], pv_done[3],
   // o_full, o_free, mma_done[2], l_full[2], l_empty[2]
-  static constexpr int NUM_BARS = 2 + 2 * 2 + 5 * 3 + 4 + 4;
+  static constexpr int NUM_BARS = 2 + 2 * K_STAGES + 2 * V_STAGES + 3 * NSB + 4 + 4;
   static constexpr int SLOT_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int USED = SLOT_OFF + 16;
   // The dynamic shared memory window starts 1 KB-aligned (checked at run time); never below
   // ~114 KB, so that one CTA (and its 512 TMEM columns) holds an SM.
   static constexpr int ALLOC = USED > 116 * 1024 ? USED : 116 * 1024;
   static_assert(ALLOC <= 232448, "shared memory budget");
+  static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
+  static_assert(HALF == 64 || HALF == 32, "softmax handles 32 or 64 keys per thread");
 };
 
 // One work tile: 128 query rows of one (sequence, query head).
@@ -153,27 +163,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   float* xl = reinterpret_cast<float*>(smem + L::XL_OFF);
   float* lrow = reinterpret_cast<float*>(smem + L::LROW_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
-  uint64_t* q_full = bars + 0;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;
-  uint64_t* k_empty = bars + 4;
-  uint64_t* v_full = bars + 6;
-  uint64_t* v_empty = bars + 9;
-  uint64_t* s_full = bars + 12;
-  uint64_t* p_full = bars + 15;
-  uint64_t* pv_done = bars + 18;   // [3]: P_j V_j done, per S buffer
-  uint64_t* o_full = bars + 21;
-  uint64_t* o_free = bars + 22;    // the epilogue has read O out of TMEM
-  uint64_t* mma_done = bars + 23;  // [2]: each issuer's last MMA done
-  uint64_t* l_full = bars + 25;    // [2]: a tile's row sums are in lrow
-  uint64_t* l_empty = bars + 27;   // [2]: the epilogue has read them
+  constexpr int BN = L::BN, K_STAGES = L::K_STAGES, V_STAGES = L::V_STAGES, HALF = L::HALF;
+  constexpr uint32_t O_COL = L::O_COL;
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* k_full = q_empty + 1;
+  uint64_t* k_empty = k_full + K_STAGES;
+  uint64_t* v_full = k_empty + K_STAGES;
+  uint64_t* v_empty = v_full + V_STAGES;
+  uint64_t* s_full = v_empty + V_STAGES;
+  uint64_t* p_full = s_full + NSB;
+  uint64_t* pv_done = p_full + NSB;   // [3]: P_j V_j done, per S buffer
+  uint64_t* o_full = pv_done + NSB;
+  uint64_t* o_free = o_full + 1;      // the epilogue has read O out of TMEM
+  uint64_t* mma_done = o_free + 1;    // [2]: each issuer's last MMA done
+  uint64_t* l_full = mma_done + 2;    // [2]: a tile's row sums are in lrow
+  uint64_t* l_empty = l_full + 2;     // [2]: the epilogue has read them
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::SLOT_OFF);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.Hq / p.Hkv;
   auto kv_tiles = [&](const WorkTile& t) { return (t.len + BN - 1) / BN; };
-  auto tile_nkv = [&](const WorkTile& t) { return p.causal ? (t.qt + 1) : kv_tiles(t); };
+  auto tile_nkv = [&](const WorkTile& t) {
+    const int all = kv_tiles(t);
+    const int diag = (t.qt + 1) * (BM / BN);  // causal: key tiles up to the end of the query tile
+    return p.causal && diag < all ? diag : all;
+  };
   // loads of the first tile that are issued before the CTA barrier: Q, and as many K and V
   // tiles as the rings hold
   auto first_loads = [&](int nst) {
@@ -191,9 +207,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
     }
-    for (int s = 0; s < 3; ++s) {
+    for (int s = 0; s < V_STAGES; ++s) {
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
+    }
+    for (int s = 0; s < NSB; ++s) {
       mbar_init(&s_full[s], 1);
       mbar_init(&p_full[s], 8);   // one arrival per softmax warp
       mbar_init(&pv_done[s], 1);
@@ -215,20 +233,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     WorkTile t;
     if (w.next(p, t)) {
       const int g = t.hq / G;
-      mbar_arrive_expect_tx(q_full, L::TILE_BYTES);
+      mbar_arrive_expect_tx(q_full, L::Q_BYTES);
       for (int c = 0; c < L::CHUNKS; ++c)
-        tma_load_3d(sQ + c * CHUNK_BYTES, &tm_q, q_full, t.hq * D + c * 64, t.base + t.qt * BM, t.z);
+        tma_load_3d(sQ + c * L::Q_PANEL, &tm_q, q_full, t.hq * D + c * 64, t.base + t.qt * BM, t.z);
       const int nk = first_loads(K_STAGES), nv = first_loads(V_STAGES);
       for (int j = 0; j < nk; ++j) {
-        mbar_arrive_expect_tx(&k_full[j], L::TILE_BYTES);
+        mbar_arrive_expect_tx(&k_full[j], L::KV_BYTES);
         for (int c = 0; c < L::CHUNKS; ++c)
-          tma_load_3d(sK + j * L::TILE_BYTES + c * CHUNK_BYTES, &tm_k, &k_full[j], g * D + c * 64, t.base + j * BN,
+          tma_load_3d(sK + j * L::KV_BYTES + c * L::KV_PANEL, &tm_k, &k_full[j], g * D + c * 64, t.base + j * BN,
                       t.z);
       }
       for (int j = 0; j < nv; ++j) {
-        mbar_arrive_expect_tx(&v_full[j], L::TILE_BYTES);
+        mbar_arrive_expect_tx(&v_full[j], L::KV_BYTES);
         for (int c = 0; c < L::CHUNKS; ++c)
-          tma_load_3d(sV + j * L::TILE_BYTES + c * CHUNK_BYTES, &tm_v, &v_full[j], g * D + c * 64, t.base + j * BN,
+          tma_load_3d(sV + j * L::KV_BYTES + c * L::KV_PANEL, &tm_v, &v_full[j], g * D + c * 64, t.base + j * BN,
                       t.z);
       }
     }
@@ -264,9 +282,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // Q of this tile replaces the previous one once all of its S = Q K^T products are done
           if (k > 0) {
             if (!mbar_wait(q_empty, (k - 1) & 1)) { ok = false; break; }
-            mbar_arrive_expect_tx(q_full, L::TILE_BYTES);
+            mbar_arrive_expect_tx(q_full, L::Q_BYTES);
             for (int c = 0; c < L::CHUNKS; ++c)
-              tma_load_3d(sQ + c * CHUNK_BYTES, &tm_q, q_full, t.hq * D + c * 64, t.base + t.qt * BM, t.z);
+              tma_load_3d(sQ + c * L::Q_PANEL, &tm_q, q_full, t.hq * D + c * 64, t.base + t.qt * BM, t.z);
           }
           nq = k + 1;
         }
@@ -274,9 +292,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int j = (k == 0 ? npre : 0); j < nkv; ++j) {
           const int st = issued % nst;
           if (!mbar_wait(&empty[st], ((issued / nst) & 1) ^ 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[st], L::TILE_BYTES);
+          mbar_arrive_expect_tx(&full[st], L::KV_BYTES);
           for (int c = 0; c < L::CHUNKS; ++c)
-            tma_load_3d(ring + st * L::TILE_BYTES + c * CHUNK_BYTES, map, &full[st], g * D + c * 64, t.base + j * BN,
+            tma_load_3d(ring + st * L::KV_BYTES + c * L::KV_PANEL, map, &full[st], g * D + c * 64, t.base + j * BN,
                         t.z);
           ++issued;
         }
@@ -310,12 +328,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t kbase = smem_u32(sK + st * L::TILE_BYTES);
-          const uint32_t s_tmem = tmem + sb * 128;
+          const uint32_t kbase = smem_u32(sK + st * L::KV_BYTES);
+          const uint32_t s_tmem = tmem + sb * BN;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
-            umma_ss(s_tmem, smem_desc_sw128(qbase + koff, 16, 1024), smem_desc_sw128(kbase + koff, 16, 1024),
+            // 16 columns of d: panel kk / 4, 32 bytes into its 128-byte rows
+            const uint32_t qoff = (kk >> 2) * L::Q_PANEL + (kk & 3) * 32;
+            const uint32_t koff = (kk >> 2) * L::KV_PANEL + (kk & 3) * 32;
+            umma_ss(s_tmem, smem_desc_sw128(qbase + qoff, 16, 1024), smem_desc_sw128(kbase + koff, 16, 1024),
                     IDESC_S, kk > 0 ? 1u : 0u);
           }
           umma_commit(&s_full[sb]);
@@ -348,8 +368,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t vbase = smem_u32(sV + st * L::TILE_BYTES);
-          const uint32_t p_tmem = tmem + sb * 128;
+          const uint32_t vbase = smem_u32(sV + st * L::KV_BYTES);
+          const uint32_t p_tmem = tmem + sb * BN;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
             // 16 keys = two 8-row swizzle atoms; d panels are BN*128 bytes apart
@@ -387,33 +407,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float l_part = 0.f;        // this half's share of the row sum
       for (int j = 0; j < nkv; ++j, ++gs) {
         const int sb = gs % NSB;
-        const uint32_t s_tmem = tmem + lane_base + sb * 128;
+        const uint32_t s_tmem = tmem + lane_base + sb * BN;
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (gs / NSB) & 1));
         tc_fence_after();
-        uint32_t sr[2][32];
-        tmem_ld32(s_tmem + h * 64, sr[0]);
-        tmem_ld32(s_tmem + h * 64 + 32, sr[1]);
-        tmem_ld_wait();
-        // last visible column of this thread's 64 keys: the causal diagonal and the end of the
-        // sequence are the only places where it is below 63
-        const int key0 = j * BN + h * 64;
-        int lim = 63;
-        if (p.causal && j == nkv - 1) lim = q - key0;
-        if (j == nkv_all - 1 && t.len - 1 - key0 < lim) lim = t.len - 1 - key0;
-        if (lim < 63) {
+        uint32_t sr[HALF / 32][32];
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
+        for (int i = 0; i < HALF / 32; ++i) tmem_ld32(s_tmem + h * HALF + 32 * i, sr[i]);
+        tmem_ld_wait();
+        // last visible column of this thread's keys: below HALF - 1 only where the tile crosses
+        // the causal diagonal or the end of the sequence
+        const int key0 = j * BN + h * HALF;
+        int lim = HALF - 1;
+        if (p.causal && q - key0 < lim) lim = q - key0;
+        if (j == nkv_all - 1 && t.len - 1 - key0 < lim) lim = t.len - 1 - key0;
+        if (lim < HALF - 1) {
+#pragma unroll
+          for (int c = 0; c < HALF; ++c)
             if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
         }
-        float mx0 = -INFINITY, mx1 = -INFINITY;
+        float mxs[HALF / 32];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          mx0 = fmax3(mx0, __uint_as_float(sr[0][2 * c]), __uint_as_float(sr[0][2 * c + 1]));
-          mx1 = fmax3(mx1, __uint_as_float(sr[1][2 * c]), __uint_as_float(sr[1][2 * c + 1]));
+        for (int i = 0; i < HALF / 32; ++i) {
+          float m = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) m = fmax3(m, __uint_as_float(sr[i][2 * c]), __uint_as_float(sr[i][2 * c + 1]));
+          mxs[i] = m;
         }
+        float mxh = mxs[0];
+#pragma unroll
+        for (int i = 1; i < HALF / 32; ++i) mxh = fmaxf(mxh, mxs[i]);
         // exchange the half-row maxima (both halves have read S, so P may overwrite it afterwards)
         float* xr = red + (gs & 1) * 256;
-        xr[h * 128 + row] = fmaxf(mx0, mx1);
+        xr[h * 128 + row] = mxh;
         named_barrier_sync(1, 256);
         const float mx = fmaxf(xr[row], xr[128 + row]);
         float alpha = 1.f;
@@ -429,11 +454,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float mb = (m_used == -INFINITY) ? 0.f : m_used * c2;
         const uint64_t nmb2 = f2_pack(-mb, -mb);
         // p = 2^(s*scale*log2e - m*scale*log2e) in f32x2 pairs; P (bf16, two per column) goes to
-        // columns 32h..32h+31 of this S buffer
+        // columns h*HALF/2 .. h*HALF/2 + HALF/2 - 1 of this S buffer
         uint64_t acc0 = 0ull, acc1 = 0ull;
-        uint32_t pk[32];
+        uint32_t pk[HALF / 2];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
+        for (int c = 0; c < HALF / 2; ++c) {
           const int e = 2 * c;
           const uint64_t xy = f2_fma(
               f2_pack(__uint_as_float(sr[e >> 5][e & 31]), __uint_as_float(sr[e >> 5][(e & 31) + 1])), c2x2, nmb2);
@@ -450,7 +475,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           f2_unpack(f2_add(acc0, acc1), a0, a1);
           l_part += a0 + a1;
         }
-        tmem_st32(s_tmem + h * 32, pk);
+        tmem_st_cols(s_tmem + h * (HALF / 2), pk);
         if (__any_sync(0xffffffffu, rescale_o)) {
           // O must hold P V of the previous step before it is rescaled
           if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(gs - 1) % NSB], ((gs - 1) / NSB) & 1));
@@ -506,44 +531,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) mbar_arrive(&l_empty[tb]);
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_full, k & 1));
       tc_fence_after();
-      uint32_t ob[D / 2];
+      const bool rowwise = p.cu_seqlens != nullptr && t.qt * BM + BM > t.len;
+      // O in groups of OGRP columns (all of it for d <= 128): bf16 pairs after the division by l
+#pragma unroll 1
+      for (int g0 = 0; g0 < D; g0 += L::OGRP) {
+        uint32_t ob[L::OGRP / 2];
 #pragma unroll
-      for (int c4 = 0; c4 < D / 32; ++c4) {
-        uint32_t r[32];
-        tmem_ld32(o_row + c4 * 32, r);
-        tmem_ld_wait();
+        for (int c4 = 0; c4 < L::OGRP / 32; ++c4) {
+          uint32_t r[32];
+          tmem_ld32(o_row + g0 + c4 * 32, r);
+          tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          ob[c4 * 16 + c] = pack_bf16x2(__uint_as_float(r[2 * c]) * inv_l, __uint_as_float(r[2 * c + 1]) * inv_l);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_free);  // the next tile's first P.V may overwrite O now
-      if (p.cu_seqlens != nullptr && t.qt * BM + BM > t.len) {
-        if (t.qt * BM + row < t.len) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
-                                                (static_cast<size_t>(t.base + t.qt * BM + row) * p.Hq + t.hq) * D);
-#pragma unroll
-          for (int u = 0; u < D / 8; ++u) dst[u] = make_uint4(ob[4 * u], ob[4 * u + 1], ob[4 * u + 2], ob[4 * u + 3]);
+          for (int c = 0; c < 16; ++c)
+            ob[c4 * 16 + c] = pack_bf16x2(__uint_as_float(r[2 * c]) * inv_l, __uint_as_float(r[2 * c + 1]) * inv_l);
         }
-        continue;
-      }
-      uint8_t* line = sO + row * 128;
-#pragma unroll
-      for (int c = 0; c < L::CHUNKS; ++c) {
-        if (et == 0) tma_store_wait_read0();  // the previous panel's store has read the staging buffer
-        named_barrier_sync(2, 128);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 w = make_uint4(ob[32 * c + 4 * u], ob[32 * c + 4 * u + 1], ob[32 * c + 4 * u + 2],
-                                     ob[32 * c + 4 * u + 3]);
-          *reinterpret_cast<uint4*>(line + ((u ^ (row & 7)) << 4)) = w;
+        if (g0 + L::OGRP == D) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(o_free);  // the next tile's first P.V may overwrite O now
         }
-        fence_proxy_async_smem();
-        named_barrier_sync(2, 128);
-        if (et == 0) {
-          tma_store_3d(&tm_o, sO, t.hq * D + c * 64, t.base + t.qt * BM, t.z);
-          tma_store_commit();
+        if (rowwise) {
+          if (t.qt * BM + row < t.len) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
+                                                  (static_cast<size_t>(t.base + t.qt * BM + row) * p.Hq + t.hq) * D +
+                                                  g0);
+#pragma unroll
+            for (int u = 0; u < L::OGRP / 8; ++u)
+              dst[u] = make_uint4(ob[4 * u], ob[4 * u + 1], ob[4 * u + 2], ob[4 * u + 3]);
+          }
+          continue;
+        }
+        uint8_t* line = sO + row * PANEL_ROW;
+#pragma unroll
+        for (int c = 0; c < L::OGRP / 64; ++c) {
+          if (et == 0) tma_store_wait_read0();  // the previous panel's store has read the staging buffer
+          named_barrier_sync(2, 128);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 w = make_uint4(ob[32 * c + 4 * u], ob[32 * c + 4 * u + 1], ob[32 * c + 4 * u + 2],
+                                       ob[32 * c + 4 * u + 3]);
+            *reinterpret_cast<uint4*>(line + ((u ^ (row & 7)) << 4)) = w;
+          }
+          fence_proxy_async_smem();
+          named_barrier_sync(2, 128);
+          if (et == 0) {
+            tma_store_3d(&tm_o, sO, t.hq * D + g0 + c * 64, t.base + t.qt * BM, t.z);
+            tma_store_commit();
+          }
         }
       }
     }
@@ -583,10 +617,12 @@ cudaError_t launch(const PrefillMaps& m, const PrefillParams& p, cudaStream_t st
 
 int prefill_rows_per_cta() { return BM; }
 int prefill_tile_rows() { return BM; }
+int prefill_kv_tile_rows(int d) { return d <= 128 ? Layout<128>::BN : Layout<256>::BN; }
 
 cudaError_t prefill_launch(int d, const PrefillMaps& maps, const PrefillParams& p, cudaStream_t stream) {
   if (d == 64) return launch<64>(maps, p, stream);
   if (d == 128) return launch<128>(maps, p, stream);
+  if (d == 256) return launch<256>(maps, p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -30,7 +30,8 @@ struct PrefillParams {
 };
 
 int prefill_rows_per_cta();
-int prefill_tile_rows();
+int prefill_tile_rows();            // rows of a Q / O box
+int prefill_kv_tile_rows(int d);    // rows of a K / V box for head dim d
 cudaError_t prefill_launch(int d, const PrefillMaps& maps, const PrefillParams& p, cudaStream_t stream);
 cudaError_t prefill_status(uint32_t* out, bool clear);
 

@@ -66,7 +66,8 @@ const char* attn_status_string(attn_status_t status);
  *   q   [B, S, Hq,  d] bf16      k, v [B, S, Hkv, d] bf16
  *   o   [B, S, Hq,  d] bf16 (output)
  *   lse [B, Hq, S]     f32 (output, may be NULL)
- *   d in {64, 128}; B, S >= 1; Hq, Hkv >= 1 with Hq % Hkv == 0.
+ *   d in {64, 128, 256}; B, S >= 1; Hq, Hkv >= 1 with Hq % Hkv == 0.  d = 256
+ *   uses 64-key tiles (the rest 128-key tiles).
  *   scale: multiplier of q.k (for example 1/sqrt(d)).
  *   causal != 0: row i sees keys 0..i (itself included); causal == 0: all S keys.
  * Row i of o is sum_j softmax_j(scale * q_i.k_j) v_j over the visible keys;

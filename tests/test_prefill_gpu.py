@@ -7,7 +7,7 @@ import torch
 
 import oracle.attention as oa
 from parity import check_lse, check_o, to_np
-from workloads import LLAMA8B, SWEEP, TINY, make_prefill_inputs, prefill_inputs_for
+from workloads import LLAMA8B, QWEN256, SWEEP, TINY, make_prefill_inputs, prefill_inputs_for
 
 pytestmark = pytest.mark.gpu
 
@@ -34,7 +34,7 @@ def test_tiny_config(attn, gpu):
 
 
 @pytest.mark.parametrize("S", [1, 7, 128, 129, 255, 256, 257, 300, 511, 640])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_ragged_lengths_causal(attn, gpu, S, d):
     """Several Q/KV tiles with a ragged tail, GQA 4:2, two batch elements."""
     x = make_prefill_inputs(2, 4, 2, S, d, seed=1000 + S + d)
@@ -42,7 +42,7 @@ def test_ragged_lengths_causal(attn, gpu, S, d):
 
 
 @pytest.mark.parametrize("S", [1, 100, 128, 300, 513])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_noncausal(attn, gpu, S, d):
     x = make_prefill_inputs(1, 2, 1, S, d, seed=2000 + S + d)
     full_compare(attn, x, 1.0 / math.sqrt(d), False, gpu, f"noncausal S={S} d={d}")
@@ -54,19 +54,21 @@ def test_mqa_and_mha(attn, gpu):
         full_compare(attn, x, 0.09, True, gpu, f"Hq={Hq} Hkv={Hkv}")
 
 
-def test_large_scores_running_max_jumps(attn, gpu):
+@pytest.mark.parametrize("d", [128, 256])
+def test_large_scores_running_max_jumps(attn, gpu, d):
     """Keys scaled so the running max jumps by far more than the lazy-rescale threshold."""
-    x = make_prefill_inputs(1, 2, 1, 700, 128, seed=44)
+    x = make_prefill_inputs(1, 2, 1, 700, d, seed=44)
     k = x.k.clone()
     k[:, 129::97] *= 8
     k[:, 400:] *= 2
     x.k = k
-    full_compare(attn, x, 1.0 / math.sqrt(128), True, gpu, "max jumps")
+    full_compare(attn, x, 1.0 / math.sqrt(d), True, gpu, f"max jumps d={d}")
 
 
-def test_row0_returns_v0_exactly(attn, gpu):
+@pytest.mark.parametrize("d", [128, 256])
+def test_row0_returns_v0_exactly(attn, gpu, d):
     """Causal row 0 sees only key 0, so O[0] = v0 bit-exactly and LSE[0] = scale * q0.k0."""
-    x = make_prefill_inputs(2, 4, 2, 130, 128, seed=5)
+    x = make_prefill_inputs(2, 4, 2, 130, d, seed=5)
     o, lse = run_prefill(attn, x, 0.1, True, gpu)
     o = o.cpu()
     for h in range(4):
@@ -134,3 +136,8 @@ def test_llama8b_full_size_sampled(attn, gpu):
 @pytest.mark.parametrize("cfg", SWEEP, ids=lambda c: c.name)
 def test_sweep_full_size_sampled(attn, gpu, cfg):
     _sampled(attn, gpu, cfg, heads=[0, 13, 31], nrows=24, seed=cfg.seed)
+
+
+def test_d256_8k_prompt_sampled(attn, gpu):
+    """Head dim 256 (64-key tiles): Hq=16, Hkv=2, S=8192, scale 2^-4; sampled rows of three heads."""
+    _sampled(attn, gpu, QWEN256, heads=[0, 7, 15], nrows=24, seed=9)

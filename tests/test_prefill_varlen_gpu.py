@@ -37,7 +37,7 @@ def compare(attn, x, scale, causal, dev, what, seqs=None, heads=None):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_ragged_pack(attn, gpu, causal, d):
     """Lengths around tile edges, an empty sequence, GQA 4:2, two trailing tokens in no sequence."""
     lens = [1, 127, 0, 128, 129, 300, 7, 513]

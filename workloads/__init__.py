@@ -96,7 +96,11 @@ LONGCTX = DecodeConfig("longctx_decode", N=8, Hq=16, Hkv=2, d=256, scale=2.0 ** 
                        lens=(6335, 19873, 27525, 42192, 67144, 83233, 94146, 122863),
                        split_tokens=(512, 1024, 2048, 4096))
 
-PREFILL_CONFIGS = (TINY, LLAMA8B) + SWEEP
+# Extra measurement (not one of the five workloads): the long-context decode model's heads
+# (Hq=16, Hkv=2, d=256, scale 2^-4) prefilling an 8K-token prompt.
+QWEN256 = PrefillConfig("qwen_d256_prefill", B=1, Hq=16, Hkv=2, S=8192, d=256, scale=2.0 ** -4, seed=7)
+
+PREFILL_CONFIGS = (TINY, LLAMA8B) + SWEEP + (QWEN256,)
 DECODE_CONFIGS = (PAGED, LONGCTX)
 
 
