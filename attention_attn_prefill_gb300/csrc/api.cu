@@ -112,6 +112,8 @@ attn_status_t prefill_common(const void* q, const void* k, const void* v, void* 
   const int longest = cu_seqlens != nullptr ? max_seqlen : rows;
   p.num_qblocks = (longest + per_cta - 1) / per_cta;
   if (p.num_qblocks > 65535) return ATTN_ERR_INVALID_ARG;
+  // the kernel's tile walk indexes (query tile, sequence, head) in 32 bits
+  if (static_cast<int64_t>(p.num_qblocks) * p.B * p.Hq > (int64_t(1) << 30)) return ATTN_ERR_INVALID_ARG;
   return from_cuda(attn::prefill_launch(d, maps, p, static_cast<cudaStream_t>(stream)));
 }
 

@@ -112,19 +112,20 @@ struct WorkTile {
 // packed sequence shorter than the longest one has no tiles at the top query-tile levels: every role
 // skips those alike, so all roles see the same list.
 struct TileWalk {
-  long long v = 0;
+  int v = 0;
+  // 32-bit index arithmetic: the host keeps tiles x 2 below 2^31
   __device__ __forceinline__ bool next(const PrefillParams& p, WorkTile& t) {
-    const long long G = gridDim.x, c = blockIdx.x;
-    const long long per_qt = static_cast<long long>(p.B) * p.Hq;
-    const long long total = per_qt * p.num_qblocks;
+    const int G = gridDim.x, c = blockIdx.x;
+    const int per_qt = p.B * p.Hq;
+    const int total = per_qt * p.num_qblocks;
     while (true) {
-      const long long idx = v * G + ((v & 1) ? (G - 1 - c) : c);
+      const int idx = v * G + ((v & 1) ? (G - 1 - c) : c);
       ++v;
       if (idx >= total) return false;
-      t.qt = p.num_qblocks - 1 - static_cast<int>(idx / per_qt);
-      const long long rem = idx % per_qt;
-      t.hq = static_cast<int>(rem % p.Hq);
-      t.b = static_cast<int>(rem / p.Hq);
+      t.qt = p.num_qblocks - 1 - idx / per_qt;
+      const int rem = idx - (idx / per_qt) * per_qt;
+      t.hq = rem % p.Hq;
+      t.b = rem / p.Hq;
       if (p.cu_seqlens == nullptr) {
         t.base = 0;
         t.z = t.b;
