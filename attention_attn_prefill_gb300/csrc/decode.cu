@@ -873,14 +873,16 @@ int split_ctas_per_sm() {
 }  // namespace
 
 int decode_split_ctas_per_sm(int d) {
-  if (d == 128) return split_ctas_per_sm<128, 4, 3>();
-  if (d == 256) return split_ctas_per_sm<256, 4, 3>();
+  if (d == 128) return split_ctas_per_sm<128, 4, 2>();
+  if (d == 256) return split_ctas_per_sm<256, 3, 2>();
   return 0;
 }
 
 cudaError_t decode_split_launch(int d, const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream) {
-  if (d == 128) return launch_split<128, 4, 3>(maps, p, stream);
-  if (d == 256) return launch_split<256, 4, 3>(maps, p, stream);
+  // 4 warps x 2 pages in flight (3 CTAs per SM) at d = 128; 3 warps x 2 pages (2 CTAs per SM) at
+  // d = 256: more resident warps per SM than deeper per-warp pipelines, measured on GB300
+  if (d == 128) return launch_split<128, 4, 2>(maps, p, stream);
+  if (d == 256) return launch_split<256, 3, 2>(maps, p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -347,12 +347,12 @@ def run_gpu(args):
         },
         "decode": {
             "value": round(gbs, 1), "unit": "GB/s", "ms": round(dec_mean, 4),
-            "roofline": {"bound": "hbm", "kernel": "decode_split_kernel<128,4,3> + combine_kernel<128>",
+            "roofline": {"bound": "hbm", "kernel": "decode_split_kernel<128,4,2> + combine_kernel<128>",
                          "achieved": round(dec_achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(dec_achieved / peaks["hbm_gbs"], 4),
                          "frac_of_8tbs": round(dec_achieved / 8000.0, 4),
                          "peak_source": f"{peak_src} HBM copy",
-                         "traffic": traffic_record("decode_split_kernel<128,4,3>")},
+                         "traffic": traffic_record("decode_split_kernel<128,4,2>")},
         },
         "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms": round(e2e_ms, 4)},
@@ -424,9 +424,10 @@ def run_reference(args):
 def run_case(args):
     """One kernel family on one named workload, for profiling: prints a short JSON line.
 
-    prefill:<name>            name in {tiny, llama8b_prefill, sweep_s1024, sweep_s2048, sweep_s4096}
-    decode:<name>:<splits>    name in {paged_decode, longctx_decode}; splits = num_splits,
-                              or t<N> for split_tokens = N
+    prefill:<name>            name in {tiny, llama8b_prefill, sweep_s1024, sweep_s2048, sweep_s4096,
+                              qwen_d256_prefill}
+    decode:<name>:<splits>    name in {paged_decode, longctx_decode}; splits = num_splits (0 = balanced
+                              mode), t<N> for split_tokens = N, or auto for the split-count rule
     """
     from workloads import DECODE_CONFIGS, PREFILL_CONFIGS
     from attention_attn_prefill_gb300.build import build
@@ -448,9 +449,14 @@ def run_case(args):
     else:
         cfg = {c.name: c for c in DECODE_CONFIGS}[name]
         spec = rest[0] if rest else "1"
-        kw = dict(split_tokens=int(spec[1:])) if spec.startswith("t") else dict(num_splits=int(spec))
         lens = decode_lens_for(cfg)
         x = decode_inputs_for(cfg)
+        if spec == "auto":
+            kw = dict(num_splits=attn.decode_auto_splits(cfg.N, cfg.Hkv, cfg.d, x.max_blocks))
+        elif spec.startswith("t"):
+            kw = dict(split_tokens=int(spec[1:]))
+        else:
+            kw = dict(num_splits=int(spec))
         dq, kc, vc, bt, sl = (t.to(dev) for t in (x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens))
         do = torch.empty_like(dq)
         dl = torch.empty((cfg.N, cfg.Hq), dtype=torch.float32, device=dev)
