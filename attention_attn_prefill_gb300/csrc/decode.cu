@@ -908,7 +908,10 @@ cudaError_t combine_launch(int d, const float* part_o, const float* part_m, cons
   return cudaLaunchKernelEx(&cfg, kern, part_o, part_m, part_l, rows, splits, out, lse);
 }
 
-constexpr int BAL_NW = 4;
+// Worker warps per CTA, pages in flight per warp and CTAs per SM of the balanced kernel.
+template <int D> struct BalCfg;
+template <> struct BalCfg<128> { static constexpr int NW = 3, NS = 2, CTAS = 3; };  // 60 KB per CTA
+template <> struct BalCfg<256> { static constexpr int NW = 2, NS = 2, CTAS = 2; };  // 80 KB per CTA
 
 size_t decode_balanced_records(int warps_total, int N, int Hkv) {
   return static_cast<size_t>(warps_total) + static_cast<size_t>(Hkv) * N;
@@ -918,14 +921,22 @@ int decode_balanced_warps(int d) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  const int ctas_per_sm = d <= 128 ? 2 : 1;  // shared memory: 112 KB per CTA at d = 128, 224 KB at 256
-  return sms * ctas_per_sm * BAL_NW;
+  if (d == 128) return sms * BalCfg<128>::CTAS * BalCfg<128>::NW;
+  if (d == 256) return sms * BalCfg<256>::CTAS * BalCfg<256>::NW;
+  return 0;
 }
 
 cudaError_t decode_balanced_launch(int d, const DecodeMaps& maps, const BalancedParams& p, cudaStream_t stream) {
-  if (p.warps_total % BAL_NW) return cudaErrorInvalidValue;
-  if (d == 128) return launch_balanced<128, BAL_NW, 3, 2>(maps, p, stream);
-  if (d == 256) return launch_balanced<256, BAL_NW, 3, 1>(maps, p, stream);
+  if (d == 128) {
+    using C = BalCfg<128>;
+    if (p.warps_total % C::NW) return cudaErrorInvalidValue;
+    return launch_balanced<128, C::NW, C::NS, C::CTAS>(maps, p, stream);
+  }
+  if (d == 256) {
+    using C = BalCfg<256>;
+    if (p.warps_total % C::NW) return cudaErrorInvalidValue;
+    return launch_balanced<256, C::NW, C::NS, C::CTAS>(maps, p, stream);
+  }
   return cudaErrorInvalidValue;
 }
 
