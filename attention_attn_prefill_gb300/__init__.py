@@ -5,10 +5,10 @@ ABI of ``include/attn.h``); this package is its Python binding.
 """
 from ._lib import (AttnError, combine, decode_auto_splits, decode_balanced_workspace_bytes, decode_num_slots,
                    decode_paged, decode_paged_noalloc, decode_workspace_bytes, device_status, header_functions, lib,
-                   library_path, prefill, prefill_varlen, split_heuristic)
+                   library_path, prefill, prefill_paged, prefill_varlen, split_heuristic)
 
 __all__ = [
     "AttnError", "combine", "decode_auto_splits", "decode_balanced_workspace_bytes", "decode_num_slots",
     "decode_paged", "decode_paged_noalloc", "decode_workspace_bytes", "device_status", "header_functions", "lib",
-    "library_path", "prefill", "prefill_varlen", "split_heuristic",
+    "library_path", "prefill", "prefill_paged", "prefill_varlen", "split_heuristic",
 ]

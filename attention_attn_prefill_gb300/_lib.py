@@ -49,6 +49,7 @@ _SIGNATURES = {
     "attn_device_status": (c_int, [c_u32_p, c_int]),
     "attn_split_heuristic": (c_int, [c_int] * 4),
     "attn_prefill_varlen": (c_int, [c_void_p] * 6 + [c_int] * 6 + [c_float, c_int, c_void_p]),
+    "attn_prefill_paged": (c_int, [c_void_p] * 8 + [c_int] * 9 + [c_float, c_int, c_void_p]),
     "attn_decode_auto_splits": (c_int, [c_int] * 4),
 }
 
@@ -145,6 +146,35 @@ def prefill_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens
         _dev(cu_seqlens, torch.int32, "cu_seqlens"), cu_seqlens.numel() - 1, int(max_seqlen), T, Hq, Hkv, d,
         float(scale), 1 if causal else 0, _stream_handle(stream))
     _check(st, "attn_prefill_varlen")
+    return out, lse
+
+
+def prefill_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
+                  cu_seqlens_q: torch.Tensor, seq_lens: torch.Tensor, max_seqlen_q: int, scale: float | None = None,
+                  causal: bool = True, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                  return_lse: bool = True, stream=None):
+    """Chunked prefill: new tokens q [T,Hq,d] against the paged cache [num_blocks,16,Hkv,d] -> (o, lse [Hq,T])."""
+    T, Hq, d = q.shape
+    num_blocks, page, Hkv, dk = k_cache.shape
+    if dk != d or v_cache.shape != k_cache.shape:
+        raise ValueError("caches must be [num_blocks, page, Hkv, d] matching q")
+    N = seq_lens.numel()
+    if block_table.dim() != 2 or block_table.shape[0] != N or cu_seqlens_q.shape != (N + 1,):
+        raise ValueError("block_table must be [N, max_blocks], cu_seqlens_q [N+1] and seq_lens [N]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    st = lib().attn_prefill_paged(
+        _dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.bfloat16, "k_cache"),
+        _dev(v_cache, torch.bfloat16, "v_cache"), _dev(block_table, torch.int32, "block_table"),
+        _dev(cu_seqlens_q, torch.int32, "cu_seqlens_q"), _dev(seq_lens, torch.int32, "seq_lens"),
+        _dev(out, torch.bfloat16, "out"), _dev(lse, torch.float32, "lse") if lse is not None else None,
+        N, int(max_seqlen_q), T, Hq, Hkv, d, page, block_table.shape[1], num_blocks, float(scale),
+        1 if causal else 0, _stream_handle(stream))
+    _check(st, "attn_prefill_paged")
     return out, lse
 
 

@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "attn.h"
@@ -71,13 +72,23 @@ int attn_version(void) { return kVersion; }
 
 namespace {
 
-// Shared by both prefill entry points: `batch` sequences of `rows` tokens each in the maps (one
+// Paged K/V for the chunked prefill entry point (absent for the others).
+struct PagedKV {
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  const int32_t* kv_lens;
+  int max_blocks, num_blocks;
+};
+
+// Shared by the prefill entry points: `batch` sequences of `rows` tokens each in the maps (one
 // packed batch of `rows` tokens for packed sequences).
 attn_status_t prefill_common(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int Hq,
                              int Hkv, int rows, int d, float scale, int causal, const int32_t* cu_seqlens,
-                             int num_seqs, int max_seqlen, void* stream) {
-  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+                             int num_seqs, int max_seqlen, const PagedKV* paged, void* stream) {
+  if (q == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (paged == nullptr && (k == nullptr || v == nullptr || !aligned16(k) || !aligned16(v))) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
   if (batch < 1 || rows < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -88,19 +99,34 @@ attn_status_t prefill_common(const void* q, const void* k, const void* v, void* 
     return ATTN_ERR_INVALID_ARG;
 
   attn::PrefillMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
   const uint64_t q_row = static_cast<uint64_t>(Hq) * d * 2, kv_row = static_cast<uint64_t>(Hkv) * d * 2;
   const uint32_t box = static_cast<uint32_t>(attn::prefill_tile_rows());
   const uint32_t kv_box = static_cast<uint32_t>(attn::prefill_kv_tile_rows(d));
   if (!encode_3d(&maps.q, q, static_cast<uint64_t>(Hq) * d, rows, batch, q_row, q_row * rows, 64, box, 1) ||
-      !encode_3d(&maps.k, k, static_cast<uint64_t>(Hkv) * d, rows, batch, kv_row, kv_row * rows, 64, kv_box, 1) ||
-      !encode_3d(&maps.v, v, static_cast<uint64_t>(Hkv) * d, rows, batch, kv_row, kv_row * rows, 64, kv_box, 1) ||
       !encode_3d(&maps.o, o, static_cast<uint64_t>(Hq) * d, rows, batch, q_row, q_row * rows, 64, box, 1))
     return ATTN_ERR_CUDA;
+  if (paged == nullptr) {
+    if (!encode_3d(&maps.k, k, static_cast<uint64_t>(Hkv) * d, rows, batch, kv_row, kv_row * rows, 64, kv_box, 1) ||
+        !encode_3d(&maps.v, v, static_cast<uint64_t>(Hkv) * d, rows, batch, kv_row, kv_row * rows, 64, kv_box, 1))
+      return ATTN_ERR_CUDA;
+  } else {
+    // {d, Hkv, num_blocks * 16}: 64-column x 1-head x 16-row boxes (one page), V also 1-row boxes
+    const uint64_t tokens = static_cast<uint64_t>(paged->num_blocks) * kPage;
+    if (!encode_3d(&maps.k, paged->k_cache, d, Hkv, tokens, static_cast<uint64_t>(d) * 2, kv_row, 64, 1, kPage) ||
+        !encode_3d(&maps.v, paged->v_cache, d, Hkv, tokens, static_cast<uint64_t>(d) * 2, kv_row, 64, 1, kPage) ||
+        !encode_3d(&maps.v_row, paged->v_cache, d, Hkv, tokens, static_cast<uint64_t>(d) * 2, kv_row, 64, 1, 1))
+      return ATTN_ERR_CUDA;
+  }
 
   attn::PrefillParams p;
   p.lse = lse;
   p.o = o;
   p.cu_seqlens = cu_seqlens;
+  p.kv_lens = paged != nullptr ? paged->kv_lens : nullptr;
+  p.block_table = paged != nullptr ? paged->block_table : nullptr;
+  p.max_blocks = paged != nullptr ? paged->max_blocks : 0;
+  p.num_blocks = paged != nullptr ? paged->num_blocks : 0;
   p.B = cu_seqlens != nullptr ? num_seqs : batch;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -121,7 +147,7 @@ attn_status_t prefill_common(const void* q, const void* k, const void* v, void* 
 
 attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                            int S, int d, float scale, int causal, void* stream) {
-  return prefill_common(q, k, v, o, lse, B, Hq, Hkv, S, d, scale, causal, nullptr, 0, 0, stream);
+  return prefill_common(q, k, v, o, lse, B, Hq, Hkv, S, d, scale, causal, nullptr, 0, 0, nullptr, stream);
 }
 
 attn_status_t attn_prefill_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -130,7 +156,27 @@ attn_status_t attn_prefill_varlen(const void* q, const void* k, const void* v, v
   if (cu_seqlens == nullptr || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return ATTN_ERR_INVALID_ARG;
   if (num_seqs < 1 || max_seqlen < 1 || total_tokens < 1) return ATTN_ERR_INVALID_ARG;
   return prefill_common(q, k, v, o, lse, 1, Hq, Hkv, total_tokens, d, scale, causal, cu_seqlens, num_seqs,
-                        max_seqlen, stream);
+                        max_seqlen, nullptr, stream);
+}
+
+attn_status_t attn_prefill_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                                 const int32_t* cu_seqlens_q, const int32_t* seq_lens, void* o, float* lse,
+                                 int num_seqs, int max_seqlen_q, int total_q, int Hq, int Hkv, int d, int page_size,
+                                 int max_blocks_per_seq, int num_blocks, float scale, int causal, void* stream) {
+  auto aligned4 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; };
+  if (k_cache == nullptr || v_cache == nullptr || !aligned16(k_cache) || !aligned16(v_cache)) return ATTN_ERR_INVALID_ARG;
+  if (block_table == nullptr || cu_seqlens_q == nullptr || seq_lens == nullptr || !aligned4(block_table) ||
+      !aligned4(cu_seqlens_q) || !aligned4(seq_lens))
+    return ATTN_ERR_INVALID_ARG;
+  if (num_seqs < 1 || max_seqlen_q < 1 || total_q < 1 || max_blocks_per_seq < 1 || num_blocks < 1)
+    return ATTN_ERR_INVALID_ARG;
+  if (page_size != kPage) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_blocks) * kPage > (int64_t(1) << 30) ||
+      static_cast<int64_t>(max_blocks_per_seq) * kPage > (int64_t(1) << 30))
+    return ATTN_ERR_INVALID_ARG;
+  const PagedKV paged{k_cache, v_cache, block_table, seq_lens, max_blocks_per_seq, num_blocks};
+  return prefill_common(q, nullptr, nullptr, o, lse, 1, Hq, Hkv, total_q, d, scale, causal, cu_seqlens_q, num_seqs,
+                        max_seqlen_q, &paged, stream);
 }
 
 int attn_decode_num_slots(int max_blocks_per_seq, int page_size, int num_splits, int split_tokens) {

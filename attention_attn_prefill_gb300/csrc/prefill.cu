@@ -103,8 +103,10 @@ struct Layout {
 // One work tile: 128 query rows of one (sequence, query head).
 struct WorkTile {
   int b, hq, qt;  // sequence, query head, query tile within the sequence
-  int base, z;    // row and batch coordinates of the sequence's first token in the maps
-  int len;        // tokens of the sequence
+  int base, z;    // row and batch coordinates of the sequence's first query token in the maps
+  int len;        // query tokens of the sequence
+  int kv_len;     // keys of the sequence (len, or its cached tokens with paged K/V)
+  int q_off;      // position of its first query among the keys (kv_len - len with paged K/V, else 0)
 };
 
 // Walks this CTA's work tiles.  Tiles (query tile, sequence, head) are ordered longest first (the
@@ -129,17 +131,22 @@ struct TileWalk {
       if (p.cu_seqlens == nullptr) {
         t.base = 0;
         t.z = t.b;
-        t.len = p.S;
+        t.len = t.kv_len = p.S;
+        t.q_off = 0;
         return true;
       }
       const int s0 = p.cu_seqlens[t.b], s1 = p.cu_seqlens[t.b + 1];
-      if (s0 < 0 || s1 < s0 || s1 > p.S || s1 - s0 > p.num_qblocks * BM) {
+      const int kvl = p.kv_lens != nullptr ? p.kv_lens[t.b] : s1 - s0;
+      if (s0 < 0 || s1 < s0 || s1 > p.S || s1 - s0 > p.num_qblocks * BM || kvl < s1 - s0 ||
+          (p.kv_lens != nullptr && kvl > p.max_blocks * 16)) {
         set_error(&g_prefill_status, kDevBadSeqlens);
         continue;  // the sequence is skipped
       }
       t.base = s0;
       t.z = 0;
       t.len = s1 - s0;
+      t.kv_len = kvl;
+      t.q_off = kvl - t.len;
       if (t.qt * BM < t.len) return true;
     }
   }
@@ -149,7 +156,7 @@ template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                       const PrefillParams p) {
+                       const __grid_constant__ CUtensorMap tm_vrow, const PrefillParams p) {
   using L = Layout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if ((smem_u32(smem) & 1023u) != 0) {  // 128B-swizzled tiles need 1 KB alignment
@@ -185,11 +192,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.Hq / p.Hkv;
-  auto kv_tiles = [&](const WorkTile& t) { return (t.len + BN - 1) / BN; };
+  auto kv_tiles = [&](const WorkTile& t) { return (t.kv_len + BN - 1) / BN; };
   auto tile_nkv = [&](const WorkTile& t) {
     const int all = kv_tiles(t);
-    const int diag = (t.qt + 1) * (BM / BN);  // causal: key tiles up to the end of the query tile
+    // causal: key tiles up to the position of the tile's last query
+    const int diag = (t.q_off + t.qt * BM + BM - 1) / BN + 1;
     return p.causal && diag < all ? diag : all;
+  };
+  // K or V tile j of work tile t into one ring stage (one expect_tx for all of its boxes)
+  auto load_kv = [&](uint8_t* dst, const CUtensorMap* map, bool is_v, uint64_t* bar, int g, const WorkTile& t,
+                     int j) {
+    mbar_arrive_expect_tx(bar, L::KV_BYTES);
+    if (p.kv_lens == nullptr) {
+      for (int c = 0; c < L::CHUNKS; ++c)
+        tma_load_3d(dst + c * L::KV_PANEL, map, bar, g * D + c * 64, t.base + j * BN, t.z);
+      return;
+    }
+    // paged: BN / 16 pages of 16 rows through the block table.  Pages past the sequence are read
+    // from rows past the cache, which the copy fills with zeros.
+    const int32_t* bt = p.block_table + static_cast<size_t>(t.b) * p.max_blocks;
+    const int oob = p.num_blocks * 16;
+    int pids[BN / 16];  // all block-table reads first, so that their latencies overlap
+#pragma unroll
+    for (int pp = 0; pp < BN / 16; ++pp) {
+      const int page = j * (BN / 16) + pp;
+      pids[pp] = page * 16 < t.kv_len ? bt[page] : -1;
+    }
+#pragma unroll
+    for (int pp = 0; pp < BN / 16; ++pp) {
+      const int valid = t.kv_len - (j * (BN / 16) + pp) * 16;  // rows of this page that hold keys
+      int row0 = oob;
+      if (valid > 0) {
+        int pid = pids[pp];
+        if (pid < 0 || pid >= p.num_blocks) {
+          set_error(&g_prefill_status, kDevBadPage);
+          pid = 0;
+        }
+        row0 = pid * 16;
+      }
+      uint8_t* pd = dst + pp * 16 * PANEL_ROW;
+      if (is_v && valid > 0 && valid < 16) {
+        // the rows past the last key must be finite (P is 0 there, but 0 * NaN is not): row by row,
+        // the tail from past the cache
+#pragma unroll 1
+        for (int r = 0; r < 16; ++r)
+#pragma unroll 1
+          for (int c = 0; c < L::CHUNKS; ++c)
+            tma_load_3d(pd + c * L::KV_PANEL + r * PANEL_ROW, &tm_vrow, bar, c * 64, g, r < valid ? row0 + r : oob);
+      } else {
+        for (int c = 0; c < L::CHUNKS; ++c) tma_load_3d(pd + c * L::KV_PANEL, map, bar, c * 64, g, row0);
+      }
+    }
   };
   // loads of the first tile that are issued before the CTA barrier: Q, and as many K and V
   // tiles as the rings hold
@@ -238,18 +291,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int c = 0; c < L::CHUNKS; ++c)
         tma_load_3d(sQ + c * L::Q_PANEL, &tm_q, q_full, t.hq * D + c * 64, t.base + t.qt * BM, t.z);
       const int nk = first_loads(K_STAGES), nv = first_loads(V_STAGES);
-      for (int j = 0; j < nk; ++j) {
-        mbar_arrive_expect_tx(&k_full[j], L::KV_BYTES);
-        for (int c = 0; c < L::CHUNKS; ++c)
-          tma_load_3d(sK + j * L::KV_BYTES + c * L::KV_PANEL, &tm_k, &k_full[j], g * D + c * 64, t.base + j * BN,
-                      t.z);
-      }
-      for (int j = 0; j < nv; ++j) {
-        mbar_arrive_expect_tx(&v_full[j], L::KV_BYTES);
-        for (int c = 0; c < L::CHUNKS; ++c)
-          tma_load_3d(sV + j * L::KV_BYTES + c * L::KV_PANEL, &tm_v, &v_full[j], g * D + c * 64, t.base + j * BN,
-                      t.z);
-      }
+      for (int j = 0; j < nk; ++j) load_kv(sK + j * L::KV_BYTES, &tm_k, false, &k_full[j], g, t, j);
+      for (int j = 0; j < nv; ++j) load_kv(sV + j * L::KV_BYTES, &tm_v, true, &v_full[j], g, t, j);
     }
   }
   if (warp == MMA_WARP) {
@@ -293,10 +336,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int j = (k == 0 ? npre : 0); j < nkv; ++j) {
           const int st = issued % nst;
           if (!mbar_wait(&empty[st], ((issued / nst) & 1) ^ 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[st], L::KV_BYTES);
-          for (int c = 0; c < L::CHUNKS; ++c)
-            tma_load_3d(ring + st * L::KV_BYTES + c * L::KV_PANEL, map, &full[st], g * D + c * 64, t.base + j * BN,
-                        t.z);
+          load_kv(ring + st * L::KV_BYTES, map, !is_k, &full[st], g, t, j);
           ++issued;
         }
       }
@@ -402,6 +442,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     WorkTile t;
     for (int k = 0; walk.next(p, t); ++k) {
       const int q = t.qt * BM + row;  // query row within the sequence
+      const int qpos = t.q_off + q;   // its position among the keys
       const int nkv = tile_nkv(t);
       const int nkv_all = kv_tiles(t);
       float m_used = -INFINITY;  // raw-score max that O and l currently refer to
@@ -419,8 +460,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // the causal diagonal or the end of the sequence
         const int key0 = j * BN + h * HALF;
         int lim = HALF - 1;
-        if (p.causal && q - key0 < lim) lim = q - key0;
-        if (j == nkv_all - 1 && t.len - 1 - key0 < lim) lim = t.len - 1 - key0;
+        if (p.causal && qpos - key0 < lim) lim = qpos - key0;
+        if (j == nkv_all - 1 && t.kv_len - 1 - key0 < lim) lim = t.kv_len - 1 - key0;
         if (lim < HALF - 1) {
 #pragma unroll
           for (int c = 0; c < HALF; ++c)
@@ -610,7 +651,7 @@ cudaError_t launch(const PrefillMaps& m, const PrefillParams& p, cudaStream_t st
   }
   const long long tiles = static_cast<long long>(p.num_qblocks) * p.B * p.Hq;
   const int grid = static_cast<int>(tiles < g_num_sms ? tiles : g_num_sms);
-  kern<<<grid, NUM_THREADS, smem, stream>>>(m.q, m.k, m.v, m.o, p);
+  kern<<<grid, NUM_THREADS, smem, stream>>>(m.q, m.k, m.v, m.o, m.v_row, p);
   return cudaGetLastError();
 }
 

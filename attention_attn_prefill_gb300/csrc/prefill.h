@@ -12,16 +12,23 @@ namespace attn {
 // sequences); 3-D maps, 64-element x 128-row boxes, 128-byte swizzle.
 struct PrefillMaps {
   CUtensorMap q, k, v, o;
+  CUtensorMap v_row;  // paged K/V only: V with one-row boxes, for the last page of a sequence
 };
 
 // Two layouts share one kernel:
 //   * fixed length (cu_seqlens == null): B sequences of S tokens, maps [B][S][H*d], LSE [B][Hq][S];
 //   * packed (cu_seqlens != null): B sequences of cu_seqlens[n+1] - cu_seqlens[n] tokens stored
 //     back to back, S = total tokens, maps [1][S][H*d], LSE [Hq][S].
+//   * paged K/V (kv_lens != null, packed queries): sequence n's keys are its kv_lens[n] cached tokens,
+//     read through block_table (16-token pages; maps {d, Hkv, num_blocks*16}); its packed queries are
+//     the last cu_seqlens[n+1] - cu_seqlens[n] of them.
 struct PrefillParams {
   float* lse;                  // LSE (see above) or null
   void* o;                     // output base (bf16), for the rows of a partial packed tile
   const int32_t* cu_seqlens;   // [B + 1] or null
+  const int32_t* kv_lens;      // [B] cached tokens per sequence (paged K/V), or null
+  const int32_t* block_table;  // [B][max_blocks] (paged K/V)
+  int max_blocks, num_blocks;  // (paged K/V)
   int B, Hq, Hkv, S;
   float scale;       // natural-units score scale
   float scale_log2;  // scale * log2(e)

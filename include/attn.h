@@ -105,6 +105,39 @@ attn_status_t attn_prefill_varlen(const void* q, const void* k, const void* v, v
                                   int Hkv, int d, float scale, int causal, void* stream);
 
 /*
+ * Chunked prefill against the paged KV cache: the new tokens of each
+ * sequence attend to all of its cached tokens (their own K/V already
+ * appended to the cache) -- the prefill form of the varlen call with a block
+ * table that "GPU Datapath: Where Every Byte Moves in One LLM Inference
+ * Step", section "Measuring the Real Kernels, One at a Time", dispatches.
+ *   q, o         [total_q, Hq, d] bf16: the new tokens of every sequence,
+ *                back to back (o is output)
+ *   k_cache,
+ *   v_cache      [num_blocks, page_size, Hkv, d] bf16, as for
+ *                attn_decode_paged
+ *   block_table  [num_seqs, max_blocks_per_seq] int32, DEVICE memory
+ *   cu_seqlens_q [num_seqs + 1] int32, DEVICE memory: sequence n's new
+ *                tokens are q rows cu_seqlens_q[n] .. cu_seqlens_q[n+1]-1
+ *   seq_lens     [num_seqs] int32, DEVICE memory: cached tokens of sequence
+ *                n, its new tokens included (they are the last ones)
+ *   lse          [Hq, total_q] f32 (output, may be NULL)
+ *   max_seqlen_q upper bound of the new tokens per sequence (host value)
+ *   d in {64, 128, 256}; page_size == 16.
+ * New token i of sequence n sits at position seq_lens[n] - q_len + i; with
+ * causal != 0 it sees the keys at positions 0 .. that position, otherwise all
+ * seq_lens[n] keys.  Tokens of the last page past seq_len are never used,
+ * even if they hold NaN.  A sequence whose offsets break the rules of
+ * attn_prefill_varlen or whose seq_len is below its new tokens or beyond its
+ * block-table row is recorded as device status 5 and skipped; a block-table
+ * entry outside [0, num_blocks) as status 2 (page 0 is read instead).
+ * Arithmetic as for attn_prefill.
+ */
+attn_status_t attn_prefill_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                                 const int32_t* cu_seqlens_q, const int32_t* seq_lens, void* o, float* lse,
+                                 int num_seqs, int max_seqlen_q, int total_q, int Hq, int Hkv, int d, int page_size,
+                                 int max_blocks_per_seq, int num_blocks, float scale, int causal, void* stream);
+
+/*
  * Number of partial slots per (sequence, query head) that attn_decode_paged
  * uses for the given split settings (1 means the split kernel writes the
  * output directly and needs no workspace).
@@ -243,7 +276,8 @@ attn_status_t attn_combine(const float* part_o, const float* part_m, const float
  * clear (0 = none; 1 = a pipeline wait timed out; 2 = block-table entry out of
  * range; 3 = a seq_len the block table cannot cover; 4 = shared memory not
  * 1 KB-aligned; 5 = cu_seqlens decreasing, past total_tokens or longer than
- * max_seqlen) and, if `clear` != 0, resets it.
+ * max_seqlen, or a seq_len that does not fit its chunk or block table) and, if
+ * `clear` != 0, resets it.
  */
 attn_status_t attn_device_status(uint32_t* code, int clear);
 

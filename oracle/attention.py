@@ -172,6 +172,45 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale: float, *,
 # the partials are merged with weights l_i * exp(m_i - M).
 # ---------------------------------------------------------------------------
 
+def prefill_paged(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, scale: float, causal: bool = True, *,
+                  seqs=None, heads=None) -> tuple[np.ndarray, np.ndarray]:
+    """Chunked prefill against a paged cache.
+
+    Sequence n has seq_lens[n] cached tokens (read through its block-table row) and its new tokens
+    are q rows cu_seqlens_q[n] .. cu_seqlens_q[n+1]-1, the last ones of the sequence: new token i sits
+    at position seq_lens[n] - q_len + i and, causally, sees the keys up to that position.  Returns
+    o [T,Hq,d] and lse [Hq,T] in float64 (NaN outside the sampled sequences/heads).  The per-row
+    definition is that of "What attention is trying to calculate" ("Why your local LLM feels dumber
+    than it is"); the paging follows section D of "GPU Datapath: Where Every Byte Moves in One LLM
+    Inference Step".
+    """
+    q = f64(q)
+    bt = np.asarray(block_table.cpu() if isinstance(block_table, torch.Tensor) else block_table)
+    cu = [int(x) for x in (cu_seqlens_q.tolist() if isinstance(cu_seqlens_q, torch.Tensor) else cu_seqlens_q)]
+    lens = [int(x) for x in (seq_lens.tolist() if isinstance(seq_lens, torch.Tensor) else seq_lens)]
+    T, Hq, _ = q.shape
+    page, Hkv, dv = k_cache.shape[1], k_cache.shape[2], v_cache.shape[3]
+    kc, vc = _PageView(k_cache), _PageView(v_cache)
+    o = np.full((T, Hq, dv), np.nan)
+    lse = np.full((Hq, T), np.nan)
+    heads = range(Hq) if heads is None else heads
+    seqs = range(len(lens)) if seqs is None else seqs
+    for n in seqs:
+        s0, s1, L = cu[n], cu[n + 1], lens[n]
+        if s1 <= s0:
+            continue
+        keys = gather_pages(kc, bt[n], L, page)
+        vals = gather_pages(vc, bt[n], L, page)
+        pos = L - (s1 - s0) + np.arange(s1 - s0)
+        visible = (np.arange(L)[None, :] <= pos[:, None]) if causal else None
+        for hq in heads:
+            g = kv_head_of(hq, Hq, Hkv)
+            ob, lb = attend(q[s0:s1, hq, :], keys[:, g, :], vals[:, g, :], scale, visible)
+            o[s0:s1, hq, :] = ob
+            lse[hq, s0:s1] = lb
+    return o, lse
+
+
 def split_ranges(seq_len: int, *, num_splits: int = 0, split_tokens: int = 0,
                  page: int = 16) -> list[tuple[int, int]]:
     """Contiguous, page-aligned token ranges of one sequence (empty ranges dropped).

@@ -20,7 +20,7 @@ import scipy.special as sps
 import torch
 
 import oracle.attention as oa
-from workloads import make_decode_inputs, make_prefill_inputs, make_varlen_inputs, randn_bf16
+from workloads import make_chunked_inputs, make_decode_inputs, make_prefill_inputs, make_varlen_inputs, randn_bf16
 from workloads.teaching import teaching_scores_values
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -305,6 +305,35 @@ def check_varlen_sequences_isolated():
     assert not np.allclose(o1[7:11], o0[7:11])
 
 
+def check_chunked_prefill_matches_scipy():
+    """Chunked prefill: each new token against scipy's softmax over the contiguous keys up to its position."""
+    ctx, ql = [20, 37, 16, 50, 9], [20, 5, 1, 0, 9]
+    x = make_chunked_inputs(ctx, ql, Hq=4, Hkv=2, d=6, seed=34, nan_tail=True, extra_blocks=2)
+    o, lse = oa.prefill_paged(x.q, x.k_cache, x.v_cache, x.block_table, x.cu_seqlens_q, x.seq_lens, 0.4)
+    q, kc, vc = oa.f64(x.q), oa.f64(x.k_cache), oa.f64(x.v_cache)
+    cu = x.cu_seqlens_q.tolist()
+    for n, L in enumerate(ctx):
+        pids = x.block_table[n, :(L + 15) // 16].tolist()
+        keys = np.concatenate([kc[p] for p in pids])[:L]
+        vals = np.concatenate([vc[p] for p in pids])[:L]
+        for i in range(ql[n]):
+            pos = L - ql[n] + i
+            for h in range(4):
+                s = 0.4 * keys[:pos + 1, h // 2] @ q[cu[n] + i, h]
+                _close(o[cu[n] + i, h], sps.softmax(s) @ vals[:pos + 1, h // 2], rtol=1e-12, atol=1e-13,
+                       what="chunked o")
+                _close(lse[h, cu[n] + i], sps.logsumexp(s), what="chunked lse")
+
+
+def check_chunked_last_token_is_decode():
+    """A one-token chunk at the end of each sequence is exactly the paged decode of that token."""
+    ctx = [33, 16, 70]
+    x = make_chunked_inputs(ctx, [1, 1, 1], Hq=4, Hkv=1, d=8, seed=35, nan_tail=True)
+    o, lse = oa.prefill_paged(x.q, x.k_cache, x.v_cache, x.block_table, x.cu_seqlens_q, x.seq_lens, 0.3)
+    od, ld = oa.decode_paged(x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens, 0.3)
+    assert np.array_equal(o, od) and np.array_equal(lse, ld.T)
+
+
 ALL_CHECKS = [
     check_worked_example_exact,
     check_worked_example_paged,
@@ -324,5 +353,7 @@ ALL_CHECKS = [
     check_varlen_matches_scipy,
     check_varlen_single_token_sequences,
     check_varlen_sequences_isolated,
+    check_chunked_prefill_matches_scipy,
+    check_chunked_last_token_is_decode,
     check_brute_force_tiny,
 ]

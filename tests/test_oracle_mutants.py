@@ -106,6 +106,41 @@ def varlen_shifted_slice(q, k, v, cu_seqlens, scale, causal=True, *, heads=None,
 
 
 ORIG_VARLEN = oa.prefill_varlen
+ORIG_PAGED = oa.prefill_paged
+
+
+def chunked_positions_from_zero(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, scale, causal=True, *,
+                                seqs=None, heads=None):
+    """New tokens treated as if they opened the sequence (offset dropped)."""
+    q = oa.f64(q)
+    cu = [int(x) for x in cu_seqlens_q.tolist()]
+    lens = [int(x) for x in seq_lens.tolist()]
+    T, Hq, _ = q.shape
+    o = np.full((T, Hq, v_cache.shape[3]), np.nan)
+    lse = np.full((Hq, T), np.nan)
+    for n, L in enumerate(lens):
+        s0, s1 = cu[n], cu[n + 1]
+        if s1 <= s0:
+            continue
+        keys = oa.gather_pages(oa._PageView(k_cache), block_table[n].tolist(), L, 16)
+        vals = oa.gather_pages(oa._PageView(v_cache), block_table[n].tolist(), L, 16)
+        pos = np.arange(s1 - s0)
+        vis = np.arange(L)[None, :] <= pos[:, None]
+        for h in range(Hq):
+            g = oa.kv_head_of(h, Hq, k_cache.shape[2])
+            ob, lb = oa.attend(q[s0:s1, h], keys[:, g], vals[:, g], scale, vis)
+            o[s0:s1, h], lse[h, s0:s1] = ob, lb
+    return o, lse
+
+
+def chunked_keys_of_chunk_only(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, scale, causal=True, *,
+                               seqs=None, heads=None):
+    """Only the chunk's own tokens used as keys (the earlier context dropped)."""
+    cu = cu_seqlens_q.tolist()
+    ql = [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+    import torch as _t
+    return ORIG_PAGED(q, k_cache, v_cache, block_table, cu_seqlens_q, _t.tensor(ql, dtype=_t.int32), scale, causal,
+                      seqs=seqs, heads=heads)
 
 MUTANTS = [
     ("attend", attend_no_scale),
@@ -119,6 +154,8 @@ MUTANTS = [
     ("combine", combine_ignores_max),
     ("prefill_varlen", varlen_positions_from_pack_start),
     ("prefill_varlen", varlen_shifted_slice),
+    ("prefill_paged", chunked_positions_from_zero),
+    ("prefill_paged", chunked_keys_of_chunk_only),
 ]
 
 

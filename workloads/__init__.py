@@ -231,6 +231,33 @@ def make_decode_inputs(lens, Hq: int, Hkv: int, d: int, seed: int, *, nan_tail: 
     return DecodeInputs(q, k_cache, v_cache, block_table, torch.tensor(lens, dtype=torch.int32))
 
 
+@dataclass
+class ChunkedInputs:
+    q: torch.Tensor             # [T, Hq, d] bf16: the new tokens of every sequence, back to back
+    k_cache: torch.Tensor       # [num_blocks, PAGE, Hkv, d] bf16 (all cached tokens, new ones included)
+    v_cache: torch.Tensor
+    block_table: torch.Tensor   # [N, max_blocks] int32
+    seq_lens: torch.Tensor      # [N] int32 cached tokens per sequence
+    cu_seqlens_q: torch.Tensor  # [N + 1] int32 offsets of the new tokens
+
+    @property
+    def max_seqlen_q(self) -> int:
+        return max(1, int((self.cu_seqlens_q[1:] - self.cu_seqlens_q[:-1]).max()))
+
+
+def make_chunked_inputs(ctx_lens, q_lens, Hq: int, Hkv: int, d: int, seed: int, **kw) -> ChunkedInputs:
+    """A paged cache of ctx_lens tokens per sequence (as make_decode_inputs) and q_lens new query
+    tokens per sequence (its last q_lens cached tokens), packed."""
+    if any(int(a) > int(b) for a, b in zip(q_lens, ctx_lens)):
+        raise ValueError("a chunk cannot be longer than its sequence")
+    x = make_decode_inputs(ctx_lens, Hq, Hkv, d, seed, **kw)
+    g = _gen(seed + 7919)
+    q = randn_bf16((int(sum(q_lens)), Hq, d), g)
+    cu = torch.zeros(len(q_lens) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor([int(v) for v in q_lens], dtype=torch.int64), 0).to(torch.int32)
+    return ChunkedInputs(q, x.k_cache, x.v_cache, x.block_table, x.seq_lens, cu)
+
+
 def decode_inputs_for(cfg: DecodeConfig, **kw) -> DecodeInputs:
     return make_decode_inputs(decode_lens_for(cfg), cfg.Hq, cfg.Hkv, cfg.d, cfg.seed, **kw)
 
