@@ -98,6 +98,7 @@ struct Layout {
   static_assert(ALLOC <= 232448, "shared memory budget");
   static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
   static_assert(HALF == 64 || HALF == 32, "softmax handles 32 or 64 keys per thread");
+  static_assert((BN / 16) * CHUNKS <= 32, "one paged K/V copy per producer lane");
 };
 
 // One work tile: 128 query rows of one (sequence, query head).
@@ -199,25 +200,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int diag = (t.q_off + t.qt * BM + BM - 1) / BN + 1;
     return p.causal && diag < all ? diag : all;
   };
+  // Paged K/V: the physical page of each of the BN / 16 pages of key tile j (-1 past the sequence).
+  // The producers read them before waiting for a free stage, so the reads overlap the wait.
+  auto fetch_pages = [&](const WorkTile& t, int j, int (&pids)[BN / 16]) {
+    const int32_t* bt = p.block_table + static_cast<size_t>(t.b) * p.max_blocks;
+#pragma unroll
+    for (int pp = 0; pp < BN / 16; ++pp) {
+      const int page = j * (BN / 16) + pp;
+      pids[pp] = page * 16 < t.kv_len ? bt[page] : -1;
+    }
+  };
   // K or V tile j of work tile t into one ring stage (one expect_tx for all of its boxes)
   auto load_kv = [&](uint8_t* dst, const CUtensorMap* map, bool is_v, uint64_t* bar, int g, const WorkTile& t,
-                     int j) {
+                     int j, const int (&pids)[BN / 16]) {
     mbar_arrive_expect_tx(bar, L::KV_BYTES);
     if (p.kv_lens == nullptr) {
       for (int c = 0; c < L::CHUNKS; ++c)
         tma_load_3d(dst + c * L::KV_PANEL, map, bar, g * D + c * 64, t.base + j * BN, t.z);
       return;
     }
-    // paged: BN / 16 pages of 16 rows through the block table.  Pages past the sequence are read
-    // from rows past the cache, which the copy fills with zeros.
-    const int32_t* bt = p.block_table + static_cast<size_t>(t.b) * p.max_blocks;
+    // paged: BN / 16 pages of 16 rows.  Pages past the sequence are read from rows past the cache,
+    // which the copy fills with zeros.
     const int oob = p.num_blocks * 16;
-    int pids[BN / 16];  // all block-table reads first, so that their latencies overlap
-#pragma unroll
-    for (int pp = 0; pp < BN / 16; ++pp) {
-      const int page = j * (BN / 16) + pp;
-      pids[pp] = page * 16 < t.kv_len ? bt[page] : -1;
-    }
 #pragma unroll
     for (int pp = 0; pp < BN / 16; ++pp) {
       const int valid = t.kv_len - (j * (BN / 16) + pp) * 16;  // rows of this page that hold keys
@@ -291,8 +295,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int c = 0; c < L::CHUNKS; ++c)
         tma_load_3d(sQ + c * L::Q_PANEL, &tm_q, q_full, t.hq * D + c * 64, t.base + t.qt * BM, t.z);
       const int nk = first_loads(K_STAGES), nv = first_loads(V_STAGES);
-      for (int j = 0; j < nk; ++j) load_kv(sK + j * L::KV_BYTES, &tm_k, false, &k_full[j], g, t, j);
-      for (int j = 0; j < nv; ++j) load_kv(sV + j * L::KV_BYTES, &tm_v, true, &v_full[j], g, t, j);
+      int pids[BN / 16] = {};
+      for (int j = 0; j < nk; ++j) {
+        if (p.kv_lens != nullptr) fetch_pages(t, j, pids);
+        load_kv(sK + j * L::KV_BYTES, &tm_k, false, &k_full[j], g, t, j, pids);
+      }
+      for (int j = 0; j < nv; ++j) {
+        if (p.kv_lens != nullptr) fetch_pages(t, j, pids);
+        load_kv(sV + j * L::KV_BYTES, &tm_v, true, &v_full[j], g, t, j, pids);
+      }
     }
   }
   if (warp == MMA_WARP) {
@@ -307,8 +318,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == PRODUCER_WARP || warp == V_WARP) {
     // ------------------------------------------------------------ TMA producers
     // Warp 8 loads Q and the K tiles, warp 11 the V tiles; each waits only on its own ring.
-    // Counters run across work tiles, so the rings never drain between tiles.
-    if (lane == 0) {
+    // Counters run across work tiles, so the rings never drain between tiles.  The whole warp runs
+    // the loop: with paged K/V, lane l reads the physical page of page l of the tile and the lanes
+    // issue one 16-row copy each, so the many small copies of a tile leave in one instruction.
+    {
       const bool is_k = warp == PRODUCER_WARP;
       const int nst = is_k ? K_STAGES : V_STAGES;
       uint64_t* full = is_k ? k_full : v_full;
@@ -316,6 +329,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint8_t* ring = is_k ? sK : sV;
       const CUtensorMap* map = is_k ? &tm_k : &tm_v;
       const int npre = first_loads(nst);
+      constexpr int PAGES = BN / 16;
       bool ok = true;
       int issued = npre, nq = 0;
       TileWalk walk;
@@ -325,26 +339,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (is_k) {
           // Q of this tile replaces the previous one once all of its S = Q K^T products are done
           if (k > 0) {
-            if (!mbar_wait(q_empty, (k - 1) & 1)) { ok = false; break; }
-            mbar_arrive_expect_tx(q_full, L::Q_BYTES);
-            for (int c = 0; c < L::CHUNKS; ++c)
-              tma_load_3d(sQ + c * L::Q_PANEL, &tm_q, q_full, t.hq * D + c * 64, t.base + t.qt * BM, t.z);
+            ok = __all_sync(0xffffffffu, mbar_wait(q_empty, (k - 1) & 1));
+            if (!ok) break;
+            if (lane == 0) {
+              mbar_arrive_expect_tx(q_full, L::Q_BYTES);
+              for (int c = 0; c < L::CHUNKS; ++c)
+                tma_load_3d(sQ + c * L::Q_PANEL, &tm_q, q_full, t.hq * D + c * 64, t.base + t.qt * BM, t.z);
+            }
           }
           nq = k + 1;
         }
         const int nkv = tile_nkv(t);
         for (int j = (k == 0 ? npre : 0); j < nkv; ++j) {
           const int st = issued % nst;
-          if (!mbar_wait(&empty[st], ((issued / nst) & 1) ^ 1)) { ok = false; break; }
-          load_kv(ring + st * L::KV_BYTES, map, !is_k, &full[st], g, t, j);
+          uint8_t* dst = ring + st * L::KV_BYTES;
+          // paged: lane l < PAGES reads the physical page of page l of this tile before the wait
+          int my_pid = -1;
+          if (p.kv_lens != nullptr && lane < PAGES) {
+            const int page = j * PAGES + lane;
+            if (page * 16 < t.kv_len) my_pid = p.block_table[static_cast<size_t>(t.b) * p.max_blocks + page];
+          }
+          ok = __all_sync(0xffffffffu, mbar_wait(&empty[st], ((issued / nst) & 1) ^ 1));
+          if (!ok) break;
+          if (lane == 0) mbar_arrive_expect_tx(&full[st], L::KV_BYTES);
+          __syncwarp();
+          if (p.kv_lens == nullptr) {
+            if (lane < L::CHUNKS)
+              tma_load_3d(dst + lane * L::KV_PANEL, map, &full[st], g * D + lane * 64, t.base + j * BN, t.z);
+          } else {
+            // lane l: page l / CHUNKS, 64-column chunk l % CHUNKS.  Pages past the sequence are read
+            // from rows past the cache, which the copy fills with zeros.
+            const int pp = lane / L::CHUNKS, c = lane % L::CHUNKS;
+            int pid = __shfl_sync(0xffffffffu, my_pid, pp < PAGES ? pp : 0);
+            if (pp < PAGES) {
+              const int oob = p.num_blocks * 16;
+              const int valid = t.kv_len - (j * PAGES + pp) * 16;  // rows of this page that hold keys
+              int row0 = oob;
+              if (valid > 0) {
+                if (pid < 0 || pid >= p.num_blocks) {
+                  set_error(&g_prefill_status, kDevBadPage);
+                  pid = 0;
+                }
+                row0 = pid * 16;
+              }
+              uint8_t* pd = dst + c * L::KV_PANEL + pp * 16 * PANEL_ROW;
+              if (!is_k && valid > 0 && valid < 16) {
+                // the V rows past the last key must be finite (P is 0 there, but 0 * NaN is not):
+                // row by row, the tail from past the cache
+                for (int r = 0; r < 16; ++r)
+                  tma_load_3d(pd + r * PANEL_ROW, &tm_vrow, &full[st], c * 64, g, r < valid ? row0 + r : oob);
+              } else {
+                tma_load_3d(pd, map, &full[st], c * 64, g, row0);
+              }
+            }
+          }
           ++issued;
         }
       }
-      if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
-      // Drain: every copy started here must have landed before the CTA exits.  The newest
-      // copy of each stage is the one whose phase is current.
-      for (int i = (issued > nst ? issued - nst : 0); i < issued; ++i) mbar_wait(&full[i % nst], (i / nst) & 1);
-      if (nq > 0) mbar_wait(q_full, (nq - 1) & 1);
+      if (lane == 0) {
+        if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
+        // Drain: every copy started here must have landed before the CTA exits.  The newest
+        // copy of each stage is the one whose phase is current.
+        for (int i = (issued > nst ? issued - nst : 0); i < issued; ++i) mbar_wait(&full[i % nst], (i / nst) & 1);
+        if (nq > 0) mbar_wait(q_full, (nq - 1) & 1);
+      }
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ S = Q K^T issue

@@ -40,7 +40,8 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from workloads import LLAMA8B, PAGED, decode_inputs_for, decode_lens_for, decode_min_bytes, prefill_inputs_for  # noqa
+from workloads import (LLAMA8B, PAGED, decode_inputs_for, decode_lens_for, decode_min_bytes, make_chunked_inputs,  # noqa
+                       prefill_inputs_for)
 
 METRIC = "prefill TFLOP/s & decode KV GB/s on 1 GB300, as % of bf16 TC peak / HBM peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -426,6 +427,8 @@ def run_case(args):
 
     prefill:<name>            name in {tiny, llama8b_prefill, sweep_s1024, sweep_s2048, sweep_s4096,
                               qwen_d256_prefill}
+    chunked:<n>x<q>of<ctx>    chunked prefill against the paged cache, Llama-8B heads: n sequences of
+                              ctx cached tokens whose last q are new
     decode:<name>:<splits>    name in {paged_decode, longctx_decode}; splits = num_splits (0 = balanced
                               mode), t<N> for split_tokens = N, or auto for the split-count rule
     """
@@ -436,7 +439,24 @@ def run_case(args):
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream(dev)
     kind, name, *rest = args.case.split(":")
-    if kind == "prefill":
+    if kind == "chunked":
+        # chunked prefill against the paged cache: <n> sequences of <ctx> cached tokens, the last <q> new
+        # (name = "<n>x<q>of<ctx>"), Llama-8B heads
+        n, rest_ = name.split("x")
+        qn, ctxn = (int(v) for v in rest_.split("of"))
+        n = int(n)
+        Hq, Hkv, d = 32, 8, 128
+        x = make_chunked_inputs([ctxn] * n, [qn] * n, Hq=Hq, Hkv=Hkv, d=d, seed=11)
+        args_ = [t.to(dev) for t in (x.q, x.k_cache, x.v_cache, x.block_table, x.cu_seqlens_q, x.seq_lens)]
+        o = torch.empty_like(args_[0])
+        lse = torch.empty((Hq, x.q.shape[0]), dtype=torch.float32, device=dev)
+        pairs = n * sum(ctxn - qn + i + 1 for i in range(qn))
+        work, unit = 4.0 * Hq * d * pairs / 1e12, "TFLOP/s"
+
+        def launch():
+            attn.prefill_paged(*args_, x.max_seqlen_q, scale=1.0 / math.sqrt(d), causal=True, out=o, lse=lse,
+                               stream=stream)
+    elif kind == "prefill":
         cfg = {c.name: c for c in PREFILL_CONFIGS}[name]
         x = prefill_inputs_for(cfg)
         q, k, v = (t.to(dev) for t in (x.q, x.k, x.v))
