@@ -362,11 +362,73 @@ def run_gpu(args):
         "wall_s_timed": round(wall, 3),
         "device_status": status,
     }
+    if not args.no_workloads:
+        line["workloads"] = workload_table(attn, dev, stream, flush, peaks, (dx, (dq, kc, vc, bt, sl)))
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def workload_table(attn, dev, stream, flush, peaks, paged_inputs, reps: int = 10):
+    """Every seeded workload (outside the timed region): mean of `reps` launches, L2 flushed before each."""
+    from workloads import DECODE_CONFIGS, PREFILL_CONFIGS
+
+    def timed(launch):
+        launch()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            launch()
+            b.record(stream)
+            ms.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ms)
+
+    out = {}
+    for cfg in PREFILL_CONFIGS:
+        x = prefill_inputs_for(cfg)
+        q, k, v = (t.to(dev) for t in (x.q, x.k, x.v))
+        o = torch.empty_like(q)
+        lse = torch.empty((cfg.B, cfg.Hq, cfg.S), dtype=torch.float32, device=dev)
+        ms = timed(lambda: attn.prefill(q, k, v, scale=cfg.scale, causal=True, out=o, lse=lse, stream=stream))
+        tf = cfg.causal_flops / (ms * 1e-3) / 1e12
+        out[cfg.name] = {"TFLOP/s": round(tf, 1), "us": round(ms * 1e3, 1),
+                         "frac": round(tf / peaks["bf16_tflops"], 4)}
+        del q, k, v, o, lse
+    for cfg in DECODE_CONFIGS:
+        if cfg.name == "paged_decode":
+            x, (dq, kc, vc, bt, sl) = paged_inputs
+        else:
+            x = decode_inputs_for(cfg)
+            dq, kc, vc, bt, sl = (t.to(dev) for t in (x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens))
+        lens = decode_lens_for(cfg)
+        nbytes = decode_min_bytes(lens, cfg.Hq, cfg.Hkv, cfg.d)
+        do = torch.empty_like(dq)
+        dl = torch.empty((cfg.N, cfg.Hq), dtype=torch.float32, device=dev)
+        specs = [dict(num_splits=n) for n in cfg.num_splits] + [dict(split_tokens=t) for t in cfg.split_tokens]
+        specs += [dict(num_splits=attn.decode_auto_splits(cfg.N, cfg.Hkv, cfg.d, x.max_blocks)),
+                  dict(num_splits=0)]
+        names = [f"splits={sp['num_splits']}" if "num_splits" in sp else f"split_tokens={sp['split_tokens']}"
+                 for sp in specs]
+        names[-2] = f"auto ({specs[-2]['num_splits']} splits)"
+        names[-1] = "balanced"
+        for name, sp in zip(names, specs):
+            ws = torch.empty(max(1, decode_ws_bytes(attn, x.max_blocks, cfg, **sp)), dtype=torch.uint8, device=dev)
+            ms = timed(lambda: attn.decode_paged(dq, kc, vc, bt, sl, scale=cfg.scale, out=do, lse=dl, workspace=ws,
+                                                 stream=stream, **sp))
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            out[f"{cfg.name} {name}"] = {"GB/s": round(gbs, 1), "us": round(ms * 1e3, 1),
+                                         "frac": round(gbs / peaks["hbm_gbs"], 4)}
+    out["_note"] = (f"each: mean of {reps} launches with L2 flushed before each, outside the timed region; "
+                    "frac against the measured bf16 dense peak (prefill) or HBM copy (decode)")
+    if attn.device_status(clear=True) != 0:
+        out["_device_status"] = "nonzero"
+    return out
 
 
 # ---------------------------------------------------------------------------- CPU oracle
@@ -519,6 +581,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-heads", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the per-workload table")
     ap.add_argument("--case", default="", help="profile one kernel on one workload (see run_case)")
     args = ap.parse_args()
     if args.case:
