@@ -58,6 +58,37 @@ def test_decode_argument_checks(attn, over, want):
     assert attn.lib().attn_decode_paged(*_decode_args(**over)) == want
 
 
+def _varlen_args(**over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, cu=FAKE, N=3, maxs=100, T=300, Hq=4, Hkv=2, d=128,
+             scale=0.1, causal=1, stream=None)
+    a.update(over)
+    return tuple(a.values())
+
+
+@pytest.mark.parametrize("over,want", [
+    (dict(cu=None), 1), (dict(cu=FAKE + 2), 1), (dict(N=0), 1), (dict(maxs=0), 1), (dict(T=0), 1),
+    (dict(Hkv=3), 1), (dict(d=96), 2), (dict(q=FAKE + 8), 1), (dict(scale=float("inf")), 1),
+])
+def test_prefill_varlen_argument_checks(attn, over, want):
+    assert attn.lib().attn_prefill_varlen(*_varlen_args(**over)) == want
+
+
+def _paged_prefill_args(**over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cu=FAKE, lens=FAKE, o=FAKE, lse=None, N=2, maxq=64, T=100, Hq=8,
+             Hkv=2, d=128, page=16, maxb=8, nblocks=16, scale=0.1, causal=1, stream=None)
+    a.update(over)
+    return tuple(a.values())
+
+
+@pytest.mark.parametrize("over,want", [
+    (dict(bt=None), 1), (dict(cu=None), 1), (dict(lens=None), 1), (dict(k=None), 1), (dict(v=FAKE + 2), 1),
+    (dict(bt=FAKE + 2), 1), (dict(N=0), 1), (dict(maxq=0), 1), (dict(nblocks=0), 1), (dict(maxb=0), 1),
+    (dict(page=32), 2), (dict(d=96), 2), (dict(Hkv=3), 1),
+])
+def test_prefill_paged_argument_checks(attn, over, want):
+    assert attn.lib().attn_prefill_paged(*_paged_prefill_args(**over)) == want
+
+
 def test_combine_argument_checks(attn):
     lib = attn.lib()
     assert lib.attn_combine(None, FAKE, FAKE, 4, 2, 128, FAKE, None, None) == 1
