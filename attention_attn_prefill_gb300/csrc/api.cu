@@ -91,7 +91,7 @@ attn_status_t prefill_common(const void* q, const void* k, const void* v, void* 
   if (!aligned16(q) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
   if (batch < 1 || rows < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;  // masked keys stay -inf only under a positive scale
   if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
   // TMA coordinates are int32 and each map dimension must stay below 2^32
   if (static_cast<int64_t>(Hq) * d > (1 << 30) || rows > (1 << 30) || batch > 65535 || Hq > 65535 ||
@@ -247,7 +247,7 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
   if (num_seqs < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_blocks_per_seq < 1 || num_blocks < 1)
     return ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;  // masked keys stay -inf only under a positive scale
   if (page_size != kPage) return ATTN_ERR_UNSUPPORTED;
   if (d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
   if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;  // query heads per KV head fill at most 16 MMA rows

@@ -68,7 +68,10 @@ const char* attn_status_string(attn_status_t status);
  *   lse [B, Hq, S]     f32 (output, may be NULL)
  *   d in {64, 128, 256}; B, S >= 1; Hq, Hkv >= 1 with Hq % Hkv == 0.  d = 256
  *   uses 64-key tiles (the rest 128-key tiles).
- *   scale: multiplier of q.k (for example 1/sqrt(d)).
+ *   scale: multiplier of q.k (for example 1/sqrt(d)); finite and > 0, else
+ *   ATTN_ERR_INVALID_ARG (the kernels keep the row maximum in unscaled units
+ *   and mask keys with -inf before scaling).  The same holds for every entry
+ *   point below that takes a scale.
  *   causal != 0: row i sees keys 0..i (itself included); causal == 0: all S keys.
  * Row i of o is sum_j softmax_j(scale * q_i.k_j) v_j over the visible keys;
  * lse[b, h, i] = ln sum_j exp(scale * q_i.k_j).

@@ -36,6 +36,8 @@ FAKE = 0x10000  # an aligned non-null address; never dereferenced by the host ch
     ((FAKE, FAKE, FAKE, FAKE, FAKE + 1, 1, 4, 2, 64, 128, 0.1, 1, None), 1),      # misaligned lse
     ((FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 64, 96, 0.1, 1, None), 2),           # d = 96 unsupported
     ((FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 64, 128, float("nan"), 1, None), 1), # NaN scale
+    ((FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 64, 128, 0.0, 1, None), 1),          # scale 0
+    ((FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 64, 128, -0.1, 1, None), 1),         # negative scale
 ])
 def test_prefill_argument_checks(attn, args, want):
     assert attn.lib().attn_prefill(*args) == want
@@ -52,6 +54,7 @@ def _decode_args(**over):
     (dict(q=None), 1), (dict(bt=FAKE + 2), 1), (dict(N=0), 1), (dict(Hkv=3), 1),
     (dict(page=32), 2), (dict(d=64), 2), (dict(Hq=40, Hkv=2), 2),
     (dict(ns=-1), 1), (dict(st=24), 1),                      # bad split count; split_tokens not a page multiple
+    (dict(scale=0.0), 1), (dict(scale=-1.0), 1),
     (dict(ws=None), 3), (dict(wsb=10), 3), (dict(ws=FAKE + 4), 3),
 ])
 def test_decode_argument_checks(attn, over, want):

@@ -141,3 +141,26 @@ def test_sweep_full_size_sampled(attn, gpu, cfg):
 def test_d256_8k_prompt_sampled(attn, gpu):
     """Head dim 256 (64-key tiles): Hq=16, Hkv=2, S=8192, scale 2^-4; sampled rows of three heads."""
     _sampled(attn, gpu, QWEN256, heads=[0, 7, 15], nrows=24, seed=9)
+
+
+def test_vanishing_scale_gives_prefix_means(attn, gpu):
+    """scale -> 0 (1e-30; 0 itself is refused): every visible key weighs the same, so row i is the
+    mean of v_0..v_i and LSE = ln(i+1)."""
+    x = make_prefill_inputs(1, 2, 1, 300, 128, seed=12)
+    o, lse = run_prefill(attn, x, 1e-30, True, gpu)
+    v = x.v[0, :, 0].double()
+    want = torch.cumsum(v, 0) / torch.arange(1, 301, dtype=torch.float64)[:, None]
+    for h in range(2):
+        check_o(to_np(o)[0, :, h], want.numpy(), "prefix means")
+        check_lse(to_np(lse)[0, h], np.log(np.arange(1, 301)), "ln(i+1)")
+
+
+def test_long_sequence_sampled(attn, gpu):
+    """One 32K-token sequence (256 query tiles, up to 256 key tiles per row); sampled rows."""
+    cfg_S = 32768
+    x = make_prefill_inputs(1, 2, 1, cfg_S, 128, seed=13)
+    o, lse = run_prefill(attn, x, 1.0 / math.sqrt(128), True, gpu)
+    rows = np.array([0, 1, 127, 128, 4095, 4096, 20000, cfg_S - 129, cfg_S - 1])
+    wo, wl = oa.prefill(x.q, x.k, x.v, 1.0 / math.sqrt(128), causal=True, rows=rows)
+    check_o(to_np(o)[0, rows], wo[0, rows], "32K rows")
+    check_lse(to_np(lse)[0][:, rows], wl[0][:, rows], "32K lse")
