@@ -8,32 +8,35 @@
 // How (the tiled flow of "Streaming process -- How the SM works inside a
 // transformer", Steps 3-8 and its code snippet, redesigned for tcgen05):
 //   * the kernel is persistent: one CTA per SM walks a list of work tiles
-//     (one 128-row Q tile of one (batch, query head) each), longest causal
-//     tiles first, and keeps its pipelines running across tile boundaries;
-//   * two producer threads, in two warps, stream Q (once per tile, Step 3)
-//     and 128-key K and V tiles through shared-memory rings (two K stages,
-//     three V stages) with mbarrier full/empty pairs (Step 6);
+//     (one 128-row Q tile of one (sequence, query head) each), longest causal
+//     tiles first, and keeps its pipelines running across tile boundaries.
+//     Sequences are a batch of equal length, packed (cu_seqlens), or new
+//     tokens whose keys come from a paged KV cache (block table);
+//   * two producer warps stream Q (once per tile, Step 3) and the K and V
+//     tiles (128 keys; 64 at d = 256) through shared-memory rings (two K
+//     stages, three V stages; two at d = 256) with mbarrier full/empty pairs
+//     (Step 6).  With a paged cache each lane issues one 16-token page copy;
 //   * one thread issues S_j = Q K_j^T into TMEM (Step 4).  S is triple-buffered
 //     in TMEM, so the tensor core computes S two steps ahead of softmax.  A
 //     second thread, in another warp, issues O += P_j V_j with P (bf16, over
-//     the first 64 columns of S_j's buffer) read straight from TMEM once
-//     softmax has written it (Step 7).  tcgen05.mma blocks its issuing thread
-//     while the tensor core's queue is full, so two issuers let one of them
-//     wait on a barrier while the other keeps the queue fed;
-//   * eight softmax warps share every row: warpgroup h takes key columns
-//     64h..64h+63.  Each thread reads its 64 scores from TMEM, masks, takes the
-//     row max (the two halves of a row exchange theirs through shared memory),
-//     exponentiates with ex2 and keeps its share of the running sum (Step 5).
-//     O is rescaled only when the row max has grown by more than 2^8 since it
-//     was last applied -- exact either way, because O and l always refer to
-//     the same max;
+//     the first half of S_j's columns) read straight from TMEM once softmax
+//     has written it (Step 7).  tcgen05.mma blocks its issuing thread while
+//     the tensor core's queue is full, so two issuers let one of them wait on
+//     a barrier while the other keeps the queue fed;
+//   * eight softmax warps share every row: warpgroup h takes the h-th half of
+//     the key columns.  Each thread reads its scores from TMEM, masks, takes
+//     the row max (the two halves of a row exchange theirs through shared
+//     memory), exponentiates with ex2 and keeps its share of the running sum
+//     (Step 5).  O is rescaled only when the row max has grown by more than
+//     2^8 since it was last applied -- exact either way, because O and l
+//     always refer to the same max;
 //   * at the end of a tile the softmax warps add the two halves of l, write
 //     LSE = m*scale + ln(l) and hand l to a fourth warpgroup, then go straight
 //     on to the next tile.  That epilogue warpgroup (one thread per row) waits
 //     for the last P_j V_j, reads O out of TMEM, releases it for the next
 //     tile's first product, divides by l, rounds to bf16 and stores the tile
 //     with TMA through a 128B-swizzled staging panel (Step 8).  Tile
-//     boundaries therefore cost the softmax warps almost nothing.
+//     boundaries therefore cost the softmax warps almost nothing;
 //   * the first tile's Q, K and V loads are issued by the thread that sets up
 //     the barriers, before the CTA-wide barrier and the TMEM allocation.
 #include <cuda.h>
