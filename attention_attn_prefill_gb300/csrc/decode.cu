@@ -22,9 +22,11 @@
 // bf16 output + LSE (one split) or its partial.
 //
 // Combine kernel: one warp per (sequence, query head) merges the partials.  It is
-// launched as a programmatic dependent of the split kernel: its CTAs may start
-// while the split kernel's last wave runs and wait (griddepcontrol.wait) until
-// every partial is written and visible, which hides the second launch.
+// launched as a programmatic dependent of the split kernel, which signals at the
+// end of each CTA: the combine's CTAs are scheduled once every split CTA has
+// written its share (earlier, they would take the registers the split kernel's
+// later waves need) and wait (griddepcontrol.wait) until all of it is visible,
+// which hides the second launch.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -120,8 +122,6 @@ __global__ void __launch_bounds__(NW * 32)
   const int g = blockIdx.y;
   const int n = blockIdx.z;
   const int G = p.G;
-  // let a dependent combine launch start early; it waits for this grid to finish before reading
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int seq_len = p.seq_lens[n];
   if (seq_len < 0 || seq_len > p.max_blocks * PAGE) {
     // a length the block table cannot cover: record it and stay inside the table
@@ -373,6 +373,8 @@ __global__ void __launch_bounds__(NW * 32)
       }
     }
   }
+  // the dependent combine may be scheduled once every CTA has written its share
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // One warp per (sequence, query head): O = sum_i w_i o_i / sum_i w_i, w_i = l_i exp(m_i - M).
