@@ -140,6 +140,8 @@ attn_status_t prefill_common(const void* q, const void* k, const void* v, void* 
   if (p.num_qblocks > 65535) return ATTN_ERR_INVALID_ARG;
   // the kernel's tile walk indexes (query tile, sequence, head) in 32 bits
   if (static_cast<int64_t>(p.num_qblocks) * p.B * p.Hq > (int64_t(1) << 30)) return ATTN_ERR_INVALID_ARG;
+  p.div_heads = attn::FastDiv::make(static_cast<uint32_t>(p.Hq));
+  p.div_level = attn::FastDiv::make(static_cast<uint32_t>(p.B * p.Hq));
   return from_cuda(attn::prefill_launch(d, maps, p, static_cast<cudaStream_t>(stream)));
 }
 

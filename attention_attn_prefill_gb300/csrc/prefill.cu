@@ -13,16 +13,19 @@
 //     Sequences are a batch of equal length, packed (cu_seqlens), or new
 //     tokens whose keys come from a paged KV cache (block table);
 //   * two producer warps stream Q (once per tile, Step 3) and the K and V
-//     tiles (128 keys; 64 at d = 256) through shared-memory rings (two K
-//     stages, three V stages; two at d = 256) with mbarrier full/empty pairs
-//     (Step 6).  With a paged cache each lane issues one 16-token page copy;
-//   * one thread issues S_j = Q K_j^T into TMEM (Step 4).  S is triple-buffered
+//     tiles (128 keys; 64 at d = 256) through shared-memory rings with
+//     mbarrier full/empty pairs (Step 6).  Q is double-buffered (single at
+//     d = 256), so the next tile's Q arrives while this tile still runs; two K
+//     stages, two V stages (three at d = 64).  With a paged cache each lane
+//     issues one 16-token page copy;
+//   * one warp issues S_j = Q K_j^T into TMEM (Step 4).  S is triple-buffered
 //     in TMEM, so the tensor core computes S two steps ahead of softmax.  A
-//     second thread, in another warp, issues O += P_j V_j with P (bf16, over
-//     the first half of S_j's columns) read straight from TMEM once softmax
-//     has written it (Step 7).  tcgen05.mma blocks its issuing thread while
-//     the tensor core's queue is full, so two issuers let one of them wait on
-//     a barrier while the other keeps the queue fed;
+//     second warp issues O += P_j V_j with P (bf16, over the first half of
+//     S_j's columns) read straight from TMEM once softmax has written it
+//     (Step 7).  Each issuing warp runs its loop converged and one elected
+//     lane issues: with warp-uniform operands a tcgen05.mma issues in about
+//     the 64 cycles a 128x128x16 product takes, and two issuers let one wait
+//     on a barrier while the other keeps the tensor core fed;
 //   * eight softmax warps share every row: warpgroup h takes the h-th half of
 //     the key columns.  Each thread reads its scores from TMEM, masks, takes
 //     the row max (the two halves of a row exchange theirs through shared
@@ -30,13 +33,14 @@
 //     (Step 5).  O is rescaled only when the row max has grown by more than
 //     2^8 since it was last applied -- exact either way, because O and l
 //     always refer to the same max;
-//   * at the end of a tile the softmax warps add the two halves of l, write
-//     LSE = m*scale + ln(l) and hand l to a fourth warpgroup, then go straight
-//     on to the next tile.  That epilogue warpgroup (one thread per row) waits
-//     for the last P_j V_j, reads O out of TMEM, releases it for the next
-//     tile's first product, divides by l, rounds to bf16 and stores the tile
-//     with TMA through a 128B-swizzled staging panel (Step 8).  Tile
-//     boundaries therefore cost the softmax warps almost nothing;
+//   * at the end of a tile the softmax warps hand their halves of l and the
+//     row max to a fourth warpgroup and go straight on to the next tile.
+//     That epilogue warpgroup (one thread per row) adds the halves, writes
+//     LSE = m*scale + ln(l), waits for the last P_j V_j, reads O out of TMEM,
+//     releases it for the next tile's first product, divides by l, rounds to
+//     bf16 and stores the tile with TMA through a 128B-swizzled staging panel
+//     (Step 8).  Tile boundaries therefore cost the softmax warps almost
+//     nothing;
 //   * the first tile's Q, K and V loads are issued by the thread that sets up
 //     the barriers, before the CTA-wide barrier and the TMEM allocation.
 #include <cuda.h>
@@ -46,6 +50,7 @@
 #include <cstdint>
 
 #include "prefill.h"
+#include "prefill_walk.cuh"
 #include "sm103.cuh"
 
 namespace attn {
@@ -54,7 +59,7 @@ __device__ uint32_t g_prefill_status;
 
 namespace {
 
-constexpr int BM = 128;          // query rows per work tile (TMEM lanes)
+using pf::BM;                    // query rows per work tile (TMEM lanes)
 constexpr int NSB = 3;           // S buffers in TMEM
 constexpr int NUM_THREADS = 512; // 8 softmax warps, 2 TMA warps, 2 MMA warps, 4 epilogue warps
 constexpr int PRODUCER_WARP = 8; // loads Q and streams K
@@ -64,16 +69,18 @@ constexpr int PV_WARP = 10;      // issues O += P V
 constexpr int EPI_WARP0 = 12;    // warps 12..15: epilogue, one thread per row
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2_THRESHOLD = 8.0f;
-constexpr int PANEL_ROW = 128;   // bytes of one 128B-swizzle panel row: 64 bf16
+using pf::PANEL_ROW;             // bytes of one 128B-swizzle panel row: 64 bf16
 
-// Tiling and shared-memory layout per head dim.  d <= 128: 128-key K/V tiles, two K and three V
-// stages.  d = 256: 64-key tiles and two stages of each, so that Q and the rings fit in shared
-// memory and O (256 columns) plus three S buffers fit in the 512 TMEM columns.
+// Tiling and shared-memory layout per head dim.  d <= 128: 128-key K/V tiles, two Q buffers (the
+// next tile's Q loads while this one runs), two K stages and two V stages (three at d = 64).
+// d = 256: 64-key tiles, one Q buffer and two stages of each, so that Q and the rings fit in
+// shared memory and O (256 columns) plus three S buffers fit in the 512 TMEM columns.
 template <int D>
 struct Layout {
   static constexpr int BN = D <= 128 ? 128 : 64;        // keys per K/V tile
+  static constexpr int Q_STAGES = D <= 128 ? 2 : 1;     // Q buffers
   static constexpr int K_STAGES = 2;                    // K_j is free as soon as S_j is done
-  static constexpr int V_STAGES = D <= 128 ? 3 : 2;     // V_j is held until P_j V_j is done
+  static constexpr int V_STAGES = D <= 64 ? 3 : 2;      // V_j is held until P_j V_j is done
   static constexpr int CHUNKS = D / 64;                 // 64-column panels per row
   static constexpr int Q_PANEL = BM * PANEL_ROW;        // one panel of a Q (or output) tile
   static constexpr int KV_PANEL = BN * PANEL_ROW;       // one panel of a K or V tile
@@ -83,16 +90,16 @@ struct Layout {
   static constexpr uint32_t O_COL = NSB * BN;           // O accumulator columns start here
   static constexpr int OGRP = D < 128 ? D : 128;        // O columns the epilogue holds at once
   static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + Q_BYTES;
+  static constexpr int K_OFF = Q_OFF + Q_STAGES * Q_BYTES;
   static constexpr int V_OFF = K_OFF + K_STAGES * KV_BYTES;
   static constexpr int OST_OFF = V_OFF + V_STAGES * KV_BYTES;   // output staging: one 64-column panel
   static constexpr int RED_OFF = OST_OFF + Q_PANEL;             // row-max exchange [2 buffers][2 halves][128]
-  static constexpr int XL_OFF = RED_OFF + 2 * 2 * 128 * 4;      // row-sum exchange [2 halves][128]
-  static constexpr int LROW_OFF = XL_OFF + 2 * 128 * 4;         // l handed to the epilogue [2 tiles][128]
-  static constexpr int BAR_OFF = LROW_OFF + 2 * 128 * 4;
-  // q_full, q_empty, k_full[K], k_empty[K], v_full[V], v_empty[V], s_full[3], p_full[3], pv_done[3],
-  // o_full, o_free, mma_done[2], l_full[2], l_empty[2]
-  static constexpr int NUM_BARS = 2 + 2 * K_STAGES + 2 * V_STAGES + 3 * NSB + 4 + 4;
+  // a tile's row sums (one per key half) and row max, handed to the epilogue: [2 tiles][3][128]
+  static constexpr int XL_OFF = RED_OFF + 2 * 2 * 128 * 4;
+  static constexpr int BAR_OFF = XL_OFF + 2 * 3 * 128 * 4;
+  // q_full[Q], q_empty[Q], k_full[K], k_empty[K], v_full[V], v_empty[V], s_full[3], p_full[3],
+  // pv_done[3], o_full, o_free, mma_done[2], l_full[2], l_empty[2]
+  static constexpr int NUM_BARS = 2 * Q_STAGES + 2 * K_STAGES + 2 * V_STAGES + 3 * NSB + 4 + 4;
   static constexpr int SLOT_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int USED = SLOT_OFF + 16;
   // The dynamic shared memory window starts 1 KB-aligned (checked at run time); never below
@@ -104,55 +111,12 @@ struct Layout {
   static_assert((BN / 16) * CHUNKS <= 32, "one paged K/V copy per producer lane");
 };
 
-// One work tile: 128 query rows of one (sequence, query head).
-struct WorkTile {
-  int b, hq, qt;  // sequence, query head, query tile within the sequence
-  int base, z;    // row and batch coordinates of the sequence's first query token in the maps
-  int len;        // query tokens of the sequence
-  int kv_len;     // keys of the sequence (len, or its cached tokens with paged K/V)
-  int q_off;      // position of its first query among the keys (kv_len - len with paged K/V, else 0)
-};
+using pf::WorkTile;
 
-// Walks this CTA's work tiles.  Tiles (query tile, sequence, head) are ordered longest first (the
-// causal cost of a tile grows with its query tile) and dealt out in a zigzag over the CTAs.  A
-// packed sequence shorter than the longest one has no tiles at the top query-tile levels: every role
-// skips those alike, so all roles see the same list.
-struct TileWalk {
-  int v = 0;
-  // 32-bit index arithmetic: the host keeps tiles x 2 below 2^31
+// The walk over this kernel's work tiles (one query head each); errors go to this kernel's status.
+struct TileWalk : pf::TileWalk {
   __device__ __forceinline__ bool next(const PrefillParams& p, WorkTile& t) {
-    const int G = gridDim.x, c = blockIdx.x;
-    const int per_qt = p.B * p.Hq;
-    const int total = per_qt * p.num_qblocks;
-    while (true) {
-      const int idx = v * G + ((v & 1) ? (G - 1 - c) : c);
-      ++v;
-      if (idx >= total) return false;
-      t.qt = p.num_qblocks - 1 - idx / per_qt;
-      const int rem = idx - (idx / per_qt) * per_qt;
-      t.hq = rem % p.Hq;
-      t.b = rem / p.Hq;
-      if (p.cu_seqlens == nullptr) {
-        t.base = 0;
-        t.z = t.b;
-        t.len = t.kv_len = p.S;
-        t.q_off = 0;
-        return true;
-      }
-      const int s0 = p.cu_seqlens[t.b], s1 = p.cu_seqlens[t.b + 1];
-      const int kvl = p.kv_lens != nullptr ? p.kv_lens[t.b] : s1 - s0;
-      if (s0 < 0 || s1 < s0 || s1 > p.S || s1 - s0 > p.num_qblocks * BM || kvl < s1 - s0 ||
-          (p.kv_lens != nullptr && kvl > p.max_blocks * 16)) {
-        set_error(&g_prefill_status, kDevBadSeqlens);
-        continue;  // the sequence is skipped
-      }
-      t.base = s0;
-      t.z = 0;
-      t.len = s1 - s0;
-      t.kv_len = kvl;
-      t.q_off = kvl - t.len;
-      if (t.qt * BM < t.len) return true;
-    }
+    return pf::TileWalk::next(p, t, &g_prefill_status);
   }
 };
 
@@ -173,13 +137,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* sO = smem + L::OST_OFF;
   float* red = reinterpret_cast<float*>(smem + L::RED_OFF);
   float* xl = reinterpret_cast<float*>(smem + L::XL_OFF);
-  float* lrow = reinterpret_cast<float*>(smem + L::LROW_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
-  constexpr int BN = L::BN, K_STAGES = L::K_STAGES, V_STAGES = L::V_STAGES, HALF = L::HALF;
+  constexpr int BN = L::BN, Q_STAGES = L::Q_STAGES, K_STAGES = L::K_STAGES, V_STAGES = L::V_STAGES;
+  constexpr int HALF = L::HALF;
   constexpr uint32_t O_COL = L::O_COL;
-  uint64_t* q_full = bars;
-  uint64_t* q_empty = q_full + 1;
-  uint64_t* k_full = q_empty + 1;
+  uint64_t* q_full = bars;                 // [Q_STAGES]
+  uint64_t* q_empty = q_full + Q_STAGES;   // [Q_STAGES]: every S product of the buffer's tile is done
+  uint64_t* k_full = q_empty + Q_STAGES;
   uint64_t* k_empty = k_full + K_STAGES;
   uint64_t* v_full = k_empty + K_STAGES;
   uint64_t* v_empty = v_full + V_STAGES;
@@ -189,20 +153,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* o_full = pv_done + NSB;
   uint64_t* o_free = o_full + 1;      // the epilogue has read O out of TMEM
   uint64_t* mma_done = o_free + 1;    // [2]: each issuer's last MMA done
-  uint64_t* l_full = mma_done + 2;    // [2]: a tile's row sums are in lrow
+  uint64_t* l_full = mma_done + 2;    // [2]: a tile's row sums and maxima are in xl
   uint64_t* l_empty = l_full + 2;     // [2]: the epilogue has read them
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::SLOT_OFF);
 
-  const int warp = threadIdx.x >> 5;
+  // The warp index and the TMEM base are made visibly warp-uniform (a broadcast from lane 0): the
+  // compiler then keeps them, and everything the MMA operands are built from, in uniform
+  // registers, and tcgen05.mma issues at the tensor core's rate instead of half of it.
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
   const int lane = threadIdx.x & 31;
   const int G = p.Hq / p.Hkv;
-  auto kv_tiles = [&](const WorkTile& t) { return (t.kv_len + BN - 1) / BN; };
-  auto tile_nkv = [&](const WorkTile& t) {
-    const int all = kv_tiles(t);
-    // causal: key tiles up to the position of the tile's last query
-    const int diag = (t.q_off + t.qt * BM + BM - 1) / BN + 1;
-    return p.causal && diag < all ? diag : all;
-  };
+  auto kv_tiles = [&](const WorkTile& t) { return pf::kv_tiles<BN>(t); };
+  // a wait taken by a whole warp, which passes only if every lane's does
+  auto wait = [&](uint64_t* bar, uint32_t parity) { return __all_sync(0xffffffffu, mbar_wait(bar, parity)); };
+  auto tile_nkv = [&](const WorkTile& t) { return pf::tile_nkv<BN>(p, t); };
   // Paged K/V: the physical page of each of the BN / 16 pages of key tile j (-1 past the sequence).
   // The producers read them before waiting for a free stage, so the reads overlap the wait.
   auto fetch_pages = [&](const WorkTile& t, int j, int (&pids)[BN / 16]) {
@@ -262,8 +226,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   };
 
   if (warp == PRODUCER_WARP && lane == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    for (int s = 0; s < Q_STAGES; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
     for (int s = 0; s < K_STAGES; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -282,8 +248,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(&mma_done[0], 1);
     mbar_init(&mma_done[1], 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&l_full[s], 4);
-      mbar_init(&l_empty[s], 4);
+      mbar_init(&l_full[s], 8);    // one arrival per softmax warp
+      mbar_init(&l_empty[s], 4);   // one arrival per epilogue warp
     }
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -316,7 +282,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
 
   if (warp == PRODUCER_WARP || warp == V_WARP) {
     // ------------------------------------------------------------ TMA producers
@@ -340,14 +306,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int k = 0; ok && walk.next(p, t); ++k) {
         const int g = t.hq / G;
         if (is_k) {
-          // Q of this tile replaces the previous one once all of its S = Q K^T products are done
+          // Q of tile k goes to buffer k % Q_STAGES once every S = Q K^T product of tile
+          // k - Q_STAGES is done: with two buffers it loads while the previous tile still runs
           if (k > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(q_empty, (k - 1) & 1));
-            if (!ok) break;
+            const int qs = k % Q_STAGES;
+            if (k >= Q_STAGES) {
+              ok = __all_sync(0xffffffffu, mbar_wait(&q_empty[qs], ((k / Q_STAGES) - 1) & 1));
+              if (!ok) break;
+            }
             if (lane == 0) {
-              mbar_arrive_expect_tx(q_full, L::Q_BYTES);
+              mbar_arrive_expect_tx(&q_full[qs], L::Q_BYTES);
               for (int c = 0; c < L::CHUNKS; ++c)
-                tma_load_3d(sQ + c * L::Q_PANEL, &tm_q, q_full, t.hq * D + c * 64, t.base + t.qt * BM, t.z);
+                tma_load_3d(sQ + qs * L::Q_BYTES + c * L::Q_PANEL, &tm_q, &q_full[qs], t.hq * D + c * 64,
+                            t.base + t.qt * BM, t.z);
             }
           }
           nq = k + 1;
@@ -404,28 +375,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // Drain: every copy started here must have landed before the CTA exits.  The newest
         // copy of each stage is the one whose phase is current.
         for (int i = (issued > nst ? issued - nst : 0); i < issued; ++i) mbar_wait(&full[i % nst], (i / nst) & 1);
-        if (nq > 0) mbar_wait(q_full, (nq - 1) & 1);
+        for (int i = (nq > Q_STAGES ? nq - Q_STAGES : 0); i < nq; ++i)
+          mbar_wait(&q_full[i % Q_STAGES], (i / Q_STAGES) & 1);
       }
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ S = Q K^T issue
     // S of global step gs goes to TMEM buffer gs % 3, which held P of step gs - 3: wait until
-    // that P.V is done.
-    if (lane == 0) {
+    // that P.V is done.  The whole warp runs the loop; one elected lane issues.
+    {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0);   // Q (K-major) x K (K-major)
-      const uint32_t qbase = smem_u32(sQ);
       bool ok = true;
       int gs = 0;
       TileWalk walk;
       WorkTile t;
       for (int k = 0; ok && walk.next(p, t); ++k) {
-        if (!mbar_wait(q_full, k & 1)) { ok = false; break; }
+        const int qs = k % Q_STAGES;
+        if (!wait(&q_full[qs], (k / Q_STAGES) & 1)) { ok = false; break; }
+        const uint32_t qbase = smem_u32(sQ + qs * L::Q_BYTES);
         const int nkv = tile_nkv(t);
         for (int j = 0; j < nkv; ++j, ++gs) {
           const int sb = gs % NSB;
           const int st = gs % K_STAGES;
-          if ((gs >= NSB && !mbar_wait(&pv_done[sb], ((gs - NSB) / NSB) & 1)) ||
-              !mbar_wait(&k_full[st], (gs / K_STAGES) & 1)) {
+          if ((gs >= NSB && !wait(&pv_done[sb], ((gs - NSB) / NSB) & 1)) ||
+              !wait(&k_full[st], (gs / K_STAGES) & 1)) {
             ok = false;
             break;
           }
@@ -437,21 +410,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // 16 columns of d: panel kk / 4, 32 bytes into its 128-byte rows
             const uint32_t qoff = (kk >> 2) * L::Q_PANEL + (kk & 3) * 32;
             const uint32_t koff = (kk >> 2) * L::KV_PANEL + (kk & 3) * 32;
-            umma_ss(s_tmem, smem_desc_sw128(qbase + qoff, 16, 1024), smem_desc_sw128(kbase + koff, 16, 1024),
-                    IDESC_S, kk > 0 ? 1u : 0u);
+            umma_ss_warp(s_tmem, smem_desc_sw128(qbase + qoff, 16, 1024), smem_desc_sw128(kbase + koff, 16, 1024),
+                         IDESC_S, kk > 0 ? 1u : 0u);
           }
-          umma_commit(&s_full[sb]);
-          umma_commit(&k_empty[st]);
+          umma_commit_warp(&s_full[sb]);
+          umma_commit_warp(&k_empty[st]);
         }
-        umma_commit(q_empty);  // Q may be replaced once this tile's products are done
+        umma_commit_warp(&q_empty[qs]);  // the buffer may take another Q once these products are done
       }
       if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
-      umma_commit(&mma_done[0]);
-      if (!mbar_wait(&mma_done[0], 0)) set_error(&g_prefill_status, kDevWaitTimeout);
+      umma_commit_warp(&mma_done[0]);
+      if (!wait(&mma_done[0], 0)) set_error(&g_prefill_status, kDevWaitTimeout);
     }
   } else if (warp == PV_WARP) {
     // ------------------------------------------------------------ O += P V issue
-    if (lane == 0) {
+    // The whole warp runs the loop; one elected lane issues.
+    {
       constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 1);    // P (TMEM) x V (MN-major)
       const uint32_t o_tmem = tmem + O_COL;
       bool ok = true;
@@ -460,12 +434,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       WorkTile t;
       for (int k = 0; ok && walk.next(p, t); ++k) {
         // the first product of a tile overwrites O: the previous tile's epilogue must have read it
-        if (k > 0 && !mbar_wait(o_free, (k - 1) & 1)) { ok = false; break; }
+        if (k > 0 && !wait(o_free, (k - 1) & 1)) { ok = false; break; }
         const int nkv = tile_nkv(t);
         for (int j = 0; j < nkv; ++j, ++gs) {
           const int sb = gs % NSB;
           const int st = gs % V_STAGES;
-          if (!mbar_wait(&p_full[sb], (gs / NSB) & 1) || !mbar_wait(&v_full[st], (gs / V_STAGES) & 1)) {
+          if (!wait(&p_full[sb], (gs / NSB) & 1) || !wait(&v_full[st], (gs / V_STAGES) & 1)) {
             ok = false;
             break;
           }
@@ -475,17 +449,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
             // 16 keys = two 8-row swizzle atoms; d panels are BN*128 bytes apart
-            umma_ts(o_tmem, p_tmem + kk * 8, smem_desc_sw128(vbase + kk * 16 * 128, BN * 128, 1024), IDESC_O,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+            umma_ts_warp(o_tmem, p_tmem + kk * 8, smem_desc_sw128(vbase + kk * 16 * 128, BN * 128, 1024), IDESC_O,
+                         (j > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&pv_done[sb]);
-          umma_commit(&v_empty[st]);
-          if (j == nkv - 1) umma_commit(o_full);
+          umma_commit_warp(&pv_done[sb]);
+          umma_commit_warp(&v_empty[st]);
+          if (j == nkv - 1) umma_commit_warp(o_full);
         }
       }
       if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
-      umma_commit(&mma_done[1]);
-      if (!mbar_wait(&mma_done[1], 0)) set_error(&g_prefill_status, kDevWaitTimeout);
+      umma_commit_warp(&mma_done[1]);
+      if (!wait(&mma_done[1], 0)) set_error(&g_prefill_status, kDevWaitTimeout);
     }
   } else if (warp < PRODUCER_WARP) {
     // ------------------------------------------------------------ softmax
@@ -598,20 +572,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[sb]);  // one arrival per warp: 256 would queue on the barrier
       }
-      // ---- end of tile: add the halves of l, write LSE, hand l to the epilogue warps.  xl is
-      // next written at the end of the next tile, after at least one more max exchange.
-      xl[h * 128 + row] = l_part;
-      named_barrier_sync(1, 256);
-      if (h == 0) {
-        const float l = xl[row] + xl[128 + row];
-        if (p.lse != nullptr && q < t.len)
-          p.lse[(static_cast<size_t>(t.z) * p.Hq + t.hq) * p.S + t.base + q] = m_used * p.scale + logf(l);
-        const int tb = k & 1;
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&l_empty[tb], ((k >> 1) & 1) ^ 1));
-        lrow[tb * 128 + row] = l;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&l_full[tb]);
-      }
+      // ---- end of tile: hand this half's share of l (and the row max) to the epilogue warps,
+      // which add the halves, write LSE and divide O by l; the softmax warps go straight on.
+      const int tb = k & 1;
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&l_empty[tb], ((k >> 1) & 1) ^ 1));
+      float* xt = xl + tb * 3 * 128;
+      xt[h * 128 + row] = l_part;
+      if (h == 0) xt[2 * 128 + row] = m_used;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&l_full[tb]);
     }
     if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
   } else {
@@ -629,9 +598,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int k = 0; walk.next(p, t); ++k) {
       const int tb = k & 1;
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&l_full[tb], (k >> 1) & 1));
-      const float inv_l = 1.f / lrow[tb * 128 + row];
+      const float* xt = xl + tb * 3 * 128;
+      const float l = xt[row] + xt[128 + row];
+      const float m_row = xt[2 * 128 + row];
       __syncwarp();
       if (lane == 0) mbar_arrive(&l_empty[tb]);
+      const float inv_l = 1.f / l;
+      if (p.lse != nullptr && t.qt * BM + row < t.len)
+        p.lse[(static_cast<size_t>(t.z) * p.Hq + t.hq) * p.S + t.base + t.qt * BM + row] = m_row * p.scale + logf(l);
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_full, k & 1));
       tc_fence_after();
       const bool rowwise = p.cu_seqlens != nullptr && t.qt * BM + BM > t.len;

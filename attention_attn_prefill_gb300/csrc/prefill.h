@@ -22,6 +22,25 @@ struct PrefillMaps {
 //   * paged K/V (kv_lens != null, packed queries): sequence n's keys are its kv_lens[n] cached tokens,
 //     read through block_table (16-token pages; maps {d, Hkv, num_blocks*16}); its packed queries are
 //     the last cu_seqlens[n+1] - cu_seqlens[n] of them.
+// x / d for 0 <= x < 2^31 by a multiply-high, an add and a shift: the round-up method of
+// Granlund and Montgomery, "Division by Invariant Integers using Multiplication" (1994), section 4,
+// with s = ceil(log2 d) and m = floor(2^32 (2^s - d) / d) + 1 < 2^32.
+struct FastDiv {
+  uint32_t m = 1, s = 0;
+  static FastDiv make(uint32_t d) {  // d >= 1
+    FastDiv f;
+    if (d == 0) d = 1;
+    while ((1ull << f.s) < d) ++f.s;
+    f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << f.s) - d)) / d + 1);
+    return f;
+  }
+#ifdef __CUDACC__
+  __device__ __forceinline__ uint32_t div(uint32_t x) const {
+    return static_cast<uint32_t>((static_cast<uint64_t>(__umulhi(x, m)) + x) >> s);
+  }
+#endif
+};
+
 struct PrefillParams {
   float* lse;                  // LSE (see above) or null
   void* o;                     // output base (bf16), for the rows of a partial packed tile
@@ -34,6 +53,8 @@ struct PrefillParams {
   float scale_log2;  // scale * log2(e)
   int causal;
   int num_qblocks;   // query tiles of the longest sequence: ceil(S or max_seqlen / 128)
+  FastDiv div_heads;  // by Hq
+  FastDiv div_level;  // by B * Hq: work tiles per query-tile level
 };
 
 int prefill_rows_per_cta();

@@ -1,0 +1,86 @@
+// Work tiles of the prefill kernels and the order in which a persistent CTA walks them.
+//
+// A work tile is one 128-row query tile of one (sequence, query head).  Tiles are ordered
+// longest first -- the causal cost of a tile grows with its query tile -- and dealt out in a zigzag
+// over the CTAs, so that every CTA gets about the same number of key steps.  Every role of a CTA
+// walks the list with its own walker and sees the same tiles, so no tile list passes between roles.
+#pragma once
+
+#include <cstdint>
+
+#include "prefill.h"
+#include "sm103.cuh"
+
+namespace attn {
+namespace pf {
+
+constexpr int BM = 128;         // query rows per work tile (TMEM lanes)
+constexpr int PANEL_ROW = 128;  // bytes of one 128B-swizzle panel row: 64 bf16
+
+struct WorkTile {
+  int b, hq, qt;  // sequence, query head (or head group), query tile within the sequence
+  int base, z;    // row and batch coordinates of the sequence's first query token in the maps
+  int len;        // query tokens of the sequence
+  int kv_len;     // keys of the sequence (len, or its cached tokens with paged K/V)
+  int q_off;      // position of its first query among the keys (kv_len - len with paged K/V, else 0)
+};
+
+// Key tiles of BN keys that a work tile's queries see: all of the sequence's keys, or (causal) those
+// up to the position of the tile's last query.
+template <int BN>
+__device__ __forceinline__ int kv_tiles(const WorkTile& t) {
+  return (t.kv_len + BN - 1) / BN;
+}
+
+template <int BN>
+__device__ __forceinline__ int tile_nkv(const PrefillParams& p, const WorkTile& t) {
+  const int all = kv_tiles<BN>(t);
+  const int diag = (t.q_off + t.qt * BM + BM - 1) / BN + 1;
+  return p.causal && diag < all ? diag : all;
+}
+
+// A packed sequence shorter than the longest one has no tiles at the top query-tile levels: every
+// role skips those alike.  The divisions go through the multipliers in the parameters, which costs
+// the roles a few cycles per tile instead of hundreds.
+struct TileWalk {
+  int v = 0;
+  // 32-bit index arithmetic: the host keeps tiles x 2 below 2^31
+  __device__ __forceinline__ bool next(const PrefillParams& p, WorkTile& t, uint32_t* status) {
+    const int G = gridDim.x, c = blockIdx.x;
+    const int per_qt = p.B * p.Hq;
+    const int total = per_qt * p.num_qblocks;
+    while (true) {
+      const int idx = v * G + ((v & 1) ? (G - 1 - c) : c);
+      ++v;
+      if (idx >= total) return false;
+      const int level = static_cast<int>(p.div_level.div(static_cast<uint32_t>(idx)));
+      t.qt = p.num_qblocks - 1 - level;
+      const int rem = idx - level * per_qt;
+      t.b = static_cast<int>(p.div_heads.div(static_cast<uint32_t>(rem)));
+      t.hq = rem - t.b * p.Hq;
+      if (p.cu_seqlens == nullptr) {
+        t.base = 0;
+        t.z = t.b;
+        t.len = t.kv_len = p.S;
+        t.q_off = 0;
+        return true;
+      }
+      const int s0 = p.cu_seqlens[t.b], s1 = p.cu_seqlens[t.b + 1];
+      const int kvl = p.kv_lens != nullptr ? p.kv_lens[t.b] : s1 - s0;
+      if (s0 < 0 || s1 < s0 || s1 > p.S || s1 - s0 > p.num_qblocks * BM || kvl < s1 - s0 ||
+          (p.kv_lens != nullptr && kvl > p.max_blocks * 16)) {
+        set_error(status, kDevBadSeqlens);
+        continue;  // the sequence is skipped
+      }
+      t.base = s0;
+      t.z = 0;
+      t.len = s1 - s0;
+      t.kv_len = kvl;
+      t.q_off = kvl - t.len;
+      if (t.qt * BM < t.len) return true;
+    }
+  }
+};
+
+}  // namespace pf
+}  // namespace attn
