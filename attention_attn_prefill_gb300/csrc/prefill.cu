@@ -26,21 +26,22 @@
 //     lane issues: with warp-uniform operands a tcgen05.mma issues in about
 //     the 64 cycles a 128x128x16 product takes, and two issuers let one wait
 //     on a barrier while the other keeps the tensor core fed;
-//   * eight softmax warps share every row: warpgroup h takes the h-th half of
-//     the key columns.  Each thread reads its scores from TMEM, masks, takes
-//     the row max (the two halves of a row exchange theirs through shared
-//     memory), exponentiates with ex2 and keeps its share of the running sum
-//     (Step 5).  O is rescaled only when the row max has grown by more than
-//     2^8 since it was last applied -- exact either way, because O and l
-//     always refer to the same max;
-//   * at the end of a tile the softmax warps hand their halves of l and the
-//     row max to a fourth warpgroup and go straight on to the next tile.
-//     That epilogue warpgroup (one thread per row) adds the halves, writes
-//     LSE = m*scale + ln(l), waits for the last P_j V_j, reads O out of TMEM,
-//     releases it for the next tile's first product, divides by l, rounds to
-//     bf16 and stores the tile with TMA through a 128B-swizzled staging panel
-//     (Step 8).  Tile boundaries therefore cost the softmax warps almost
-//     nothing;
+//   * eight softmax warps, each with 16 whole rows of the tile (four threads
+//     per row through the 16x256b TMEM access shape).  Each thread reads its
+//     scores from TMEM, masks, takes the row max (two shuffles within the
+//     row's four threads), exponentiates with ex2 and keeps its share of the
+//     running sum (Step 5).  No warp waits for another, so the two softmax
+//     warps that share a scheduler interleave their phases.  O is rescaled
+//     only when the row max has grown by more than 2^8 since it was last
+//     applied -- exact either way, because O and l always refer to the same
+//     max;
+//   * at the end of a tile the softmax warps hand l and the row max to a
+//     fourth warpgroup and go straight on to the next tile.  That epilogue
+//     warpgroup (one thread per row) writes LSE = m*scale + ln(l), waits for
+//     the last P_j V_j, reads O out of TMEM, releases it for the next tile's
+//     first product, divides by l, rounds to bf16 and stores the tile with
+//     TMA through a 128B-swizzled staging panel (Step 8).  Tile boundaries
+//     therefore cost the softmax warps almost nothing;
 //   * the first tile's Q, K and V loads are issued by the thread that sets up
 //     the barriers, before the CTA-wide barrier and the TMEM allocation.
 #include <cuda.h>
@@ -86,17 +87,15 @@ struct Layout {
   static constexpr int KV_PANEL = BN * PANEL_ROW;       // one panel of a K or V tile
   static constexpr int Q_BYTES = CHUNKS * Q_PANEL;
   static constexpr int KV_BYTES = CHUNKS * KV_PANEL;
-  static constexpr int HALF = BN / 2;                   // keys per softmax thread and step
   static constexpr uint32_t O_COL = NSB * BN;           // O accumulator columns start here
   static constexpr int OGRP = D < 128 ? D : 128;        // O columns the epilogue holds at once
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + Q_STAGES * Q_BYTES;
   static constexpr int V_OFF = K_OFF + K_STAGES * KV_BYTES;
   static constexpr int OST_OFF = V_OFF + V_STAGES * KV_BYTES;   // output staging: one 64-column panel
-  static constexpr int RED_OFF = OST_OFF + Q_PANEL;             // row-max exchange [2 buffers][2 halves][128]
-  // a tile's row sums (one per key half) and row max, handed to the epilogue: [2 tiles][3][128]
-  static constexpr int XL_OFF = RED_OFF + 2 * 2 * 128 * 4;
-  static constexpr int BAR_OFF = XL_OFF + 2 * 3 * 128 * 4;
+  // a tile's row sums and row maxima, handed to the epilogue: [2 tiles][2][128]
+  static constexpr int XL_OFF = OST_OFF + Q_PANEL;
+  static constexpr int BAR_OFF = XL_OFF + 2 * 2 * 128 * 4;
   // q_full[Q], q_empty[Q], k_full[K], k_empty[K], v_full[V], v_empty[V], s_full[3], p_full[3],
   // pv_done[3], o_full, o_free, mma_done[2], l_full[2], l_empty[2]
   static constexpr int NUM_BARS = 2 * Q_STAGES + 2 * K_STAGES + 2 * V_STAGES + 3 * NSB + 4 + 4;
@@ -107,7 +106,7 @@ struct Layout {
   static constexpr int ALLOC = USED > 116 * 1024 ? USED : 116 * 1024;
   static_assert(ALLOC <= 232448, "shared memory budget");
   static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
-  static_assert(HALF == 64 || HALF == 32, "softmax handles 32 or 64 keys per thread");
+  static_assert(BN == 64 || BN == 128, "the softmax takes 8 or 16 groups of 8 columns");
   static_assert((BN / 16) * CHUNKS <= 32, "one paged K/V copy per producer lane");
 };
 
@@ -135,11 +134,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* sK = smem + L::K_OFF;
   uint8_t* sV = smem + L::V_OFF;
   uint8_t* sO = smem + L::OST_OFF;
-  float* red = reinterpret_cast<float*>(smem + L::RED_OFF);
   float* xl = reinterpret_cast<float*>(smem + L::XL_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   constexpr int BN = L::BN, Q_STAGES = L::Q_STAGES, K_STAGES = L::K_STAGES, V_STAGES = L::V_STAGES;
-  constexpr int HALF = L::HALF;
   constexpr uint32_t O_COL = L::O_COL;
   uint64_t* q_full = bars;                 // [Q_STAGES]
   uint64_t* q_empty = q_full + Q_STAGES;   // [Q_STAGES]: every S product of the buffer's tile is done
@@ -163,7 +160,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
   const int lane = threadIdx.x & 31;
   const int G = p.Hq / p.Hkv;
-  auto kv_tiles = [&](const WorkTile& t) { return pf::kv_tiles<BN>(t); };
   // a wait taken by a whole warp, which passes only if every lane's does
   auto wait = [&](uint64_t* bar, uint32_t parity) { return __all_sync(0xffffffffu, mbar_wait(bar, parity)); };
   auto tile_nkv = [&](const WorkTile& t) { return pf::tile_nkv<BN>(p, t); };
@@ -463,12 +459,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp < PRODUCER_WARP) {
     // ------------------------------------------------------------ softmax
-    // A wait that runs out of time clears `ok`; the warp then skips its remaining waits but
-    // keeps the named-barrier schedule, so no other warp is left at a barrier.
-    const int h = warp >> 2;                  // which half of the key columns
-    const int row = (warp & 3) * 32 + lane;   // TMEM lane = query row within the tile
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t o_half = tmem + lane_base + O_COL + h * (D / 2);
+    // Warp w takes 16 whole rows: TMEM lanes r0 .. r0 + 15 with r0 = 32 (w % 4) + 16 (w / 4).
+    // Through the 16x256b TMEM shape four threads share a row: thread t holds rows r0 + t/4 ("a")
+    // and r0 + t/4 + 8 ("b"), columns 8i + 2(t % 4) and 8i + 2(t % 4) + 1 of each group i of 8
+    // columns.  A row max is then two shuffles, and no warp waits for another.  A wait that runs
+    // out of time clears `ok`; the warp then skips its remaining waits.
+    constexpr int NG = BN / 8;  // 8-column groups per S tile
+    const int r0 = (warp & 3) * 32 + (warp >> 2) * 16;
+    const int ra = r0 + (lane >> 2);  // row a; row b is ra + 8
+    const int cq = 2 * (lane & 3);    // this thread's first column in each group
+    const uint32_t lane_base = static_cast<uint32_t>(r0) << 16;
     const float c2 = p.scale_log2;
     const uint64_t c2x2 = f2_pack(c2, c2);
     bool ok = true;
@@ -476,95 +476,111 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     TileWalk walk;
     WorkTile t;
     for (int k = 0; walk.next(p, t); ++k) {
-      const int q = t.qt * BM + row;  // query row within the sequence
-      const int qpos = t.q_off + q;   // its position among the keys
+      const int qa = t.q_off + t.qt * BM + ra;  // positions of rows a and b among the keys
+      const int qb = qa + 8;
       const int nkv = tile_nkv(t);
-      const int nkv_all = kv_tiles(t);
-      float m_used = -INFINITY;  // raw-score max that O and l currently refer to
-      float l_part = 0.f;        // this half's share of the row sum
+      float m_a = -INFINITY, m_b = -INFINITY;  // raw-score maxima that O and l currently refer to
+      float l_a = 0.f, l_b = 0.f;              // this thread's shares of the row sums
       for (int j = 0; j < nkv; ++j, ++gs) {
         const int sb = gs % NSB;
         const uint32_t s_tmem = tmem + lane_base + sb * BN;
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (gs / NSB) & 1));
         tc_fence_after();
-        uint32_t sr[HALF / 32][32];
-#pragma unroll
-        for (int i = 0; i < HALF / 32; ++i) tmem_ld32(s_tmem + h * HALF + 32 * i, sr[i]);
+        uint32_t sr[4 * NG];
+        tmem_ld16_256b<NG>(s_tmem, sr);
         tmem_ld_wait();
-        // last visible column of this thread's keys: below HALF - 1 only where the tile crosses
+        // last visible column of each row in this tile: below BN - 1 only where the tile crosses
         // the causal diagonal or the end of the sequence
-        const int key0 = j * BN + h * HALF;
-        int lim = HALF - 1;
-        if (p.causal && qpos - key0 < lim) lim = qpos - key0;
-        if (j == nkv_all - 1 && t.kv_len - 1 - key0 < lim) lim = t.kv_len - 1 - key0;
-        if (lim < HALF - 1) {
-#pragma unroll
-          for (int c = 0; c < HALF; ++c)
-            if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+        const int key0 = j * BN;
+        int lim_a = t.kv_len - 1 - key0, lim_b = lim_a;
+        if (p.causal) {
+          lim_a = min(lim_a, qa - key0);
+          lim_b = min(lim_b, qb - key0);
         }
-        float mxs[HALF / 32];
+        if (min(lim_a, lim_b) < BN - 1) {
 #pragma unroll
-        for (int i = 0; i < HALF / 32; ++i) {
-          float m = -INFINITY;
+          for (int i = 0; i < NG; ++i)
 #pragma unroll
-          for (int c = 0; c < 16; ++c) m = fmax3(m, __uint_as_float(sr[i][2 * c]), __uint_as_float(sr[i][2 * c + 1]));
-          mxs[i] = m;
+            for (int e = 0; e < 2; ++e) {
+              const int c = 8 * i + cq + e;
+              if (c > lim_a) sr[4 * i + e] = __float_as_uint(-INFINITY);
+              if (c > lim_b) sr[4 * i + 2 + e] = __float_as_uint(-INFINITY);
+            }
         }
-        float mxh = mxs[0];
+        float mxa = -INFINITY, mxb = -INFINITY;
 #pragma unroll
-        for (int i = 1; i < HALF / 32; ++i) mxh = fmaxf(mxh, mxs[i]);
-        // exchange the half-row maxima (both halves have read S, so P may overwrite it afterwards)
-        float* xr = red + (gs & 1) * 256;
-        xr[h * 128 + row] = mxh;
-        named_barrier_sync(1, 256);
-        const float mx = fmaxf(xr[row], xr[128 + row]);
-        float alpha = 1.f;
+        for (int i = 0; i < NG; ++i) {
+          mxa = fmax3(mxa, __uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1]));
+          mxb = fmax3(mxb, __uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3]));
+        }
+        mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
+        mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
+        mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
+        mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
+        float alpha_a = 1.f, alpha_b = 1.f;
         bool rescale_o = false;
         if (j == 0) {
-          m_used = mx;
-        } else if ((mx - m_used) * c2 > RESCALE_LOG2_THRESHOLD) {
-          alpha = ex2_approx((m_used - mx) * c2);
-          l_part *= alpha;
-          rescale_o = true;
-          m_used = mx;
+          m_a = mxa;
+          m_b = mxb;
+        } else {
+          if ((mxa - m_a) * c2 > RESCALE_LOG2_THRESHOLD) {
+            alpha_a = ex2_approx((m_a - mxa) * c2);
+            l_a *= alpha_a;
+            m_a = mxa;
+            rescale_o = true;
+          }
+          if ((mxb - m_b) * c2 > RESCALE_LOG2_THRESHOLD) {
+            alpha_b = ex2_approx((m_b - mxb) * c2);
+            l_b *= alpha_b;
+            m_b = mxb;
+            rescale_o = true;
+          }
         }
-        const float mb = (m_used == -INFINITY) ? 0.f : m_used * c2;
-        const uint64_t nmb2 = f2_pack(-mb, -mb);
-        // p = 2^(s*scale*log2e - m*scale*log2e) in f32x2 pairs; P (bf16, two per column) goes to
-        // columns h*HALF/2 .. h*HALF/2 + HALF/2 - 1 of this S buffer
-        uint64_t acc0 = 0ull, acc1 = 0ull;
-        uint32_t pk[HALF / 2];
+        const float mba = (m_a == -INFINITY) ? 0.f : m_a * c2;
+        const float mbb = (m_b == -INFINITY) ? 0.f : m_b * c2;
+        const uint64_t nma = f2_pack(-mba, -mba), nmb = f2_pack(-mbb, -mbb);
+        // p = 2^(s*scale*log2e - m*scale*log2e) in f32x2 pairs.  P (bf16, two per column) goes to the
+        // first BN / 2 columns of this S buffer: the pair of columns 8i + cq, + 1 to column 4i + cq/2,
+        // which is where the 16x128b shape puts this thread's registers 2i (row a) and 2i + 1 (row b).
+        uint64_t acc_a = 0ull, acc_b = 0ull;
+        uint32_t pk[2 * NG];
 #pragma unroll
-        for (int c = 0; c < HALF / 2; ++c) {
-          const int e = 2 * c;
-          const uint64_t xy = f2_fma(
-              f2_pack(__uint_as_float(sr[e >> 5][e & 31]), __uint_as_float(sr[e >> 5][(e & 31) + 1])), c2x2, nmb2);
+        for (int i = 0; i < NG; ++i) {
           float x0, x1;
-          f2_unpack(xy, x0, x1);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          if (c & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
-          else acc0 = f2_add(acc0, f2_pack(p0, p1));
-          pk[c] = pack_bf16x2(p0, p1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1])), c2x2, nma), x0, x1);
+          const float pa0 = ex2_approx(x0), pa1 = ex2_approx(x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3])), c2x2, nmb), x0, x1);
+          const float pb0 = ex2_approx(x0), pb1 = ex2_approx(x1);
+          acc_a = f2_add(acc_a, f2_pack(pa0, pa1));
+          acc_b = f2_add(acc_b, f2_pack(pb0, pb1));
+          pk[2 * i] = pack_bf16x2(pa0, pa1);
+          pk[2 * i + 1] = pack_bf16x2(pb0, pb1);
         }
         {
-          float a0, a1;
-          f2_unpack(f2_add(acc0, acc1), a0, a1);
-          l_part += a0 + a1;
+          float a0, a1, b0, b1;
+          f2_unpack(acc_a, a0, a1);
+          f2_unpack(acc_b, b0, b1);
+          l_a += a0 + a1;
+          l_b += b0 + b1;
         }
-        tmem_st_cols(s_tmem + h * (HALF / 2), pk);
+        tmem_st16_128b<NG>(s_tmem, pk);
         if (__any_sync(0xffffffffu, rescale_o)) {
           // O must hold P V of the previous step before it is rescaled
           if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(gs - 1) % NSB], ((gs - 1) / NSB) & 1));
           tc_fence_after();
 #pragma unroll 1
-          for (int c4 = 0; c4 < D / 64; ++c4) {
+          for (int c64 = 0; c64 < D; c64 += 64) {
             uint32_t r[32];
-            tmem_ld32(o_half + c4 * 32, r);
+            tmem_ld16_256b_x8(tmem + lane_base + O_COL + c64, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-            tmem_st32(o_half + c4 * 32, r);
+            for (int i = 0; i < 8; ++i) {
+              r[4 * i] = __float_as_uint(__uint_as_float(r[4 * i]) * alpha_a);
+              r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) * alpha_a);
+              r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) * alpha_b);
+              r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) * alpha_b);
+            }
+            tmem_st16_256b_x8(tmem + lane_base + O_COL + c64, r);
           }
         }
         tmem_st_wait();
@@ -572,13 +588,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[sb]);  // one arrival per warp: 256 would queue on the barrier
       }
-      // ---- end of tile: hand this half's share of l (and the row max) to the epilogue warps,
-      // which add the halves, write LSE and divide O by l; the softmax warps go straight on.
+      // ---- end of tile: add the four threads' shares of each row sum and hand l and the row max
+      // to the epilogue warps, which write LSE and divide O by l; the softmax warps go straight on.
+      l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+      l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+      l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+      l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
       const int tb = k & 1;
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&l_empty[tb], ((k >> 1) & 1) ^ 1));
-      float* xt = xl + tb * 3 * 128;
-      xt[h * 128 + row] = l_part;
-      if (h == 0) xt[2 * 128 + row] = m_used;
+      float* xt = xl + tb * 2 * 128;
+      if ((lane & 3) == 0) {
+        xt[ra] = l_a;
+        xt[ra + 8] = l_b;
+        xt[128 + ra] = m_a;
+        xt[128 + ra + 8] = m_b;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&l_full[tb]);
     }
@@ -598,9 +622,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int k = 0; walk.next(p, t); ++k) {
       const int tb = k & 1;
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&l_full[tb], (k >> 1) & 1));
-      const float* xt = xl + tb * 3 * 128;
-      const float l = xt[row] + xt[128 + row];
-      const float m_row = xt[2 * 128 + row];
+      const float* xt = xl + tb * 2 * 128;
+      const float l = xt[row];
+      const float m_row = xt[128 + row];
       __syncwarp();
       if (lane == 0) mbar_arrive(&l_empty[tb]);
       const float inv_l = 1.f / l;
