@@ -70,6 +70,9 @@ constexpr int PV_WARP = 10;      // issues O += P V
 constexpr int EPI_WARP0 = 12;    // warps 12..15: epilogue, one thread per row
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2_THRESHOLD = 8.0f;
+constexpr uint32_t REG_SOFTMAX = 168, REG_OTHER = 64, REG_EPI = 112;  // registers per thread, see below
+static_assert(8 * 32 * REG_SOFTMAX + 4 * 32 * REG_OTHER + 4 * 32 * REG_EPI == 128 * NUM_THREADS, "register split");
+constexpr float P_PARTIAL_LIMIT = 4294967296.0f;  // 2^32: bound on a thread's share of a step's row sum
 using pf::PANEL_ROW;             // bytes of one 128B-swizzle panel row: 64 bf16
 
 // Tiling and shared-memory layout per head dim.  d <= 128: 128-key K/V tiles, two Q buffers (the
@@ -280,184 +283,191 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
 
-  if (warp == PRODUCER_WARP || warp == V_WARP) {
-    // ------------------------------------------------------------ TMA producers
-    // Warp 8 loads Q and the K tiles, warp 11 the V tiles; each waits only on its own ring.
-    // Counters run across work tiles, so the rings never drain between tiles.  The whole warp runs
-    // the loop: with paged K/V, lane l reads the physical page of page l of the tile and the lanes
-    // issue one 16-row copy each, so the many small copies of a tile leave in one instruction.
-    {
-      const bool is_k = warp == PRODUCER_WARP;
-      const int nst = is_k ? K_STAGES : V_STAGES;
-      uint64_t* full = is_k ? k_full : v_full;
-      uint64_t* empty = is_k ? k_empty : v_empty;
-      uint8_t* ring = is_k ? sK : sV;
-      const CUtensorMap* map = is_k ? &tm_k : &tm_v;
-      const int npre = first_loads(nst);
-      constexpr int PAGES = BN / 16;
-      bool ok = true;
-      int issued = npre, nq = 0;
-      TileWalk walk;
-      WorkTile t;
-      for (int k = 0; ok && walk.next(p, t); ++k) {
-        const int g = t.hq / G;
-        if (is_k) {
-          // Q of tile k goes to buffer k % Q_STAGES once every S = Q K^T product of tile
-          // k - Q_STAGES is done: with two buffers it loads while the previous tile still runs
-          if (k > 0) {
-            const int qs = k % Q_STAGES;
-            if (k >= Q_STAGES) {
-              ok = __all_sync(0xffffffffu, mbar_wait(&q_empty[qs], ((k / Q_STAGES) - 1) & 1));
-              if (!ok) break;
+  // Each warpgroup sets its register budget at the top of its branch, so that the compiler
+  // allocates the role's code within it: the softmax warps take 168 registers per thread, the
+  // loading and MMA warps 64, the epilogue 112 (launched with 128 x 512 = 65536).
+  if (warp >= PRODUCER_WARP && warp < EPI_WARP0) {
+    regs_dec<REG_OTHER>();
+    if (warp == PRODUCER_WARP || warp == V_WARP) {
+      // ------------------------------------------------------------ TMA producers
+      // Warp 8 loads Q and the K tiles, warp 11 the V tiles; each waits only on its own ring.
+      // Counters run across work tiles, so the rings never drain between tiles.  The whole warp runs
+      // the loop: with paged K/V, lane l reads the physical page of page l of the tile and the lanes
+      // issue one 16-row copy each, so the many small copies of a tile leave in one instruction.
+      {
+        const bool is_k = warp == PRODUCER_WARP;
+        const int nst = is_k ? K_STAGES : V_STAGES;
+        uint64_t* full = is_k ? k_full : v_full;
+        uint64_t* empty = is_k ? k_empty : v_empty;
+        uint8_t* ring = is_k ? sK : sV;
+        const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+        const int npre = first_loads(nst);
+        constexpr int PAGES = BN / 16;
+        bool ok = true;
+        int issued = npre, nq = 0;
+        TileWalk walk;
+        WorkTile t;
+        for (int k = 0; ok && walk.next(p, t); ++k) {
+          const int g = t.hq / G;
+          if (is_k) {
+            // Q of tile k goes to buffer k % Q_STAGES once every S = Q K^T product of tile
+            // k - Q_STAGES is done: with two buffers it loads while the previous tile still runs
+            if (k > 0) {
+              const int qs = k % Q_STAGES;
+              if (k >= Q_STAGES) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&q_empty[qs], ((k / Q_STAGES) - 1) & 1));
+                if (!ok) break;
+              }
+              if (lane == 0) {
+                mbar_arrive_expect_tx(&q_full[qs], L::Q_BYTES);
+                for (int c = 0; c < L::CHUNKS; ++c)
+                  tma_load_3d(sQ + qs * L::Q_BYTES + c * L::Q_PANEL, &tm_q, &q_full[qs], t.hq * D + c * 64,
+                              t.base + t.qt * BM, t.z);
+              }
             }
-            if (lane == 0) {
-              mbar_arrive_expect_tx(&q_full[qs], L::Q_BYTES);
-              for (int c = 0; c < L::CHUNKS; ++c)
-                tma_load_3d(sQ + qs * L::Q_BYTES + c * L::Q_PANEL, &tm_q, &q_full[qs], t.hq * D + c * 64,
-                            t.base + t.qt * BM, t.z);
+            nq = k + 1;
+          }
+          const int nkv = tile_nkv(t);
+          for (int j = (k == 0 ? npre : 0); j < nkv; ++j) {
+            const int st = issued % nst;
+            uint8_t* dst = ring + st * L::KV_BYTES;
+            // paged: lane l < PAGES reads the physical page of page l of this tile before the wait
+            int my_pid = -1;
+            if (p.kv_lens != nullptr && lane < PAGES) {
+              const int page = j * PAGES + lane;
+              if (page * 16 < t.kv_len) my_pid = p.block_table[static_cast<size_t>(t.b) * p.max_blocks + page];
             }
-          }
-          nq = k + 1;
-        }
-        const int nkv = tile_nkv(t);
-        for (int j = (k == 0 ? npre : 0); j < nkv; ++j) {
-          const int st = issued % nst;
-          uint8_t* dst = ring + st * L::KV_BYTES;
-          // paged: lane l < PAGES reads the physical page of page l of this tile before the wait
-          int my_pid = -1;
-          if (p.kv_lens != nullptr && lane < PAGES) {
-            const int page = j * PAGES + lane;
-            if (page * 16 < t.kv_len) my_pid = p.block_table[static_cast<size_t>(t.b) * p.max_blocks + page];
-          }
-          ok = __all_sync(0xffffffffu, mbar_wait(&empty[st], ((issued / nst) & 1) ^ 1));
-          if (!ok) break;
-          if (lane == 0) mbar_arrive_expect_tx(&full[st], L::KV_BYTES);
-          __syncwarp();
-          if (p.kv_lens == nullptr) {
-            if (lane < L::CHUNKS)
-              tma_load_3d(dst + lane * L::KV_PANEL, map, &full[st], g * D + lane * 64, t.base + j * BN, t.z);
-          } else {
-            // lane l: page l / CHUNKS, 64-column chunk l % CHUNKS.  Pages past the sequence are read
-            // from rows past the cache, which the copy fills with zeros.
-            const int pp = lane / L::CHUNKS, c = lane % L::CHUNKS;
-            int pid = __shfl_sync(0xffffffffu, my_pid, pp < PAGES ? pp : 0);
-            if (pp < PAGES) {
-              const int oob = p.num_blocks * 16;
-              const int valid = t.kv_len - (j * PAGES + pp) * 16;  // rows of this page that hold keys
-              int row0 = oob;
-              if (valid > 0) {
-                if (pid < 0 || pid >= p.num_blocks) {
-                  set_error(&g_prefill_status, kDevBadPage);
-                  pid = 0;
+            ok = __all_sync(0xffffffffu, mbar_wait(&empty[st], ((issued / nst) & 1) ^ 1));
+            if (!ok) break;
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], L::KV_BYTES);
+            __syncwarp();
+            if (p.kv_lens == nullptr) {
+              if (lane < L::CHUNKS)
+                tma_load_3d(dst + lane * L::KV_PANEL, map, &full[st], g * D + lane * 64, t.base + j * BN, t.z);
+            } else {
+              // lane l: page l / CHUNKS, 64-column chunk l % CHUNKS.  Pages past the sequence are read
+              // from rows past the cache, which the copy fills with zeros.
+              const int pp = lane / L::CHUNKS, c = lane % L::CHUNKS;
+              int pid = __shfl_sync(0xffffffffu, my_pid, pp < PAGES ? pp : 0);
+              if (pp < PAGES) {
+                const int oob = p.num_blocks * 16;
+                const int valid = t.kv_len - (j * PAGES + pp) * 16;  // rows of this page that hold keys
+                int row0 = oob;
+                if (valid > 0) {
+                  if (pid < 0 || pid >= p.num_blocks) {
+                    set_error(&g_prefill_status, kDevBadPage);
+                    pid = 0;
+                  }
+                  row0 = pid * 16;
                 }
-                row0 = pid * 16;
-              }
-              uint8_t* pd = dst + c * L::KV_PANEL + pp * 16 * PANEL_ROW;
-              if (!is_k && valid > 0 && valid < 16) {
-                // the V rows past the last key must be finite (P is 0 there, but 0 * NaN is not):
-                // row by row, the tail from past the cache
-                for (int r = 0; r < 16; ++r)
-                  tma_load_3d(pd + r * PANEL_ROW, &tm_vrow, &full[st], c * 64, g, r < valid ? row0 + r : oob);
-              } else {
-                tma_load_3d(pd, map, &full[st], c * 64, g, row0);
+                uint8_t* pd = dst + c * L::KV_PANEL + pp * 16 * PANEL_ROW;
+                if (!is_k && valid > 0 && valid < 16) {
+                  // the V rows past the last key must be finite (P is 0 there, but 0 * NaN is not):
+                  // row by row, the tail from past the cache
+                  for (int r = 0; r < 16; ++r)
+                    tma_load_3d(pd + r * PANEL_ROW, &tm_vrow, &full[st], c * 64, g, r < valid ? row0 + r : oob);
+                } else {
+                  tma_load_3d(pd, map, &full[st], c * 64, g, row0);
+                }
               }
             }
+            ++issued;
           }
-          ++issued;
+        }
+        if (lane == 0) {
+          if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
+          // Drain: every copy started here must have landed before the CTA exits.  The newest
+          // copy of each stage is the one whose phase is current.
+          for (int i = (issued > nst ? issued - nst : 0); i < issued; ++i) mbar_wait(&full[i % nst], (i / nst) & 1);
+          for (int i = (nq > Q_STAGES ? nq - Q_STAGES : 0); i < nq; ++i)
+            mbar_wait(&q_full[i % Q_STAGES], (i / Q_STAGES) & 1);
         }
       }
-      if (lane == 0) {
+    } else if (warp == MMA_WARP) {
+      // ------------------------------------------------------------ S = Q K^T issue
+      // S of global step gs goes to TMEM buffer gs % 3, which held P of step gs - 3: wait until
+      // that P.V is done.  The whole warp runs the loop; one elected lane issues.
+      {
+        constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0);   // Q (K-major) x K (K-major)
+        bool ok = true;
+        int gs = 0;
+        TileWalk walk;
+        WorkTile t;
+        for (int k = 0; ok && walk.next(p, t); ++k) {
+          const int qs = k % Q_STAGES;
+          if (!wait(&q_full[qs], (k / Q_STAGES) & 1)) { ok = false; break; }
+          const uint32_t qbase = smem_u32(sQ + qs * L::Q_BYTES);
+          const int nkv = tile_nkv(t);
+          for (int j = 0; j < nkv; ++j, ++gs) {
+            const int sb = gs % NSB;
+            const int st = gs % K_STAGES;
+            if ((gs >= NSB && !wait(&pv_done[sb], ((gs - NSB) / NSB) & 1)) ||
+                !wait(&k_full[st], (gs / K_STAGES) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t kbase = smem_u32(sK + st * L::KV_BYTES);
+            const uint32_t s_tmem = tmem + sb * BN;
+  #pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              // 16 columns of d: panel kk / 4, 32 bytes into its 128-byte rows
+              const uint32_t qoff = (kk >> 2) * L::Q_PANEL + (kk & 3) * 32;
+              const uint32_t koff = (kk >> 2) * L::KV_PANEL + (kk & 3) * 32;
+              umma_ss_warp(s_tmem, smem_desc_sw128(qbase + qoff, 16, 1024), smem_desc_sw128(kbase + koff, 16, 1024),
+                           IDESC_S, kk > 0 ? 1u : 0u);
+            }
+            umma_commit_warp(&s_full[sb]);
+            umma_commit_warp(&k_empty[st]);
+          }
+          umma_commit_warp(&q_empty[qs]);  // the buffer may take another Q once these products are done
+        }
         if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
-        // Drain: every copy started here must have landed before the CTA exits.  The newest
-        // copy of each stage is the one whose phase is current.
-        for (int i = (issued > nst ? issued - nst : 0); i < issued; ++i) mbar_wait(&full[i % nst], (i / nst) & 1);
-        for (int i = (nq > Q_STAGES ? nq - Q_STAGES : 0); i < nq; ++i)
-          mbar_wait(&q_full[i % Q_STAGES], (i / Q_STAGES) & 1);
+        umma_commit_warp(&mma_done[0]);
+        if (!wait(&mma_done[0], 0)) set_error(&g_prefill_status, kDevWaitTimeout);
       }
-    }
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ S = Q K^T issue
-    // S of global step gs goes to TMEM buffer gs % 3, which held P of step gs - 3: wait until
-    // that P.V is done.  The whole warp runs the loop; one elected lane issues.
-    {
-      constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0);   // Q (K-major) x K (K-major)
-      bool ok = true;
-      int gs = 0;
-      TileWalk walk;
-      WorkTile t;
-      for (int k = 0; ok && walk.next(p, t); ++k) {
-        const int qs = k % Q_STAGES;
-        if (!wait(&q_full[qs], (k / Q_STAGES) & 1)) { ok = false; break; }
-        const uint32_t qbase = smem_u32(sQ + qs * L::Q_BYTES);
-        const int nkv = tile_nkv(t);
-        for (int j = 0; j < nkv; ++j, ++gs) {
-          const int sb = gs % NSB;
-          const int st = gs % K_STAGES;
-          if ((gs >= NSB && !wait(&pv_done[sb], ((gs - NSB) / NSB) & 1)) ||
-              !wait(&k_full[st], (gs / K_STAGES) & 1)) {
-            ok = false;
-            break;
+    } else if (warp == PV_WARP) {
+      // ------------------------------------------------------------ O += P V issue
+      // The whole warp runs the loop; one elected lane issues.
+      {
+        constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 1);    // P (TMEM) x V (MN-major)
+        const uint32_t o_tmem = tmem + O_COL;
+        bool ok = true;
+        int gs = 0;
+        TileWalk walk;
+        WorkTile t;
+        for (int k = 0; ok && walk.next(p, t); ++k) {
+          // the first product of a tile overwrites O: the previous tile's epilogue must have read it
+          if (k > 0 && !wait(o_free, (k - 1) & 1)) { ok = false; break; }
+          const int nkv = tile_nkv(t);
+          for (int j = 0; j < nkv; ++j, ++gs) {
+            const int sb = gs % NSB;
+            const int st = gs % V_STAGES;
+            if (!wait(&p_full[sb], (gs / NSB) & 1) || !wait(&v_full[st], (gs / V_STAGES) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t vbase = smem_u32(sV + st * L::KV_BYTES);
+            const uint32_t p_tmem = tmem + sb * BN;
+  #pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              // 16 keys = two 8-row swizzle atoms; d panels are BN*128 bytes apart
+              umma_ts_warp(o_tmem, p_tmem + kk * 8, smem_desc_sw128(vbase + kk * 16 * 128, BN * 128, 1024), IDESC_O,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit_warp(&pv_done[sb]);
+            umma_commit_warp(&v_empty[st]);
+            if (j == nkv - 1) umma_commit_warp(o_full);
           }
-          tc_fence_after();
-          const uint32_t kbase = smem_u32(sK + st * L::KV_BYTES);
-          const uint32_t s_tmem = tmem + sb * BN;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            // 16 columns of d: panel kk / 4, 32 bytes into its 128-byte rows
-            const uint32_t qoff = (kk >> 2) * L::Q_PANEL + (kk & 3) * 32;
-            const uint32_t koff = (kk >> 2) * L::KV_PANEL + (kk & 3) * 32;
-            umma_ss_warp(s_tmem, smem_desc_sw128(qbase + qoff, 16, 1024), smem_desc_sw128(kbase + koff, 16, 1024),
-                         IDESC_S, kk > 0 ? 1u : 0u);
-          }
-          umma_commit_warp(&s_full[sb]);
-          umma_commit_warp(&k_empty[st]);
         }
-        umma_commit_warp(&q_empty[qs]);  // the buffer may take another Q once these products are done
+        if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
+        umma_commit_warp(&mma_done[1]);
+        if (!wait(&mma_done[1], 0)) set_error(&g_prefill_status, kDevWaitTimeout);
       }
-      if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
-      umma_commit_warp(&mma_done[0]);
-      if (!wait(&mma_done[0], 0)) set_error(&g_prefill_status, kDevWaitTimeout);
-    }
-  } else if (warp == PV_WARP) {
-    // ------------------------------------------------------------ O += P V issue
-    // The whole warp runs the loop; one elected lane issues.
-    {
-      constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 1);    // P (TMEM) x V (MN-major)
-      const uint32_t o_tmem = tmem + O_COL;
-      bool ok = true;
-      int gs = 0;
-      TileWalk walk;
-      WorkTile t;
-      for (int k = 0; ok && walk.next(p, t); ++k) {
-        // the first product of a tile overwrites O: the previous tile's epilogue must have read it
-        if (k > 0 && !wait(o_free, (k - 1) & 1)) { ok = false; break; }
-        const int nkv = tile_nkv(t);
-        for (int j = 0; j < nkv; ++j, ++gs) {
-          const int sb = gs % NSB;
-          const int st = gs % V_STAGES;
-          if (!wait(&p_full[sb], (gs / NSB) & 1) || !wait(&v_full[st], (gs / V_STAGES) & 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t vbase = smem_u32(sV + st * L::KV_BYTES);
-          const uint32_t p_tmem = tmem + sb * BN;
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            // 16 keys = two 8-row swizzle atoms; d panels are BN*128 bytes apart
-            umma_ts_warp(o_tmem, p_tmem + kk * 8, smem_desc_sw128(vbase + kk * 16 * 128, BN * 128, 1024), IDESC_O,
-                         (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit_warp(&pv_done[sb]);
-          umma_commit_warp(&v_empty[st]);
-          if (j == nkv - 1) umma_commit_warp(o_full);
-        }
-      }
-      if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
-      umma_commit_warp(&mma_done[1]);
-      if (!wait(&mma_done[1], 0)) set_error(&g_prefill_status, kDevWaitTimeout);
     }
   } else if (warp < PRODUCER_WARP) {
+    regs_inc<REG_SOFTMAX>();
     // ------------------------------------------------------------ softmax
     // Warp w takes 16 whole rows: TMEM lanes r0 .. r0 + 15 with r0 = 32 (w % 4) + 16 (w / 4).
     // Through the 16x256b TMEM shape four threads share a row: thread t holds rows r0 + t/4 ("a")
@@ -507,62 +517,77 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (c > lim_b) sr[4 * i + 2 + e] = __float_as_uint(-INFINITY);
             }
         }
-        float mxa = -INFINITY, mxb = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < NG; ++i) {
-          mxa = fmax3(mxa, __uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1]));
-          mxb = fmax3(mxb, __uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3]));
-        }
-        mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
-        mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
-        mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
-        mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
+        // The exponentials are taken against a reference max per row: exact for any reference (O
+        // and l always refer to the same one), and nothing overflows while every p stays below
+        // 2^32.  The first step of a tile takes the row max as the reference.  A later step keeps
+        // the reference unless one of this thread's partial row sums leaves that range; only then
+        // does it take the row max, move the reference (rescaling O and l when the max has grown by
+        // more than 2^8) and compute its P again.
         float alpha_a = 1.f, alpha_b = 1.f;
         bool rescale_o = false;
-        if (j == 0) {
-          m_a = mxa;
-          m_b = mxb;
-        } else {
-          if ((mxa - m_a) * c2 > RESCALE_LOG2_THRESHOLD) {
-            alpha_a = ex2_approx((m_a - mxa) * c2);
-            l_a *= alpha_a;
-            m_a = mxa;
-            rescale_o = true;
-          }
-          if ((mxb - m_b) * c2 > RESCALE_LOG2_THRESHOLD) {
-            alpha_b = ex2_approx((m_b - mxb) * c2);
-            l_b *= alpha_b;
-            m_b = mxb;
-            rescale_o = true;
-          }
-        }
-        const float mba = (m_a == -INFINITY) ? 0.f : m_a * c2;
-        const float mbb = (m_b == -INFINITY) ? 0.f : m_b * c2;
-        const uint64_t nma = f2_pack(-mba, -mba), nmb = f2_pack(-mbb, -mbb);
-        // p = 2^(s*scale*log2e - m*scale*log2e) in f32x2 pairs.  P (bf16, two per column) goes to the
-        // first BN / 2 columns of this S buffer: the pair of columns 8i + cq, + 1 to column 4i + cq/2,
-        // which is where the 16x128b shape puts this thread's registers 2i (row a) and 2i + 1 (row b).
-        uint64_t acc_a = 0ull, acc_b = 0ull;
         uint32_t pk[2 * NG];
+        float ps_a = 0.f, ps_b = 0.f;  // this step's shares of the two row sums
+        const bool need_max = __any_sync(0xffffffffu, j == 0 || !(m_a > -INFINITY) || !(m_b > -INFINITY));
+        for (int pass = need_max ? 1 : 0; pass < 2; ++pass) {
+          if (pass == 1) {
+            float mxa = -INFINITY, mxb = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < NG; ++i) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1])), c2x2, nma), x0, x1);
-          const float pa0 = ex2_approx(x0), pa1 = ex2_approx(x1);
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3])), c2x2, nmb), x0, x1);
-          const float pb0 = ex2_approx(x0), pb1 = ex2_approx(x1);
-          acc_a = f2_add(acc_a, f2_pack(pa0, pa1));
-          acc_b = f2_add(acc_b, f2_pack(pb0, pb1));
-          pk[2 * i] = pack_bf16x2(pa0, pa1);
-          pk[2 * i + 1] = pack_bf16x2(pb0, pb1);
-        }
-        {
+            for (int i = 0; i < NG; ++i) {
+              mxa = fmax3(mxa, __uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1]));
+              mxb = fmax3(mxb, __uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3]));
+            }
+            mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
+            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
+            mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
+            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
+            if (!(m_a > -INFINITY)) {
+              m_a = mxa;
+            } else if ((mxa - m_a) * c2 > RESCALE_LOG2_THRESHOLD) {
+              alpha_a = ex2_approx((m_a - mxa) * c2);
+              l_a *= alpha_a;
+              m_a = mxa;
+              rescale_o = true;
+            }
+            if (!(m_b > -INFINITY)) {
+              m_b = mxb;
+            } else if ((mxb - m_b) * c2 > RESCALE_LOG2_THRESHOLD) {
+              alpha_b = ex2_approx((m_b - mxb) * c2);
+              l_b *= alpha_b;
+              m_b = mxb;
+              rescale_o = true;
+            }
+          }
+          const float mba = (m_a == -INFINITY) ? 0.f : m_a * c2;
+          const float mbb = (m_b == -INFINITY) ? 0.f : m_b * c2;
+          const uint64_t nma = f2_pack(-mba, -mba), nmb = f2_pack(-mbb, -mbb);
+          // p = 2^(s*scale*log2e - m*scale*log2e) in f32x2 pairs.  P (bf16, two per column) goes to
+          // the first BN / 2 columns of this S buffer: the pair of columns 8i + cq, + 1 to column
+          // 4i + cq/2, which is where the 16x128b shape puts this thread's registers 2i (row a) and
+          // 2i + 1 (row b).
+          uint64_t acc_a = 0ull, acc_b = 0ull;
+#pragma unroll
+          for (int i = 0; i < NG; ++i) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1])), c2x2, nma), x0,
+                      x1);
+            const float pa0 = ex2_approx(x0), pa1 = ex2_approx(x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3])), c2x2, nmb),
+                      x0, x1);
+            const float pb0 = ex2_approx(x0), pb1 = ex2_approx(x1);
+            acc_a = f2_add(acc_a, f2_pack(pa0, pa1));
+            acc_b = f2_add(acc_b, f2_pack(pb0, pb1));
+            pk[2 * i] = pack_bf16x2(pa0, pa1);
+            pk[2 * i + 1] = pack_bf16x2(pb0, pb1);
+          }
           float a0, a1, b0, b1;
           f2_unpack(acc_a, a0, a1);
           f2_unpack(acc_b, b0, b1);
-          l_a += a0 + a1;
-          l_b += b0 + b1;
+          ps_a = a0 + a1;
+          ps_b = b0 + b1;
+          if (pass == 1 || !__any_sync(0xffffffffu, !(ps_a <= P_PARTIAL_LIMIT) || !(ps_b <= P_PARTIAL_LIMIT))) break;
         }
+        l_a += ps_a;
+        l_b += ps_b;
         tmem_st16_128b<NG>(s_tmem, pk);
         if (__any_sync(0xffffffffu, rescale_o)) {
           // O must hold P V of the previous step before it is rescaled
@@ -608,6 +633,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
   } else {
+    regs_dec<REG_EPI>();
     // ------------------------------------------------------------ epilogue
     // One thread per row: wait for the tile's last P.V, read O out of TMEM (bf16 pairs after
     // the division by l), release O, then store 64-column panels through the staging buffer.
