@@ -654,6 +654,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&l_empty[tb]);
       const float inv_l = 1.f / l;
+      const uint64_t il2 = f2_pack(inv_l, inv_l);
       if (p.lse != nullptr && t.qt * BM + row < t.len)
         p.lse[(static_cast<size_t>(t.z) * p.Hq + t.hq) * p.S + t.base + t.qt * BM + row] = m_row * p.scale + logf(l);
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_full, k & 1));
@@ -670,7 +671,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 16; ++c)
-            ob[c4 * 16 + c] = pack_bf16x2(__uint_as_float(r[2 * c]) * inv_l, __uint_as_float(r[2 * c + 1]) * inv_l);
+          {
+            float o0, o1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])), il2), o0, o1);
+            ob[c4 * 16 + c] = pack_bf16x2(o0, o1);
+          }
         }
         if (g0 + L::OGRP == D) {
           tc_fence_before();

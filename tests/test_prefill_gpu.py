@@ -65,6 +65,19 @@ def test_large_scores_running_max_jumps(attn, gpu, d):
     full_compare(attn, x, 1.0 / math.sqrt(d), True, gpu, f"max jumps d={d}")
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_score_jump_past_the_reference_range(attn, gpu, d):
+    """A few keys past the first key tile scaled by 64: against the first tile's row max their
+    exponentials would overflow, so every row that sees them must take the row max again and
+    rescale (the step's second pass), and rows that do not see them keep the first reference."""
+    x = make_prefill_inputs(1, 2, 1, 600, d, seed=45)
+    k = x.k.clone()
+    k[:, 200::131] *= 64
+    x.k = k
+    full_compare(attn, x, 1.0 / math.sqrt(d), True, gpu, f"score jump d={d}")
+    full_compare(attn, x, 1.0 / math.sqrt(d), False, gpu, f"score jump non-causal d={d}")
+
+
 @pytest.mark.parametrize("d", [128, 256])
 def test_row0_returns_v0_exactly(attn, gpu, d):
     """Causal row 0 sees only key 0, so O[0] = v0 bit-exactly and LSE[0] = scale * q0.k0."""
