@@ -103,11 +103,15 @@ attn_status_t prefill_common(const void* q, const void* k, const void* v, void* 
   const uint64_t q_row = static_cast<uint64_t>(Hq) * d * 2, kv_row = static_cast<uint64_t>(Hkv) * d * 2;
   const uint32_t box = static_cast<uint32_t>(attn::prefill_tile_rows());
   const uint32_t kv_box = static_cast<uint32_t>(attn::prefill_kv_tile_rows(d));
+  // equal-length batches at d = 128 with an even number of query heads per KV head run as CTA pairs,
+  // whose K boxes hold one CTA's half of a key tile
+  const bool cta2 = attn::prefill_cta2_supported(d, Hq, Hkv, cu_seqlens != nullptr || paged != nullptr);
+  const uint32_t k_box = cta2 ? static_cast<uint32_t>(attn::prefill_cta2_k_rows()) : kv_box;
   if (!encode_3d(&maps.q, q, static_cast<uint64_t>(Hq) * d, rows, batch, q_row, q_row * rows, 64, box, 1) ||
       !encode_3d(&maps.o, o, static_cast<uint64_t>(Hq) * d, rows, batch, q_row, q_row * rows, 64, box, 1))
     return ATTN_ERR_CUDA;
   if (paged == nullptr) {
-    if (!encode_3d(&maps.k, k, static_cast<uint64_t>(Hkv) * d, rows, batch, kv_row, kv_row * rows, 64, kv_box, 1) ||
+    if (!encode_3d(&maps.k, k, static_cast<uint64_t>(Hkv) * d, rows, batch, kv_row, kv_row * rows, 64, k_box, 1) ||
         !encode_3d(&maps.v, v, static_cast<uint64_t>(Hkv) * d, rows, batch, kv_row, kv_row * rows, 64, kv_box, 1))
       return ATTN_ERR_CUDA;
   } else {
@@ -142,6 +146,7 @@ attn_status_t prefill_common(const void* q, const void* k, const void* v, void* 
   if (static_cast<int64_t>(p.num_qblocks) * p.B * p.Hq > (int64_t(1) << 30)) return ATTN_ERR_INVALID_ARG;
   p.div_heads = attn::FastDiv::make(static_cast<uint32_t>(p.Hq));
   p.div_level = attn::FastDiv::make(static_cast<uint32_t>(p.B * p.Hq));
+  if (cta2) return from_cuda(attn::prefill_cta2_launch(maps, p, static_cast<cudaStream_t>(stream)));
   return from_cuda(attn::prefill_launch(d, maps, p, static_cast<cudaStream_t>(stream)));
 }
 

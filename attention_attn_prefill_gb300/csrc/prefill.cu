@@ -759,11 +759,14 @@ cudaError_t prefill_launch(int d, const PrefillMaps& maps, const PrefillParams& 
 }
 
 cudaError_t prefill_status(uint32_t* out, bool clear) {
+  uint32_t pair = 0;
   cudaError_t e = cudaMemcpyFromSymbol(out, g_prefill_status, sizeof(uint32_t));
   if (e == cudaSuccess && clear) {
     const uint32_t zero = 0;
     e = cudaMemcpyToSymbol(g_prefill_status, &zero, sizeof(uint32_t));
   }
+  if (e == cudaSuccess) e = prefill_cta2_status(&pair, clear);
+  if (e == cudaSuccess && *out == 0) *out = pair;
   return e;
 }
 

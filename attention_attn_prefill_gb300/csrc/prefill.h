@@ -61,6 +61,14 @@ int prefill_rows_per_cta();
 int prefill_tile_rows();            // rows of a Q / O box
 int prefill_kv_tile_rows(int d);    // rows of a K / V box for head dim d
 cudaError_t prefill_launch(int d, const PrefillMaps& maps, const PrefillParams& p, cudaStream_t stream);
-cudaError_t prefill_status(uint32_t* out, bool clear);
+cudaError_t prefill_status(uint32_t* out, bool clear);  // both prefill kernels' status words
+
+// CTA-pair kernel (prefill_cta2.cu): head dim 128, an even number of query heads per KV head, a batch
+// of equal-length sequences.  Its K map has boxes of prefill_cta2_k_rows() rows (a CTA's half of a
+// K tile); Q, V and O maps are as for the single-head kernel.
+bool prefill_cta2_supported(int d, int Hq, int Hkv, bool packed);
+int prefill_cta2_k_rows();
+cudaError_t prefill_cta2_launch(const PrefillMaps& maps, const PrefillParams& p, cudaStream_t stream);
+cudaError_t prefill_cta2_status(uint32_t* out, bool clear);
 
 }  // namespace attn

@@ -1,0 +1,641 @@
+// Causal (or full) prefill attention forward on sm_103a, head dim 128, as CTA pairs: the two CTAs of a
+// cluster take two query heads of one KV head (the same query tile of each), and every tcgen05.mma
+// is a 256-row product over both SMs (cta_group::2).
+//
+// What it computes: "Why your local LLM feels dumber than it is" (Part 3.14), section "What attention
+// is trying to calculate" -- O = softmax(scale*QK^T) V per query row over the keys it may see (causal:
+// keys j <= i), plus the natural-log LSE of each row -- with the tiled online softmax of "Streaming
+// process -- How the SM works inside a transformer", Steps 3-8.
+//
+// How it differs from the single-head kernel (prefill.cu), whose softmax, rescaling and epilogue it
+// shares:
+//   * CTA r of a pair holds the 128 query rows of head 2p + r (Q, double-buffered), the K tile's keys
+//     64r .. 64r + 63 and the V tile's head-dim columns 64r .. 64r + 63.  The even CTA issues
+//     S = Q K^T as one M = 256, N = 128 product (A split by rows, B by keys) and O += P V as one
+//     M = 256, N = 128 product (P from each CTA's TMEM, V split by columns); each CTA gets its own
+//     128 rows of S and O in its TMEM.  So each CTA streams half of every K and V tile: its rings
+//     hold four 16 KB stages each, twice the lookahead of the single-head kernel at the same shared
+//     memory, and one issue stream feeds two SMs;
+//   * both CTAs' copies complete on the even CTA's full barriers.  The even CTA arms each of them for
+//     both halves before the first copy and again right after its MMA issuer has consumed a phase,
+//     before the commit that frees the stage, so no copy can land on a phase that is not armed yet.
+//     The even CTA's commits reach both CTAs' barriers (multicast); the odd CTA's softmax and
+//     epilogue warps arrive on the even CTA's p_full and o_free (relaxed arrivals, after their TMEM
+//     stores or loads have completed and a tcgen05 fence);
+//   * sequences are a batch of equal length (packed sequences and paged K/V use the single-head kernel).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "prefill.h"
+#include "prefill_walk.cuh"
+#include "sm103.cuh"
+
+namespace attn {
+
+__device__ uint32_t g_prefill_cta2_status;
+
+namespace {
+
+using pf::BM;
+using pf::PANEL_ROW;
+using pf::WorkTile;
+
+constexpr int D = 128;           // head dim
+constexpr int BN = 128;          // keys per step
+constexpr int CHUNKS = D / 64;   // 64-column panels per row
+constexpr int NSB = 3;           // S buffers in TMEM
+constexpr int NUM_THREADS = 512; // 8 softmax warps, 2 TMA warps, 2 MMA warps, 4 epilogue warps
+constexpr int PRODUCER_WARP = 8; // loads Q and streams K
+constexpr int MMA_WARP = 9;      // issues S = Q K^T (even CTA), owns the TMEM allocation
+constexpr int PV_WARP = 10;      // issues O += P V (even CTA)
+constexpr int V_WARP = 11;       // streams V
+constexpr int EPI_WARP0 = 12;    // warps 12..15: epilogue, one thread per row
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float RESCALE_LOG2_THRESHOLD = 8.0f;
+constexpr float P_PARTIAL_LIMIT = 4294967296.0f;  // 2^32: bound on a thread's share of a step's row sum
+constexpr uint32_t REG_SOFTMAX = 168, REG_OTHER = 72, REG_EPI = 104;
+static_assert(8 * 32 * REG_SOFTMAX + 4 * 32 * REG_OTHER + 4 * 32 * REG_EPI == 128 * NUM_THREADS, "register split");
+
+constexpr int Q_STAGES = 2, K_STAGES = 4, V_STAGES = 4;
+constexpr int Q_PANEL = BM * PANEL_ROW;        // one panel of a Q (or output) tile: 16 KB
+constexpr int Q_BYTES = CHUNKS * Q_PANEL;      // this CTA's 128 query rows
+constexpr int KH_ROWS = BN / 2;                // keys of a K tile held by one CTA
+constexpr int KH_PANEL = KH_ROWS * PANEL_ROW;  // 8 KB
+constexpr int K_BYTES = CHUNKS * KH_PANEL;     // this CTA's half of a K tile: 16 KB
+constexpr int V_BYTES = BN * PANEL_ROW;        // all BN keys, this CTA's 64 head-dim columns: 16 KB
+constexpr int OGRP = D;                        // O columns the epilogue holds at once
+constexpr uint32_t O_COL = NSB * BN;           // O accumulator columns start here
+constexpr int Q_OFF = 0;
+constexpr int K_OFF = Q_OFF + Q_STAGES * Q_BYTES;
+constexpr int V_OFF = K_OFF + K_STAGES * K_BYTES;
+constexpr int OST_OFF = V_OFF + V_STAGES * V_BYTES;  // output staging: one 64-column panel
+constexpr int XL_OFF = OST_OFF + Q_PANEL;            // row sums and maxima for the epilogue [2 tiles][2][128]
+constexpr int BAR_OFF = XL_OFF + 2 * 2 * 128 * 4;
+// q_full[Q], q_empty[Q], k_full[K], k_empty[K], v_full[V], v_empty[V], s_full[3], p_full[3], pv_done[3],
+// o_full, o_free, mma_done[2], l_full[2], l_empty[2]
+constexpr int NUM_BARS = 2 * Q_STAGES + 2 * K_STAGES + 2 * V_STAGES + 3 * NSB + 4 + 4;
+constexpr int SLOT_OFF = BAR_OFF + NUM_BARS * 8;
+constexpr int SMEM_BYTES = SLOT_OFF + 16;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
+constexpr uint16_t BOTH = 3, EVEN = 1;  // CTA masks for multicast commits
+
+// Work units: (query tile, sequence, head pair), longest first, dealt out in a zigzag over the
+// clusters; CTA r of the pair takes head 2 * pair + r.  The host sets the divisors to B * Hq / 2
+// (units per query-tile level) and Hq / 2.
+struct PairWalk {
+  int v = 0;
+  __device__ __forceinline__ bool next(const PrefillParams& p, WorkTile& t, int rank) {
+    const int G = static_cast<int>(num_clusters_x()), c = static_cast<int>(cluster_id_x());
+    const int pairs = p.Hq >> 1;
+    const int per_qt = p.B * pairs;
+    const int total = per_qt * p.num_qblocks;
+    const int idx = v * G + ((v & 1) ? (G - 1 - c) : c);
+    ++v;
+    if (idx >= total) return false;
+    const int level = static_cast<int>(p.div_level.div(static_cast<uint32_t>(idx)));
+    t.qt = p.num_qblocks - 1 - level;
+    const int rem = idx - level * per_qt;
+    t.b = static_cast<int>(p.div_heads.div(static_cast<uint32_t>(rem)));
+    t.hq = 2 * (rem - t.b * pairs) + rank;
+    t.base = 0;
+    t.z = t.b;
+    t.len = t.kv_len = p.S;
+    t.q_off = 0;
+    return true;
+  }
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                        const PrefillParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if ((smem_u32(smem) & 1023u) != 0) {  // both CTAs see the same launch: both return
+    if (threadIdx.x == 0) set_error(&g_prefill_cta2_status, kDevMisaligned);
+    return;
+  }
+  uint8_t* sQ = smem + Q_OFF;
+  uint8_t* sK = smem + K_OFF;
+  uint8_t* sV = smem + V_OFF;
+  uint8_t* sO = smem + OST_OFF;
+  float* xl = reinterpret_cast<float*>(smem + XL_OFF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+  uint64_t* q_full = bars;                 // [Q_STAGES] (even CTA): both CTAs' Q rows are in
+  uint64_t* q_empty = q_full + Q_STAGES;   // [Q_STAGES]: every S product of the buffer's tile is done
+  uint64_t* k_full = q_empty + Q_STAGES;   // (even CTA) both halves of the K tile are in
+  uint64_t* k_empty = k_full + K_STAGES;
+  uint64_t* v_full = k_empty + K_STAGES;   // (even CTA) both halves of the V tile are in
+  uint64_t* v_empty = v_full + V_STAGES;
+  uint64_t* s_full = v_empty + V_STAGES;
+  uint64_t* p_full = s_full + NSB;         // (even CTA) both CTAs' P are in TMEM
+  uint64_t* pv_done = p_full + NSB;        // [3]: P_j V_j done, per S buffer
+  uint64_t* o_full = pv_done + NSB;
+  uint64_t* o_free = o_full + 1;           // (even CTA) both epilogues have read O out of TMEM
+  uint64_t* mma_done = o_free + 1;         // [2]: each issuer's last MMA done (even CTA)
+  uint64_t* l_full = mma_done + 2;         // [2]: a tile's row sums and maxima are in xl
+  uint64_t* l_empty = l_full + 2;          // [2]: the epilogue has read them
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SLOT_OFF);
+
+  // warp index and TMEM base made visibly warp-uniform, so the MMA operands stay in uniform registers
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
+  const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int G = p.Hq / p.Hkv;
+  auto wait = [&](uint64_t* bar, uint32_t parity) { return __all_sync(0xffffffffu, mbar_wait(bar, parity)); };
+  auto tile_nkv = [&](const WorkTile& t) { return pf::tile_nkv<BN>(p, t); };
+  struct Walk : PairWalk {};
+
+  if (warp == PRODUCER_WARP && lane == 0) {
+    for (int s = 0; s < Q_STAGES; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    for (int s = 0; s < K_STAGES; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < V_STAGES; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int s = 0; s < NSB; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 16);  // one arrival per softmax warp of both CTAs
+      mbar_init(&pv_done[s], 1);
+    }
+    mbar_init(o_full, 1);
+    mbar_init(o_free, 8);          // one arrival per epilogue warp of both CTAs
+    mbar_init(&mma_done[0], 1);
+    mbar_init(&mma_done[1], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&l_full[s], 8);    // one arrival per softmax warp
+      mbar_init(&l_empty[s], 4);   // one arrival per epilogue warp
+    }
+    if (rank == 0) {
+      // arm the first phase of every full barrier for both CTAs' halves
+      for (int s = 0; s < Q_STAGES; ++s) mbar_arrive_expect_tx(&q_full[s], 2 * Q_BYTES);
+      for (int s = 0; s < K_STAGES; ++s) mbar_arrive_expect_tx(&k_full[s], 2 * K_BYTES);
+      for (int s = 0; s < V_STAGES; ++s) mbar_arrive_expect_tx(&v_full[s], 2 * V_BYTES);
+    }
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any copy, commit or arrival crosses the pair
+  tc_fence_after();
+  const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
+
+  // Each warpgroup sets its register budget at the top of its branch: 168 registers per thread for
+  // the softmax warps, 72 for the loading and MMA warps, 104 for the epilogue.
+  if (warp >= PRODUCER_WARP && warp < EPI_WARP0) {
+    regs_dec<REG_OTHER>();
+    if (warp == PRODUCER_WARP || warp == V_WARP) {
+      // ------------------------------------------------------------ TMA producers (both CTAs)
+      // Warp 8 loads Q and this CTA's half of each K tile, warp 11 its half of each V tile; each
+      // waits on its own ring's empty barriers, which the even CTA's commits reach.  The copies
+      // complete on the even CTA's full barriers, already armed for both halves.
+      const bool is_k = warp == PRODUCER_WARP;
+      const int nst = is_k ? K_STAGES : V_STAGES;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      bool ok = true;
+      int issued = 0, nq = 0;
+      Walk walk;
+      WorkTile t;
+      for (int k = 0; ok && walk.next(p, t, rank); ++k) {
+        const int g = t.hq / G;
+        if (is_k) {
+          const int qs = k % Q_STAGES;
+          if (k >= Q_STAGES) {
+            ok = wait(&q_empty[qs], ((k / Q_STAGES) - 1) & 1);
+            if (!ok) break;
+          }
+          if (lane == 0) {
+            const uint32_t bar = cluster_addr(&q_full[qs], 0);
+            for (int c = 0; c < CHUNKS; ++c)
+              tma_load_3d_pair(sQ + qs * Q_BYTES + c * Q_PANEL, &tm_q, bar, t.hq * D + c * 64, t.qt * BM, t.z);
+          }
+          nq = k + 1;
+        }
+        const int nkv = tile_nkv(t);
+        for (int j = 0; j < nkv; ++j) {
+          const int st = issued % nst;
+          ok = wait(&empty[st], ((issued / nst) & 1) ^ 1);
+          if (!ok) break;
+          const uint32_t bar = cluster_addr(&full[st], 0);
+          if (is_k) {
+            // keys j * BN + 64 * rank .. + 63, both 64-column panels of d
+            if (lane < CHUNKS)
+              tma_load_3d_pair(sK + st * K_BYTES + lane * KH_PANEL, &tm_k, bar, g * D + lane * 64,
+                               j * BN + rank * KH_ROWS, t.z);
+          } else if (lane == 0) {
+            // all BN keys, head-dim columns 64 * rank .. + 63
+            tma_load_3d_pair(sV + st * V_BYTES, &tm_v, bar, g * D + rank * 64, j * BN, t.z);
+          }
+          ++issued;
+        }
+      }
+      if (lane == 0) {
+        if (!ok) set_error(&g_prefill_cta2_status, kDevWaitTimeout);
+        // Drain (even CTA, which holds the full barriers): every copy of the pair must have landed
+        // before the CTAs exit.  The newest copy of each stage is the one whose phase is current.
+        if (rank == 0) {
+          for (int i = (issued > nst ? issued - nst : 0); i < issued; ++i)
+            mbar_wait(&full[i % nst], (i / nst) & 1);
+          for (int i = (nq > Q_STAGES ? nq - Q_STAGES : 0); i < nq; ++i)
+            mbar_wait(&q_full[i % Q_STAGES], (i / Q_STAGES) & 1);
+        }
+      }
+    } else if (warp == MMA_WARP && rank == 0) {
+      // ------------------------------------------------------------ S = Q K^T issue (even CTA)
+      // S of global step gs goes to TMEM buffer gs % 3 (in both SMs), which held P of step gs - 3:
+      // wait until that P.V is done.  The whole warp runs the loop; one elected lane issues.
+      constexpr uint32_t IDESC_S = idesc_bf16_f32(2 * BM, BN, 0);  // Q (K-major) x K (K-major), M = 256
+      bool ok = true;
+      int gs = 0;
+      Walk walk;
+      WorkTile t;
+      for (int k = 0; ok && walk.next(p, t, rank); ++k) {
+        const int qs = k % Q_STAGES;
+        if (!wait(&q_full[qs], (k / Q_STAGES) & 1)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&q_full[qs], 2 * Q_BYTES);  // arm its next phase
+        const uint32_t qbase = smem_u32(sQ + qs * Q_BYTES);
+        const int nkv = tile_nkv(t);
+        for (int j = 0; j < nkv; ++j, ++gs) {
+          const int sb = gs % NSB;
+          const int st = gs % K_STAGES;
+          if ((gs >= NSB && !wait(&pv_done[sb], ((gs - NSB) / NSB) & 1)) || !wait(&k_full[st], (gs / K_STAGES) & 1)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(&k_full[st], 2 * K_BYTES);  // arm its next phase
+          tc_fence_after();
+          const uint32_t kbase = smem_u32(sK + st * K_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            // 16 columns of d: panel kk / 4, 32 bytes into its 128-byte rows
+            const uint32_t qoff = (kk >> 2) * Q_PANEL + (kk & 3) * 32;
+            const uint32_t koff = (kk >> 2) * KH_PANEL + (kk & 3) * 32;
+            umma_ss_pair_warp(tmem + sb * BN, smem_desc_sw128(qbase + qoff, 16, 1024),
+                              smem_desc_sw128(kbase + koff, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+          }
+          umma_commit_pair_warp(&s_full[sb], BOTH);
+          umma_commit_pair_warp(&k_empty[st], BOTH);
+        }
+        umma_commit_pair_warp(&q_empty[qs], BOTH);  // the buffers may take another Q once these are done
+      }
+      if (!ok) set_error(&g_prefill_cta2_status, kDevWaitTimeout);
+      umma_commit_pair_warp(&mma_done[0], EVEN);
+      if (!wait(&mma_done[0], 0)) set_error(&g_prefill_cta2_status, kDevWaitTimeout);
+    } else if (warp == PV_WARP && rank == 0) {
+      // ------------------------------------------------------------ O += P V issue (even CTA)
+      constexpr uint32_t IDESC_O = idesc_bf16_f32(2 * BM, D, 1);  // P (TMEM) x V (MN-major), M = 256
+      const uint32_t o_tmem = tmem + O_COL;
+      bool ok = true;
+      int gs = 0;
+      Walk walk;
+      WorkTile t;
+      for (int k = 0; ok && walk.next(p, t, rank); ++k) {
+        // the first product of a tile overwrites O: both epilogues must have read the previous one
+        if (k > 0 && !wait(o_free, (k - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const int nkv = tile_nkv(t);
+        for (int j = 0; j < nkv; ++j, ++gs) {
+          const int sb = gs % NSB;
+          const int st = gs % V_STAGES;
+          if (!wait(&p_full[sb], (gs / NSB) & 1) || !wait(&v_full[st], (gs / V_STAGES) & 1)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(&v_full[st], 2 * V_BYTES);  // arm its next phase
+          tc_fence_after();
+          const uint32_t vbase = smem_u32(sV + st * V_BYTES);
+          const uint32_t p_tmem = tmem + sb * BN;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)  // 16 keys = two 8-row swizzle atoms of this CTA's panel
+            umma_ts_pair_warp(o_tmem, p_tmem + kk * 8, smem_desc_sw128(vbase + kk * 16 * 128, BN * 128, 1024),
+                              IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit_pair_warp(&pv_done[sb], BOTH);
+          umma_commit_pair_warp(&v_empty[st], BOTH);
+          if (j == nkv - 1) umma_commit_pair_warp(o_full, BOTH);
+        }
+      }
+      if (!ok) set_error(&g_prefill_cta2_status, kDevWaitTimeout);
+      umma_commit_pair_warp(&mma_done[1], EVEN);
+      if (!wait(&mma_done[1], 0)) set_error(&g_prefill_cta2_status, kDevWaitTimeout);
+    }
+  } else if (warp < PRODUCER_WARP) {
+    regs_inc<REG_SOFTMAX>();
+    // ------------------------------------------------------------ softmax
+    // Warp w takes 16 whole rows: TMEM lanes r0 .. r0 + 15 with r0 = 32 (w % 4) + 16 (w / 4).
+    // Through the 16x256b TMEM shape four threads share a row: thread t holds rows r0 + t/4 ("a")
+    // and r0 + t/4 + 8 ("b"), columns 8i + 2(t % 4) and 8i + 2(t % 4) + 1 of each group i of 8
+    // columns.  A row max is then two shuffles, and no warp waits for another.  A wait that runs
+    // out of time clears `ok`; the warp then skips its remaining waits.
+    constexpr int NG = BN / 8;  // 8-column groups per S tile
+    const int r0 = (warp & 3) * 32 + (warp >> 2) * 16;
+    const int ra = r0 + (lane >> 2);  // row a; row b is ra + 8
+    const int cq = 2 * (lane & 3);    // this thread's first column in each group
+    const uint32_t lane_base = static_cast<uint32_t>(r0) << 16;
+    const float c2 = p.scale_log2;
+    const uint64_t c2x2 = f2_pack(c2, c2);
+    bool ok = true;
+    int gs = 0;
+    Walk walk;
+    WorkTile t;
+    for (int k = 0; walk.next(p, t, rank); ++k) {
+      const int qa = t.q_off + t.qt * BM + ra;  // positions of rows a and b among the keys
+      const int qb = qa + 8;
+      const int nkv = tile_nkv(t);
+      float m_a = -INFINITY, m_b = -INFINITY;  // raw-score maxima that O and l currently refer to
+      float l_a = 0.f, l_b = 0.f;              // this thread's shares of the row sums
+      for (int j = 0; j < nkv; ++j, ++gs) {
+        const int sb = gs % NSB;
+        const uint32_t s_tmem = tmem + lane_base + sb * BN;
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (gs / NSB) & 1));
+        tc_fence_after();
+        uint32_t sr[4 * NG];
+        tmem_ld16_256b<NG>(s_tmem, sr);
+        tmem_ld_wait();
+        // last visible column of each row in this tile: below BN - 1 only where the tile crosses
+        // the causal diagonal or the end of the sequence
+        const int key0 = j * BN;
+        int lim_a = t.kv_len - 1 - key0, lim_b = lim_a;
+        if (p.causal) {
+          lim_a = min(lim_a, qa - key0);
+          lim_b = min(lim_b, qb - key0);
+        }
+        if (min(lim_a, lim_b) < BN - 1) {
+#pragma unroll
+          for (int i = 0; i < NG; ++i)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int c = 8 * i + cq + e;
+              if (c > lim_a) sr[4 * i + e] = __float_as_uint(-INFINITY);
+              if (c > lim_b) sr[4 * i + 2 + e] = __float_as_uint(-INFINITY);
+            }
+        }
+        // The exponentials are taken against a reference max per row: exact for any reference (O
+        // and l always refer to the same one), and nothing overflows while every p stays below
+        // 2^32.  The first step of a tile takes the row max as the reference.  A later step keeps
+        // the reference unless one of this thread's partial row sums leaves that range; only then
+        // does it take the row max, move the reference (rescaling O and l when the max has grown by
+        // more than 2^8) and compute its P again.
+        float alpha_a = 1.f, alpha_b = 1.f;
+        bool rescale_o = false;
+        uint32_t pk[2 * NG];
+        float ps_a = 0.f, ps_b = 0.f;  // this step's shares of the two row sums
+        const bool need_max = __any_sync(0xffffffffu, j == 0 || !(m_a > -INFINITY) || !(m_b > -INFINITY));
+        for (int pass = need_max ? 1 : 0; pass < 2; ++pass) {
+          if (pass == 1) {
+            float mxa = -INFINITY, mxb = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < NG; ++i) {
+              mxa = fmax3(mxa, __uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1]));
+              mxb = fmax3(mxb, __uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3]));
+            }
+            mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
+            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
+            mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
+            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
+            if (!(m_a > -INFINITY)) {
+              m_a = mxa;
+            } else if ((mxa - m_a) * c2 > RESCALE_LOG2_THRESHOLD) {
+              alpha_a = ex2_approx((m_a - mxa) * c2);
+              l_a *= alpha_a;
+              m_a = mxa;
+              rescale_o = true;
+            }
+            if (!(m_b > -INFINITY)) {
+              m_b = mxb;
+            } else if ((mxb - m_b) * c2 > RESCALE_LOG2_THRESHOLD) {
+              alpha_b = ex2_approx((m_b - mxb) * c2);
+              l_b *= alpha_b;
+              m_b = mxb;
+              rescale_o = true;
+            }
+          }
+          const float mba = (m_a == -INFINITY) ? 0.f : m_a * c2;
+          const float mbb = (m_b == -INFINITY) ? 0.f : m_b * c2;
+          const uint64_t nma = f2_pack(-mba, -mba), nmb = f2_pack(-mbb, -mbb);
+          // p = 2^(s*scale*log2e - m*scale*log2e) in f32x2 pairs.  P (bf16, two per column) goes to
+          // the first BN / 2 columns of this S buffer: the pair of columns 8i + cq, + 1 to column
+          // 4i + cq/2, which is where the 16x128b shape puts this thread's registers 2i (row a) and
+          // 2i + 1 (row b).
+          uint64_t acc_a = 0ull, acc_b = 0ull;
+#pragma unroll
+          for (int i = 0; i < NG; ++i) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1])), c2x2, nma), x0,
+                      x1);
+            const float pa0 = ex2_approx(x0), pa1 = ex2_approx(x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3])), c2x2, nmb),
+                      x0, x1);
+            const float pb0 = ex2_approx(x0), pb1 = ex2_approx(x1);
+            acc_a = f2_add(acc_a, f2_pack(pa0, pa1));
+            acc_b = f2_add(acc_b, f2_pack(pb0, pb1));
+            pk[2 * i] = pack_bf16x2(pa0, pa1);
+            pk[2 * i + 1] = pack_bf16x2(pb0, pb1);
+          }
+          float a0, a1, b0, b1;
+          f2_unpack(acc_a, a0, a1);
+          f2_unpack(acc_b, b0, b1);
+          ps_a = a0 + a1;
+          ps_b = b0 + b1;
+          if (pass == 1 || !__any_sync(0xffffffffu, !(ps_a <= P_PARTIAL_LIMIT) || !(ps_b <= P_PARTIAL_LIMIT))) break;
+        }
+        l_a += ps_a;
+        l_b += ps_b;
+        tmem_st16_128b<NG>(s_tmem, pk);
+        if (__any_sync(0xffffffffu, rescale_o)) {
+          // O must hold P V of the previous step before it is rescaled
+          if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(gs - 1) % NSB], ((gs - 1) / NSB) & 1));
+          tc_fence_after();
+#pragma unroll 1
+          for (int c64 = 0; c64 < D; c64 += 64) {
+            uint32_t r[32];
+            tmem_ld16_256b_x8(tmem + lane_base + O_COL + c64, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              r[4 * i] = __float_as_uint(__uint_as_float(r[4 * i]) * alpha_a);
+              r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) * alpha_a);
+              r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) * alpha_b);
+              r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) * alpha_b);
+            }
+            tmem_st16_256b_x8(tmem + lane_base + O_COL + c64, r);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(cluster_addr(&p_full[sb], 0));  // one per warp, on the even CTA's barrier
+      }
+      // ---- end of tile: add the four threads' shares of each row sum and hand l and the row max
+      // to the epilogue warps, which write LSE and divide O by l; the softmax warps go straight on.
+      l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+      l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+      l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+      l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+      const int tb = k & 1;
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&l_empty[tb], ((k >> 1) & 1) ^ 1));
+      float* xt = xl + tb * 2 * 128;
+      if ((lane & 3) == 0) {
+        xt[ra] = l_a;
+        xt[ra + 8] = l_b;
+        xt[128 + ra] = m_a;
+        xt[128 + ra + 8] = m_b;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&l_full[tb]);
+    }
+    if (!ok) set_error(&g_prefill_cta2_status, kDevWaitTimeout);
+  } else {
+    regs_dec<REG_EPI>();
+    // ------------------------------------------------------------ epilogue
+    // One thread per row: wait for the tile's last P.V, read O out of TMEM (bf16 pairs after
+    // the division by l), release O, then store 64-column panels through the staging buffer.
+    // The last tile of a packed sequence that ends inside it is written row by row instead, so
+    // that the rows of the next sequence are left alone.
+    const int row = (warp & 3) * 32 + lane;
+    const int et = threadIdx.x - EPI_WARP0 * 32;
+    const uint32_t o_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + O_COL;
+    bool ok = true;
+    Walk walk;
+    WorkTile t;
+    for (int k = 0; walk.next(p, t, rank); ++k) {
+      const int tb = k & 1;
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&l_full[tb], (k >> 1) & 1));
+      const float* xt = xl + tb * 2 * 128;
+      const float l = xt[row];
+      const float m_row = xt[128 + row];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&l_empty[tb]);
+      const float inv_l = 1.f / l;
+      const uint64_t il2 = f2_pack(inv_l, inv_l);
+      if (p.lse != nullptr && t.qt * BM + row < t.len)
+        p.lse[(static_cast<size_t>(t.z) * p.Hq + t.hq) * p.S + t.base + t.qt * BM + row] = m_row * p.scale + logf(l);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_full, k & 1));
+      tc_fence_after();
+      const bool rowwise = p.cu_seqlens != nullptr && t.qt * BM + BM > t.len;
+      // O in groups of OGRP columns (all of it for d <= 128): bf16 pairs after the division by l
+#pragma unroll 1
+      for (int g0 = 0; g0 < D; g0 += OGRP) {
+        uint32_t ob[OGRP / 2];
+#pragma unroll
+        for (int c4 = 0; c4 < OGRP / 32; ++c4) {
+          uint32_t r[32];
+          tmem_ld32(o_row + g0 + c4 * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+          {
+            float o0, o1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])), il2), o0, o1);
+            ob[c4 * 16 + c] = pack_bf16x2(o0, o1);
+          }
+        }
+        if (g0 + OGRP == D) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(cluster_addr(o_free, 0));  // the next tile's first P.V may overwrite O
+        }
+        if (rowwise) {
+          if (t.qt * BM + row < t.len) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
+                                                  (static_cast<size_t>(t.base + t.qt * BM + row) * p.Hq + t.hq) * D +
+                                                  g0);
+#pragma unroll
+            for (int u = 0; u < OGRP / 8; ++u)
+              dst[u] = make_uint4(ob[4 * u], ob[4 * u + 1], ob[4 * u + 2], ob[4 * u + 3]);
+          }
+          continue;
+        }
+        uint8_t* line = sO + row * PANEL_ROW;
+#pragma unroll
+        for (int c = 0; c < OGRP / 64; ++c) {
+          if (et == 0) tma_store_wait_read0();  // the previous panel's store has read the staging buffer
+          named_barrier_sync(2, 128);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 w = make_uint4(ob[32 * c + 4 * u], ob[32 * c + 4 * u + 1], ob[32 * c + 4 * u + 2],
+                                       ob[32 * c + 4 * u + 3]);
+            *reinterpret_cast<uint4*>(line + ((u ^ (row & 7)) << 4)) = w;
+          }
+          fence_proxy_async_smem();
+          named_barrier_sync(2, 128);
+          if (et == 0) {
+            tma_store_3d(&tm_o, sO, t.hq * D + g0 + c * 64, t.base + t.qt * BM, t.z);
+            tma_store_commit();
+          }
+        }
+      }
+    }
+    if (!ok) set_error(&g_prefill_cta2_status, kDevWaitTimeout);
+    if (et == 0) tma_store_wait0();
+  }
+
+
+  __syncwarp();  // single-lane roles rejoin their warps before the CTA barrier
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the even CTA's products have finished with the odd CTA's memory
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, TMEM_COLS);
+  }
+}
+
+int g_num_sms = 0;
+
+}  // namespace
+
+bool prefill_cta2_supported(int d, int Hq, int Hkv, bool packed) {
+  return d == D && !packed && Hkv > 0 && Hq % Hkv == 0 && (Hq / Hkv) % 2 == 0;
+}
+
+cudaError_t prefill_cta2_launch(const PrefillMaps& m, const PrefillParams& p_in, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(prefill_cta2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  if (g_num_sms == 0) {
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  }
+  PrefillParams p = p_in;
+  p.div_heads = FastDiv::make(static_cast<uint32_t>(p.Hq / 2));
+  p.div_level = FastDiv::make(static_cast<uint32_t>(p.B * (p.Hq / 2)));
+  const long long units = static_cast<long long>(p.num_qblocks) * p.B * (p.Hq / 2);
+  const int clusters = static_cast<int>(units < g_num_sms / 2 ? units : g_num_sms / 2);
+  prefill_cta2_kernel<<<2 * clusters, NUM_THREADS, SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.o, p);
+  return cudaGetLastError();
+}
+
+int prefill_cta2_k_rows() { return KH_ROWS; }
+
+cudaError_t prefill_cta2_status(uint32_t* out, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_prefill_cta2_status, sizeof(uint32_t));
+  if (e == cudaSuccess && clear) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_prefill_cta2_status, &zero, sizeof(uint32_t));
+  }
+  return e;
+}
+
+}  // namespace attn
