@@ -352,10 +352,10 @@ def run_gpu(args):
         "prefill": {
             "value": round(tflops, 2), "unit": "TFLOP/s", "ms": round(pre_mean, 4),
             "roofline": {
-                "bound": "tensor", "kernel": "prefill_fwd_kernel<128>", "achieved": round(achieved, 2),
+                "bound": "tensor", "kernel": "prefill_cta2_kernel", "achieved": round(achieved, 2),
                 "peak": peak_tc, "unit": "TFLOP/s", "frac": round(achieved / peak_tc, 4),
                 "peak_source": f"{peak_src} bf16 dense (burst)",
-                "traffic": traffic_record("prefill_fwd_kernel<128>"), "algorithmic_bytes": cfg.min_bytes,
+                "traffic": traffic_record("prefill_cta2_kernel"), "algorithmic_bytes": cfg.min_bytes,
             },
         },
         "decode": {"value": round(gbs, 1), "unit": "GB/s", "ms": round(dec_mean, 4), "roofline": dec_roof},

@@ -48,6 +48,22 @@ def test_noncausal(attn, gpu, S, d):
     full_compare(attn, x, 1.0 / math.sqrt(d), False, gpu, f"noncausal S={S} d={d}")
 
 
+@pytest.mark.parametrize("S", [1, 129, 300, 640])
+@pytest.mark.parametrize("Hq,Hkv", [(3, 1), (6, 2)])
+def test_single_head_kernel_odd_groups(attn, gpu, S, Hq, Hkv):
+    """Odd query heads per KV head at d = 128: the single-head kernel (pairs need an even group)."""
+    x = make_prefill_inputs(2, Hq, Hkv, S, 128, seed=3000 + S + Hq)
+    full_compare(attn, x, 1.0 / math.sqrt(128), True, gpu, f"odd groups Hq={Hq} Hkv={Hkv} S={S}")
+
+
+@pytest.mark.parametrize("S", [1, 127, 128, 129, 1000])
+@pytest.mark.parametrize("Hq,Hkv", [(2, 1), (8, 2), (16, 2)])
+def test_pair_kernel_groups(attn, gpu, S, Hq, Hkv):
+    """Even query heads per KV head at d = 128: CTA pairs, including one work unit and ragged tails."""
+    x = make_prefill_inputs(1, Hq, Hkv, S, 128, seed=4000 + S + Hq)
+    full_compare(attn, x, 1.0 / math.sqrt(128), True, gpu, f"pairs Hq={Hq} Hkv={Hkv} S={S}")
+
+
 def test_mqa_and_mha(attn, gpu):
     for Hq, Hkv in ((8, 1), (3, 3)):
         x = make_prefill_inputs(1, Hq, Hkv, 200, 128, seed=30 + Hq)
