@@ -10,9 +10,11 @@ Modules:
   attention  -- the exact definition in float64 (prefill, paged decode, the
                 split/combine decomposition); every function is pinned by tests.
   numerics   -- float32 / bfloat16 rounding helpers (round to nearest even).
-  split_sim  -- the scalar group-split simulation of the long-context decode
-                page (FlashAttention-2-like partition, float32 state, bfloat16
-                weights in the numerator) and its split-count heuristic.
+  split_sim  -- the scalar group-split simulations of the long-context decode
+                page: the group geometries, per-group rounding and merges of
+                the Triton, FlashAttention-2, XQA and TensorRT-LLM decode
+                algorithms, under float32 or exact arithmetic, and the
+                FlashAttention-2 split-count heuristic.
 
 Parity status: every function here is pinned by closed forms, invariants,
 brute force on tiny inputs or values the pages print (see tests/).
