@@ -51,7 +51,15 @@ _SIGNATURES = {
     "attn_prefill_varlen": (c_int, [c_void_p] * 6 + [c_int] * 6 + [c_float, c_int, c_void_p]),
     "attn_prefill_paged": (c_int, [c_void_p] * 8 + [c_int] * 9 + [c_float, c_int, c_void_p]),
     "attn_decode_auto_splits": (c_int, [c_int] * 4),
+    "attn_emulated_partitions": (c_int, [c_int] * 5),
+    "attn_emulated_num_slots": (c_int, [c_int] * 4),
+    "attn_emulated_workspace_bytes": (c_size_t, [c_int] * 4),
+    "attn_decode_paged_emulated": (c_int, [c_void_p] * 7 + [c_int] * 9 + [c_float, c_void_p, c_size_t, c_void_p]),
+    "attn_merge_emulated": (c_int, [c_int] + [c_void_p] * 3 + [c_int] * 3 + [c_void_p] * 4),
 }
+
+# Decode numerics of other backends (attn_numerics_t).
+NUMERICS = {"triton": 1, "fa2": 2, "xqa": 3, "trt": 4}
 
 
 def library_path() -> str:
@@ -292,6 +300,102 @@ def combine(part_o: torch.Tensor, part_m: torch.Tensor, part_l: torch.Tensor, ou
         _dev(lse, torch.float32, "lse") if lse is not None else None, _stream_handle(stream))
     _check(st, "attn_combine")
     return out, lse
+
+
+def _numerics(name: str) -> int:
+    if name not in NUMERICS:
+        raise ValueError(f"numerics must be one of {sorted(NUMERICS)}")
+    return NUMERICS[name]
+
+
+def emulated_partitions(numerics: str, num_seqs: int, Hkv: int, max_tokens: int, sm_count: int) -> int:
+    """Group count the backend would pick on a GPU of ``sm_count`` SMs (host arithmetic only)."""
+    n = int(lib().attn_emulated_partitions(_numerics(numerics), num_seqs, Hkv, max_tokens, sm_count))
+    if n < 1:
+        raise AttnError(1, "attn_emulated_partitions")
+    return n
+
+
+def emulated_num_slots(numerics: str, max_blocks_per_seq: int, partitions: int = 0,
+                       page_size: int = PAGE_TOKENS) -> int:
+    return int(lib().attn_emulated_num_slots(_numerics(numerics), max_blocks_per_seq, page_size, partitions))
+
+
+def decode_paged_emulated(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
+                          seq_lens: torch.Tensor, numerics: str, partitions: int | None = None,
+                          sm_count: int | None = None, max_tokens: int | None = None, scale: float | None = None,
+                          out: torch.Tensor | None = None, lse: torch.Tensor | None = None, return_lse: bool = True,
+                          workspace: torch.Tensor | None = None, stream=None):
+    """Paged decode with another backend's numerics ("triton", "fa2", "xqa" or "trt").
+
+    ``partitions`` defaults to the count the backend picks for ``max_tokens`` (the block table's
+    capacity if not given) on a GPU of ``sm_count`` SMs (this device's if not given).  Returns
+    (o, lse, workspace); the workspace holds the per-group partials (see include/attn.h).
+    """
+    N, Hq, d = q.shape
+    num_blocks, page, Hkv, dk = k_cache.shape
+    if dk != d or v_cache.shape != k_cache.shape:
+        raise ValueError("caches must be [num_blocks, page, Hkv, d] matching q")
+    if block_table.dim() != 2 or block_table.shape[0] != N or seq_lens.shape != (N,):
+        raise ValueError("block_table must be [N, max_blocks] and seq_lens [N]")
+    max_blocks = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if partitions is None:
+        if sm_count is None:
+            sm_count = torch.cuda.get_device_properties(q.device).multi_processor_count
+        partitions = emulated_partitions(numerics, N, Hkv, max_tokens or max_blocks * page, sm_count)
+    slots = emulated_num_slots(numerics, max_blocks, partitions, page)
+    if slots < 1:
+        raise AttnError(1, "attn_emulated_num_slots")
+    need = int(lib().attn_emulated_workspace_bytes(N, Hq, d, slots))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((N, Hq), dtype=torch.float32, device=q.device)
+    st = lib().attn_decode_paged_emulated(
+        _dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.bfloat16, "k_cache"),
+        _dev(v_cache, torch.bfloat16, "v_cache"), _dev(block_table, torch.int32, "block_table"),
+        _dev(seq_lens, torch.int32, "seq_lens"), _dev(out, torch.bfloat16, "out"),
+        _dev(lse, torch.float32, "lse") if lse is not None else None,
+        N, Hq, Hkv, d, page, max_blocks, num_blocks, _numerics(numerics), partitions, float(scale),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(st, "attn_decode_paged_emulated")
+    return out, lse, workspace
+
+
+def emulated_partials(workspace: torch.Tensor, N: int, Hq: int, d: int, slots: int):
+    """Views of the partials a call of decode_paged_emulated left in its workspace:
+    (part_o [N*Hq, slots, d], part_m [N*Hq, slots], part_l [N*Hq, slots])."""
+    f = workspace.view(torch.float32)
+    rows = N * Hq
+    po = f[:rows * slots * d].view(rows, slots, d)
+    pm = f[rows * slots * d:rows * slots * (d + 1)].view(rows, slots)
+    pl = f[rows * slots * (d + 1):rows * slots * (d + 2)].view(rows, slots)
+    return po, pm, pl
+
+
+def merge_emulated(numerics: str, part_o: torch.Tensor, part_m: torch.Tensor, part_l: torch.Tensor,
+                   want_f32: bool = True, want_bf16: bool = True, return_lse: bool = True, stream=None):
+    """A backend's merge on given partials: part_o [rows, splits, d], part_m/part_l [rows, splits] f32
+    -> (o_f32 [rows, d] or None, o [rows, d] bf16 or None, lse [rows] or None)."""
+    rows, splits, d = part_o.shape
+    if part_m.shape != (rows, splits) or part_l.shape != (rows, splits):
+        raise ValueError("part_m and part_l must be [rows, splits]")
+    dev = part_o.device
+    o32 = torch.empty((rows, d), dtype=torch.float32, device=dev) if want_f32 else None
+    o = torch.empty((rows, d), dtype=torch.bfloat16, device=dev) if want_bf16 else None
+    lse = torch.empty((rows,), dtype=torch.float32, device=dev) if return_lse else None
+    st = lib().attn_merge_emulated(
+        _numerics(numerics), _dev(part_o, torch.float32, "part_o"), _dev(part_m, torch.float32, "part_m"),
+        _dev(part_l, torch.float32, "part_l"), rows, splits, d,
+        _dev(o32, torch.float32, "o_f32") if o32 is not None else None,
+        _dev(o, torch.bfloat16, "o") if o is not None else None,
+        _dev(lse, torch.float32, "lse") if lse is not None else None, _stream_handle(stream))
+    _check(st, "attn_merge_emulated")
+    return o32, o, lse
 
 
 def device_status(clear: bool = True) -> int:

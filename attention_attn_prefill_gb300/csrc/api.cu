@@ -240,11 +240,14 @@ size_t attn_decode_balanced_workspace_bytes(int num_seqs, int Hq, int Hkv, int d
          sizeof(float);
 }
 
-attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
-                                const int32_t* seq_lens, void* o, float* lse, int num_seqs, int Hq, int Hkv, int d,
-                                int page_size, int max_blocks_per_seq, int num_blocks, int num_splits,
-                                int split_tokens, float scale, void* workspace, size_t workspace_bytes,
-                                void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Argument checks shared by the paged decode entry points.
+attn_status_t check_decode_args(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                                const int32_t* seq_lens, const void* o, const float* lse, int num_seqs, int Hq,
+                                int Hkv, int d, int page_size, int max_blocks_per_seq, int num_blocks, float scale) {
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr || seq_lens == nullptr ||
       o == nullptr)
     return ATTN_ERR_INVALID_ARG;
@@ -260,6 +263,64 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;  // query heads per KV head fill at most 16 MMA rows
   if (num_seqs > 65535 || Hkv > 65535) return ATTN_ERR_INVALID_ARG;
   if (static_cast<int64_t>(num_blocks) * page_size > (int64_t(1) << 31) - 1) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+// TMA maps of the paged caches: {d, Hkv, num_blocks * page} with 64 x 1 x page boxes.
+bool encode_cache_maps(attn::DecodeMaps* maps, const void* k_cache, const void* v_cache, int Hkv, int d,
+                       int num_blocks, int page_size) {
+  const uint64_t row = static_cast<uint64_t>(Hkv) * d * 2;
+  const uint64_t tokens = static_cast<uint64_t>(num_blocks) * page_size;
+  return encode_3d(&maps->k, k_cache, d, Hkv, tokens, static_cast<uint64_t>(d) * 2, row, 64, 1, page_size) &&
+         encode_3d(&maps->v, v_cache, d, Hkv, tokens, static_cast<uint64_t>(d) * 2, row, 64, 1, page_size);
+}
+
+// Fields of the split kernel's parameters common to every mode.
+attn::DecodeParams decode_params(const void* q, const int32_t* block_table, const int32_t* seq_lens, void* o,
+                                 float* lse, int num_seqs, int Hq, int Hkv, int max_blocks_per_seq, int num_blocks,
+                                 float scale) {
+  attn::DecodeParams p = {};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.N = num_seqs;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.emu = attn::kEmuNone;
+  p.granule_pages = 1;
+  return p;
+}
+
+static_assert(ATTN_NUMERICS_TRITON == attn::kEmuTriton && ATTN_NUMERICS_FA2 == attn::kEmuFa2 &&
+                  ATTN_NUMERICS_XQA == attn::kEmuXqa && ATTN_NUMERICS_TRT == attn::kEmuTrt,
+              "public and internal numerics codes must agree");
+
+bool numerics_valid(int numerics) { return numerics >= ATTN_NUMERICS_TRITON && numerics <= ATTN_NUMERICS_TRT; }
+
+constexpr int kTrtTileTokens = 128;     // one TensorRT-LLM partial per 128-token tile
+constexpr int kXqaTileTokens = 256;     // XQA deals 256-token tiles round-robin
+constexpr int kFa2BlockTokens = 64;     // FlashAttention 2 splits whole 64-token blocks
+constexpr int kTritonSegments = 16;     // Triton always uses 16 groups
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                                const int32_t* seq_lens, void* o, float* lse, int num_seqs, int Hq, int Hkv, int d,
+                                int page_size, int max_blocks_per_seq, int num_blocks, int num_splits,
+                                int split_tokens, float scale, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  const attn_status_t chk = check_decode_args(q, k_cache, v_cache, block_table, seq_lens, o, lse, num_seqs, Hq, Hkv,
+                                              d, page_size, max_blocks_per_seq, num_blocks, scale);
+  if (chk != ATTN_OK) return chk;
   if (num_splits == 0 && split_tokens == 0) {
     // balanced mode: equal shares of all pages per worker warp, then a combine
     attn::BalancedParams bp;
@@ -268,11 +329,7 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
     const size_t need = attn_decode_balanced_workspace_bytes(num_seqs, Hq, Hkv, d);
     if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
     attn::DecodeMaps bmaps;
-    const uint64_t brow = static_cast<uint64_t>(Hkv) * d * 2;
-    const uint64_t btokens = static_cast<uint64_t>(num_blocks) * page_size;
-    if (!encode_3d(&bmaps.k, k_cache, d, Hkv, btokens, static_cast<uint64_t>(d) * 2, brow, 64, 1, page_size) ||
-        !encode_3d(&bmaps.v, v_cache, d, Hkv, btokens, static_cast<uint64_t>(d) * 2, brow, 64, 1, page_size))
-      return ATTN_ERR_CUDA;
+    if (!encode_cache_maps(&bmaps, k_cache, v_cache, Hkv, d, num_blocks, page_size)) return ATTN_ERR_CUDA;
     bp.q = static_cast<const __nv_bfloat16*>(q);
     bp.block_table = block_table;
     bp.seq_lens = seq_lens;
@@ -296,29 +353,13 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
     return ATTN_ERR_WORKSPACE;
 
   attn::DecodeMaps maps;
-  const uint64_t row = static_cast<uint64_t>(Hkv) * d * 2;
-  const uint64_t tokens = static_cast<uint64_t>(num_blocks) * page_size;
-  if (!encode_3d(&maps.k, k_cache, d, Hkv, tokens, static_cast<uint64_t>(d) * 2, row, 64, 1, page_size) ||
-      !encode_3d(&maps.v, v_cache, d, Hkv, tokens, static_cast<uint64_t>(d) * 2, row, 64, 1, page_size))
-    return ATTN_ERR_CUDA;
+  if (!encode_cache_maps(&maps, k_cache, v_cache, Hkv, d, num_blocks, page_size)) return ATTN_ERR_CUDA;
 
-  attn::DecodeParams p;
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.block_table = block_table;
-  p.seq_lens = seq_lens;
-  p.o = static_cast<__nv_bfloat16*>(o);
-  p.lse = lse;
-  p.N = num_seqs;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.G = Hq / Hkv;
-  p.max_blocks = max_blocks_per_seq;
-  p.num_blocks = num_blocks;
+  attn::DecodeParams p = decode_params(q, block_table, seq_lens, o, lse, num_seqs, Hq, Hkv, max_blocks_per_seq,
+                                       num_blocks, scale);
   p.splits = slots;
   p.split_pages = split_tokens > 0 ? split_tokens / page_size : 0;
   p.num_splits = split_tokens > 0 ? 0 : slots;
-  p.scale = scale;
-  p.scale_log2 = scale * 1.4426950408889634f;
   p.write_final = slots == 1 ? 1 : 0;
   float* ws = static_cast<float*>(workspace);
   const size_t nrow = static_cast<size_t>(num_seqs) * Hq;
@@ -343,6 +384,103 @@ attn_status_t attn_combine(const float* part_o, const float* part_m, const float
   if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
   return from_cuda(attn::combine_launch(d, part_o, part_m, part_l, rows, num_splits, o, lse,
                                         static_cast<cudaStream_t>(stream)));
+}
+
+int attn_emulated_partitions(int numerics, int num_seqs, int Hkv, int max_tokens, int sm_count) {
+  if (!numerics_valid(numerics) || num_seqs < 1 || Hkv < 1 || max_tokens < 1 || sm_count < 1) return 0;
+  const int64_t units = static_cast<int64_t>(num_seqs) * Hkv;
+  switch (numerics) {
+    case ATTN_NUMERICS_TRITON:
+      return kTritonSegments;
+    case ATTN_NUMERICS_FA2:
+      if (units > (int64_t(1) << 30) || sm_count > (1 << 29)) return 0;
+      return attn_split_heuristic(static_cast<int>(units), 2 * sm_count,
+                                  (max_tokens + kFa2BlockTokens - 1) / kFa2BlockTokens, kAutoMaxSplits);
+    case ATTN_NUMERICS_XQA: {
+      const int64_t share = sm_count / units;
+      const int tiles = (max_tokens + kXqaTileTokens - 1) / kXqaTileTokens;
+      return share < 1 ? 1 : (share < tiles ? static_cast<int>(share) : tiles);
+    }
+    default:
+      return (max_tokens + kTrtTileTokens - 1) / kTrtTileTokens;
+  }
+}
+
+int attn_emulated_num_slots(int numerics, int max_blocks_per_seq, int page_size, int partitions) {
+  if (!numerics_valid(numerics) || max_blocks_per_seq < 1 || page_size != kPage) return 0;
+  if (numerics == ATTN_NUMERICS_TRT) {
+    const int64_t slots = (static_cast<int64_t>(max_blocks_per_seq) * page_size + kTrtTileTokens - 1) / kTrtTileTokens;
+    return slots > 65535 ? 0 : static_cast<int>(slots);
+  }
+  return partitions >= 1 && partitions <= 65535 ? partitions : 0;
+}
+
+size_t attn_emulated_workspace_bytes(int num_seqs, int Hq, int d, int slots) {
+  if (num_seqs < 1 || Hq < 1 || d < 1 || slots < 1) return 0;
+  return static_cast<size_t>(num_seqs) * Hq * slots * (static_cast<size_t>(d) + 2) * sizeof(float);
+}
+
+attn_status_t attn_decode_paged_emulated(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_table, const int32_t* seq_lens, void* o, float* lse,
+                                         int num_seqs, int Hq, int Hkv, int d, int page_size, int max_blocks_per_seq,
+                                         int num_blocks, int numerics, int partitions, float scale, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  const attn_status_t chk = check_decode_args(q, k_cache, v_cache, block_table, seq_lens, o, lse, num_seqs, Hq, Hkv,
+                                              d, page_size, max_blocks_per_seq, num_blocks, scale);
+  if (chk != ATTN_OK) return chk;
+  if (!numerics_valid(numerics)) return ATTN_ERR_INVALID_ARG;
+  const int slots = attn_emulated_num_slots(numerics, max_blocks_per_seq, page_size, partitions);
+  if (slots < 1) return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_emulated_workspace_bytes(num_seqs, Hq, d, slots);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+
+  attn::DecodeMaps maps;
+  if (!encode_cache_maps(&maps, k_cache, v_cache, Hkv, d, num_blocks, page_size)) return ATTN_ERR_CUDA;
+  attn::DecodeParams p = decode_params(q, block_table, seq_lens, o, lse, num_seqs, Hq, Hkv, max_blocks_per_seq,
+                                       num_blocks, scale);
+  p.emu = numerics;
+  p.splits = slots;
+  p.write_final = 0;
+  p.num_splits = slots;
+  switch (numerics) {
+    case ATTN_NUMERICS_FA2:
+      p.granule_pages = kFa2BlockTokens / kPage;
+      break;
+    case ATTN_NUMERICS_XQA:
+      p.rr_tile_pages = kXqaTileTokens / kPage;
+      break;
+    case ATTN_NUMERICS_TRT:
+      p.split_pages = kTrtTileTokens / kPage;
+      p.num_splits = 0;
+      p.warp_groups = 1;  // 8-page groups: one per warp
+      break;
+    default:
+      break;
+  }
+  float* ws = static_cast<float*>(workspace);
+  const size_t nrow = static_cast<size_t>(num_seqs) * Hq;
+  p.part_o = ws;
+  p.part_m = ws + nrow * slots * d;
+  p.part_l = ws + nrow * slots * (d + 1);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = attn::decode_split_emulated_launch(d, maps, p, st);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  return from_cuda(attn::merge_emulated_launch(numerics, p.part_o, p.part_m, p.part_l, static_cast<int>(nrow), slots,
+                                               d, nullptr, o, lse, st));
+}
+
+attn_status_t attn_merge_emulated(int numerics, const float* part_o, const float* part_m, const float* part_l,
+                                  int rows, int num_splits, int d, float* o_f32, void* o, float* lse, void* stream) {
+  if (!numerics_valid(numerics)) return ATTN_ERR_INVALID_ARG;
+  if (part_o == nullptr || part_m == nullptr || part_l == nullptr || (o_f32 == nullptr && o == nullptr))
+    return ATTN_ERR_INVALID_ARG;
+  auto misaligned = [](const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0; };
+  if (misaligned(part_o, 4) || misaligned(part_m, 4) || misaligned(part_l, 4) || misaligned(o_f32, 4) ||
+      misaligned(o, 2) || misaligned(lse, 4))
+    return ATTN_ERR_INVALID_ARG;
+  if (rows < 1 || num_splits < 1 || d < 1 || d > 1024) return ATTN_ERR_INVALID_ARG;
+  return from_cuda(attn::merge_emulated_launch(numerics, part_o, part_m, part_l, rows, num_splits, d, o_f32, o, lse,
+                                               static_cast<cudaStream_t>(stream)));
 }
 
 attn_status_t attn_device_status(uint32_t* code, int clear) {

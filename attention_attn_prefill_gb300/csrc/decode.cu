@@ -105,7 +105,48 @@ __device__ __forceinline__ void split_pages(const DecodeParams& p, int L, int s,
   if (span <= 0 || first > pages) first = end = pages;
 }
 
-template <int D, int NW, int NS>
+// Pages of group s in the emulating variant.  Round-robin groups (tp > 0) own the tiles
+// s, s + num_splits, ... of tp pages each: page i of the group is first + (i / tp) * stride + i % tp,
+// and end - first is their count.  Otherwise the group is contiguous, [first, end), with the
+// num_splits rule counted in blocks of granule_pages pages.
+__device__ __forceinline__ void emu_group_pages(const DecodeParams& p, int L, int s, int& first, int& end, int& tp,
+                                                int& stride) {
+  const int pages = (L + PAGE - 1) / PAGE;
+  tp = p.rr_tile_pages;
+  stride = 0;
+  if (tp > 0) {
+    const int P = p.num_splits;
+    const int tiles = (pages + tp - 1) / tp;
+    const int c = tiles > s ? (tiles - 1 - s) / P + 1 : 0;  // tiles of this group
+    first = s * tp;
+    stride = P * tp;
+    int count = 0;
+    if (c > 0) {
+      const int last = (s + (c - 1) * P) * tp;  // first page of the group's last tile
+      count = (c - 1) * tp + (pages - last < tp ? pages - last : tp);
+    }
+    end = first + count;
+    return;
+  }
+  int span = p.split_pages;
+  if (span <= 0) {
+    const int gr = p.granule_pages;
+    span = gr * (((pages + gr - 1) / gr + p.num_splits - 1) / p.num_splits);
+  }
+  first = s * span;
+  end = first + span < pages ? first + span : pages;
+  if (span <= 0 || first > pages) first = end = pages;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// EMU: the variant that reproduces another backend's decode numerics (p.emu): its group
+// geometry, an exact running max (every increase rescales), XQA's bf16 weights in the sum,
+// and the backend's stored value (normalised or not, f32 or bf16-rounded).  Always writes partials.
+// With p.warp_groups (small fixed-size groups) each warp owns a whole group, CTA x serving
+// groups x * NW .. x * NW + NW - 1, and writes that group's partial from its own record.
+template <int D, int NW, int NS, bool EMU>
 __global__ void __launch_bounds__(NW * 32)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const DecodeParams p) {
@@ -128,9 +169,23 @@ __global__ void __launch_bounds__(NW * 32)
     if (threadIdx.x == 0) set_error(&g_decode_status, kDevBadSplit);
     seq_len = seq_len < 0 ? 0 : p.max_blocks * PAGE;
   }
-  int pfirst, pend;
-  split_pages(p, seq_len, s, pfirst, pend);
+  // group of this warp and its share of the group's pages: page i of the share is wstart + k * wstep
+  const bool wg = EMU && p.warp_groups;
+  const int wstart = wg ? 0 : warp, wstep = wg ? 1 : NW;
+  int pfirst, pend, rr_tp = 0, rr_stride = 0;
+  if constexpr (EMU)
+    emu_group_pages(p, seq_len, wg ? s * NW + warp : s, pfirst, pend, rr_tp, rr_stride);
+  else
+    split_pages(p, seq_len, s, pfirst, pend);
   const int npages = pend - pfirst;
+  // page of the sequence that the group's i-th page is
+  auto page_at = [&](int i) -> int {
+    if constexpr (EMU) {
+      if (rr_tp > 0) return pfirst + (i / rr_tp) * rr_stride + i % rr_tp;
+    }
+    return pfirst + i;
+  };
+  const bool xqa_sum = EMU && p.emu == kEmuXqa;  // the sum adds the bf16-rounded weights
 
   // Q rows of the G heads sharing KV head g (rows >= G are zero), swizzled by 16-byte unit.
   for (int i = threadIdx.x; i < 16 * (D / 8); i += NW * 32) {
@@ -149,10 +204,10 @@ __global__ void __launch_bounds__(NW * 32)
 
   uint8_t* my_stages = smem + L::STAGE_OFF + warp * L::WARP_BYTES;
   uint64_t* my_bars = bars + warp * NS;
-  const int n_my = npages > warp ? (npages - warp + NW - 1) / NW : 0;
+  const int n_my = npages > wstart ? (npages - wstart + wstep - 1) / wstep : 0;
 
   auto issue = [&](int k) {
-    const int pi = pfirst + warp + k * NW;
+    const int pi = page_at(wstart + k * wstep);
     int pid = p.block_table[static_cast<size_t>(n) * p.max_blocks + pi];
     if (pid < 0 || pid >= p.num_blocks) {
       set_error(&g_decode_status, kDevBadPage);
@@ -209,7 +264,7 @@ __global__ void __launch_bounds__(NW * 32)
     uint8_t* st = my_stages + (k % NS) * L::STAGE_BYTES;
     const uint32_t k_base = smem_u32(st);
     const uint32_t v_base = k_base + L::KV_BYTES;
-    const int tok0 = (pfirst + warp + k * NW) * PAGE;
+    const int tok0 = page_at(wstart + k * wstep) * PAGE;
     const int valid = seq_len - tok0 < PAGE ? seq_len - tok0 : PAGE;
     if (valid < PAGE) {
       // zero the V rows past the end of the sequence: P is 0 there, but 0 * NaN would not be
@@ -256,13 +311,13 @@ __global__ void __launch_bounds__(NW * 32)
       m_a = mx_a;
       m_b = mx_b;
     } else {
-      if ((mx_a - m_a) * c2 > RESCALE_LOG2_THRESHOLD) {
+      if (EMU ? mx_a > m_a : (mx_a - m_a) * c2 > RESCALE_LOG2_THRESHOLD) {
         al_a = ex2_approx((m_a - mx_a) * c2);
         l_a *= al_a;
         m_a = mx_a;
         rs = true;
       }
-      if ((mx_b - m_b) * c2 > RESCALE_LOG2_THRESHOLD) {
+      if (EMU ? mx_b > m_b : (mx_b - m_b) * c2 > RESCALE_LOG2_THRESHOLD) {
         al_b = ex2_approx((m_b - mx_b) * c2);
         l_b *= al_b;
         m_b = mx_b;
@@ -284,14 +339,20 @@ __global__ void __launch_bounds__(NW * 32)
       pr[nb][1] = ex2_approx(fmaf(sacc[nb][1], c2, -mb_a));
       pr[nb][2] = ex2_approx(fmaf(sacc[nb][2], c2, -mb_b));
       pr[nb][3] = ex2_approx(fmaf(sacc[nb][3], c2, -mb_b));
-      l_a += pr[nb][0] + pr[nb][1];
-      l_b += pr[nb][2] + pr[nb][3];
+      if (!xqa_sum) {
+        l_a += pr[nb][0] + pr[nb][1];
+        l_b += pr[nb][2] + pr[nb][3];
+      }
     }
     uint32_t pa[4];
     pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
     pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
     pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
     pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+    if (xqa_sum) {
+      l_a += (bf16_lo(pa[0]) + bf16_hi(pa[0])) + (bf16_lo(pa[2]) + bf16_hi(pa[2]));
+      l_b += (bf16_lo(pa[1]) + bf16_hi(pa[1])) + (bf16_lo(pa[3]) + bf16_hi(pa[3]));
+    }
     // ---- O += P V
 #pragma unroll
     for (int nb = 0; nb < D / 8; nb += 2) {
@@ -339,8 +400,34 @@ __global__ void __launch_bounds__(NW * 32)
   }
   __syncthreads();
 
-  // ---- merge the warps and write the final output or this split's partial
   const uint8_t* rec0 = smem + L::STAGE_OFF;
+  // a group's partial, from its max M (log2-scaled), sum Lsum and unnormalised output O
+  auto write_partial = [&](size_t slot, int x, float M, float Lsum, float O) {
+    float val = (Lsum > 0.f) ? O / Lsum : 0.f;
+    if constexpr (EMU) {
+      if (p.emu == kEmuTriton || p.emu == kEmuTrt) val = O;  // the weighted-value sum itself
+      if (p.emu == kEmuXqa || p.emu == kEmuTrt) val = __bfloat162float(__float2bfloat16_rn(val));
+    }
+    p.part_o[slot * D + x] = val;
+    if (x == 0) {
+      p.part_m[slot] = (Lsum > 0.f) ? M * LN2 : -INFINITY;
+      p.part_l[slot] = Lsum;
+    }
+  };
+  if (wg) {
+    // ---- one group per warp: its record is the group's partial
+    for (int i = threadIdx.x; i < NW * G * D; i += NW * 32) {
+      const int w = i / (G * D), r = (i / D) % G, x = i % D;
+      const int grp = s * NW + w;
+      if (grp >= p.splits) continue;
+      const float* rm = reinterpret_cast<const float*>(rec0 + w * L::WARP_BYTES);
+      const size_t row = static_cast<size_t>(n) * p.Hq + g * G + r;
+      write_partial(row * p.splits + grp, x, rm[r], rm[16 + r], rm[32 + r * D + x]);
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    return;
+  }
+  // ---- merge the warps and write the final output or this split's partial
   for (int i = threadIdx.x; i < G * D; i += NW * 32) {
     const int r = i / D, x = i % D;
     float M = -INFINITY;
@@ -365,12 +452,7 @@ __global__ void __launch_bounds__(NW * 32)
       p.o[row * D + x] = __float2bfloat16_rn(out);
       if (x == 0 && p.lse != nullptr) p.lse[row] = (Lsum > 0.f) ? (M + log2f(Lsum)) * LN2 : -INFINITY;
     } else {
-      const size_t slot = row * p.splits + s;
-      p.part_o[slot * D + x] = (Lsum > 0.f) ? O / Lsum : 0.f;
-      if (x == 0) {
-        p.part_m[slot] = (Lsum > 0.f) ? M * LN2 : -INFINITY;
-        p.part_l[slot] = Lsum;
-      }
+      write_partial(row * p.splits + s, x, M, Lsum, O);
     }
   }
   // the dependent combine may be scheduled once every CTA has written its share
@@ -851,20 +933,20 @@ cudaError_t launch_balanced(const DecodeMaps& m, const BalancedParams& p, cudaSt
   return cudaLaunchKernelEx(&cfg, combine_balanced_kernel<D>, p);
 }
 
-template <int D, int NW, int NS>
+template <int D, int NW, int NS, bool EMU = false>
 cudaError_t launch_split(const DecodeMaps& m, const DecodeParams& p, cudaStream_t stream) {
-  auto kern = decode_split_kernel<D, NW, NS>;
+  auto kern = decode_split_kernel<D, NW, NS, EMU>;
   const int smem = DLayout<D, NW, NS>::ALLOC;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.splits, p.Hkv, p.N);
+  dim3 grid(EMU && p.warp_groups ? (p.splits + NW - 1) / NW : p.splits, p.Hkv, p.N);
   kern<<<grid, NW * 32, smem, stream>>>(m.k, m.v, p);
   return cudaGetLastError();
 }
 
 template <int D, int NW, int NS>
 int split_ctas_per_sm() {
-  auto kern = decode_split_kernel<D, NW, NS>;
+  auto kern = decode_split_kernel<D, NW, NS, false>;
   const int smem = DLayout<D, NW, NS>::ALLOC;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
   int n = 0;
@@ -885,6 +967,13 @@ cudaError_t decode_split_launch(int d, const DecodeMaps& maps, const DecodeParam
   // d = 256: more resident warps per SM than deeper per-warp pipelines, measured on GB300
   if (d == 128) return launch_split<128, 4, 2>(maps, p, stream);
   if (d == 256) return launch_split<256, 3, 2>(maps, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t decode_split_emulated_launch(int d, const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream) {
+  if (p.emu == kEmuNone || p.write_final) return cudaErrorInvalidValue;
+  if (d == 128) return launch_split<128, 4, 2, true>(maps, p, stream);
+  if (d == 256) return launch_split<256, 3, 2, true>(maps, p, stream);
   return cudaErrorInvalidValue;
 }
 

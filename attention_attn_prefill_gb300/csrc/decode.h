@@ -32,6 +32,21 @@ struct DecodeParams {
   float scale;
   float scale_log2;
   int write_final;  // 1: write o / lse directly (one split)
+  // Backend-numerics emulation (read only by the emulating kernel variant):
+  int emu;            // EmuNumerics value
+  int rr_tile_pages;  // > 0: groups take tiles of this many pages round-robin (num_splits groups)
+  int granule_pages;  // pages per block of the num_splits rule (>= 1)
+  int warp_groups;    // 1: each warp owns a whole group (fixed-size groups of split_pages pages)
+};
+
+// Decode numerics of other backends that the emulating split kernel and merge reproduce:
+// where the groups come from, what a group stores, and how the groups are merged.
+enum EmuNumerics : int {
+  kEmuNone = 0,
+  kEmuTriton = 1,  // contiguous groups of 16-token tiles; f32 weighted-value sum; merged at the largest max
+  kEmuFa2 = 2,     // contiguous groups of 64-token blocks; f32 normalised output; merged by log-sums
+  kEmuXqa = 3,     // 256-token tiles round-robin; bf16 weights in the sum; bf16 normalised output
+  kEmuTrt = 4,     // one group per 128-token tile; bf16 weighted-value sum; ordered running merge
 };
 
 // Balanced ("stream-K") decode: every warp of a persistent grid takes an equal
@@ -56,6 +71,11 @@ int decode_balanced_warps(int d);  // worker warps of the split grid on the curr
 cudaError_t decode_balanced_launch(int d, const DecodeMaps& maps, const BalancedParams& p, cudaStream_t stream);
 
 cudaError_t decode_split_launch(int d, const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream);
+// The split kernel's emulating variant (p.emu != kEmuNone): always writes partials.
+cudaError_t decode_split_emulated_launch(int d, const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream);
+// Merge of emulated partials in the chosen backend's float32 operation order; o32 and o may be null.
+cudaError_t merge_emulated_launch(int numerics, const float* part_o, const float* part_m, const float* part_l,
+                                  int rows, int splits, int d, float* o32, void* o, float* lse, cudaStream_t stream);
 int decode_split_ctas_per_sm(int d);  // resident split-kernel CTAs per SM on the current device (0 on error)
 cudaError_t combine_launch(int d, const float* part_o, const float* part_m, const float* part_l, int rows,
                            int splits, void* o, float* lse, cudaStream_t stream);

@@ -1,0 +1,204 @@
+// Merges of split-KV decode partials in the float32 operation order of other backends.
+//
+// "Why your local LLM feels dumber than it is" (Part 3.14), section "Backend
+// names expand into four decode algorithms", describes how four decode
+// backends combine their groups.  This kernel reproduces each combination
+// step by step in float32, with every add, multiply and divide rounded on its
+// own (no fused multiply-add) and every exp / log evaluated in double precision
+// and rounded once to float32:
+//   Triton   top = max m_i;  c_i = exp(m_i - top);  L += l_i c_i;  N += n_i c_i;  out = N / L
+//   FA2      lse_i = m_i + log l_i;  top = max lse_i;  w_i = exp(lse_i - top);
+//            W += w_i;  N += o_i w_i;  out = N / W
+//   XQA      top = max m_i;  w_i = l_i exp(m_i - top);  W += w_i;  N += o_i w_i;  out = N / W
+//   TRT      one group after another: M' = max(M, m_i);  a = exp(M - M') (0 before the first
+//            group);  b = exp(m_i - M');  L = L a + l_i b;  N = N a + bf16(n_i) b;  out = N / L
+// Groups are visited in slot order; slots with l_i <= 0 are empty and skipped.  The
+// log-sum-exp the library also returns is the largest max (or log-sum) plus log of the
+// merged sum, rounded the same way.
+//
+// One CTA per row: the per-slot factors of a chunk of slots are computed in parallel (the
+// running maxima of the ordered merge by a warp-wide max scan) and kept in shared memory; then
+// every thread runs the sequential accumulation for its own NC consecutive output components,
+// with the stored values of the next U slots loaded ahead into registers, so that the loads
+// overlap while the additions stay in slot order.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "decode.h"
+
+namespace attn {
+namespace {
+
+constexpr int MT = 128;     // threads per row
+constexpr int CHUNK = 256;  // slots whose factors are staged at once
+constexpr int MAX_D = 1024;
+
+__device__ __forceinline__ float exp_rn(float x) { return static_cast<float>(exp(static_cast<double>(x))); }
+__device__ __forceinline__ float log_rn(float x) { return static_cast<float>(log(static_cast<double>(x))); }
+__device__ __forceinline__ float bf16_rn(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// FA2's group statistic: m + log l, each step rounded.
+__device__ __forceinline__ float log_sum(float m, float l) { return __fadd_rn(m, log_rn(l)); }
+
+// NC: output components per thread (d <= MT * NC); U: slots whose values are loaded ahead.
+template <int NC, int U>
+__global__ void __launch_bounds__(MT) merge_emulated_kernel(const float* __restrict__ part_o,
+                                                            const float* __restrict__ part_m,
+                                                            const float* __restrict__ part_l, int splits, int d,
+                                                            int mode, float* __restrict__ o32,
+                                                            __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ float f_a[CHUNK], f_b[CHUNK], f_l[CHUNK];
+  __shared__ float red[MT / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const size_t row = blockIdx.x;
+  const float* pm = part_m + row * splits;
+  const float* pl = part_l + row * splits;
+  const float* po = part_o + row * splits * static_cast<size_t>(d);
+
+  // largest max (log-sum for FA2) over the non-empty groups; the ordered merge keeps a running one
+  float top = -INFINITY;
+  if (mode != kEmuTrt) {
+    for (int i = tid; i < splits; i += MT) {
+      const float l = pl[i];
+      if (l > 0.f) top = fmaxf(top, mode == kEmuFa2 ? log_sum(pm[i], l) : pm[i]);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) top = fmaxf(top, __shfl_xor_sync(0xffffffffu, top, off));
+    if (lane == 0) red[warp] = top;
+    __syncthreads();
+    top = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  }
+
+  const int x0 = tid * NC;  // this thread's first output component
+  float acc[NC];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) acc[c] = 0.f;
+  float wsum = 0.f;
+  float run = -INFINITY;  // ordered merge: running max before the current chunk
+  bool any = false;
+
+  for (int base = 0; base < splits; base += CHUNK) {
+    const int n = splits - base < CHUNK ? splits - base : CHUNK;
+    if (mode == kEmuTrt) {
+      // warp 0: running max before (f_a) and after (f_b) each slot, by a max scan over the live slots
+      if (warp == 0) {
+        for (int j0 = 0; j0 < n; j0 += 32) {
+          const int j = j0 + lane;
+          const float l = j < n ? pl[base + j] : 0.f;
+          const float v = l > 0.f ? pm[base + j] : -INFINITY;
+          float incl = v;
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const float t = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl = fmaxf(incl, t);
+          }
+          incl = fmaxf(incl, run);
+          float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+          if (lane == 0) excl = run;
+          if (j < n) {
+            f_a[j] = excl;
+            f_b[j] = incl;
+            f_l[j] = l;
+          }
+          run = __shfl_sync(0xffffffffu, incl, 31);
+        }
+      }
+      __syncthreads();
+      for (int j = tid; j < n; j += MT) {
+        const float l = f_l[j];
+        if (!(l > 0.f)) continue;
+        const float before = f_a[j], after = f_b[j];
+        f_a[j] = before == -INFINITY ? 0.f : exp_rn(__fsub_rn(before, after));  // keeps the running state
+        f_b[j] = exp_rn(__fsub_rn(pm[base + j], after));                          // takes the new group
+      }
+    } else {
+      for (int j = tid; j < n; j += MT) {
+        const float l = pl[base + j];
+        f_l[j] = l;
+        if (!(l > 0.f)) continue;
+        const float m = pm[base + j];
+        if (mode == kEmuFa2)
+          f_a[j] = exp_rn(__fsub_rn(log_sum(m, l), top));
+        else if (mode == kEmuXqa)
+          f_a[j] = __fmul_rn(l, exp_rn(__fsub_rn(m, top)));
+        else
+          f_a[j] = exp_rn(__fsub_rn(m, top));
+      }
+    }
+    __syncthreads();
+    // the groups in slot order, each thread on its own components
+    for (int j0 = 0; j0 < n; j0 += U) {
+      float val[U][NC];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        // indices clamped into the row, so that every load is in bounds; the value is dropped there
+        const int j = j0 + u < n ? j0 + u : n - 1;
+        const float* src = po + static_cast<size_t>(base + j) * d;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          const int x = x0 + c < d ? x0 + c : d - 1;
+          val[u][c] = (j0 + u < n && x0 + c < d) ? src[x] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + u;
+        const float l = j < n ? f_l[j] : 0.f;
+        if (!(l > 0.f)) continue;
+        any = true;
+        if (mode == kEmuTrt) {
+          const float a = f_a[j], b = f_b[j];
+          wsum = __fadd_rn(__fmul_rn(wsum, a), __fmul_rn(l, b));
+#pragma unroll
+          for (int c = 0; c < NC; ++c) acc[c] = __fadd_rn(__fmul_rn(acc[c], a), __fmul_rn(bf16_rn(val[u][c]), b));
+        } else {
+          const float w = f_a[j];
+          wsum = __fadd_rn(wsum, mode == kEmuTriton ? __fmul_rn(l, w) : w);
+#pragma unroll
+          for (int c = 0; c < NC; ++c) acc[c] = __fadd_rn(acc[c], __fmul_rn(val[u][c], w));
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (mode == kEmuTrt) top = run;
+
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const int x = x0 + c;
+    if (x >= d) continue;
+    const float out = any ? __fdiv_rn(acc[c], wsum) : 0.f;
+    if (o32 != nullptr) o32[row * d + x] = out;
+    if (o != nullptr) o[row * d + x] = __float2bfloat16_rn(out);
+  }
+  if (lse != nullptr && tid == 0) lse[row] = any ? __fadd_rn(top, log_rn(wsum)) : -INFINITY;
+}
+
+}  // namespace
+
+cudaError_t merge_emulated_launch(int numerics, const float* part_o, const float* part_m, const float* part_l,
+                                  int rows, int splits, int d, float* o32, void* o, float* lse, cudaStream_t stream) {
+  if (numerics < kEmuTriton || numerics > kEmuTrt || rows < 1 || splits < 1 || d < 1 || d > MAX_D)
+    return cudaErrorInvalidValue;
+  void (*kern)(const float*, const float*, const float*, int, int, int, float*, __nv_bfloat16*, float*) =
+      d <= MT ? merge_emulated_kernel<1, 32>
+              : d <= 2 * MT ? merge_emulated_kernel<2, 32>
+                            : d <= 4 * MT ? merge_emulated_kernel<4, 16> : merge_emulated_kernel<8, 8>;
+  // programmatic dependent launch: the partials may come from the kernel just before it
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(rows);
+  cfg.blockDim = dim3(MT);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, part_o, part_m, part_l, splits, d, numerics, o32,
+                            static_cast<__nv_bfloat16*>(o), lse);
+}
+
+}  // namespace attn

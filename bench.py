@@ -428,6 +428,20 @@ def workload_table(attn, dev, stream, flush, peaks, paged_inputs, reps: int = 10
             gbs = nbytes / (ms * 1e-3) / 1e9
             out[f"{cfg.name} {name}"] = {"GB/s": round(gbs, 1), "us": round(ms * 1e3, 1),
                                          "frac": round(gbs / peaks["hbm_gbs"], 4)}
+        # other backends' decode numerics, with the group counts they would pick on this GPU
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        for backend in attn.NUMERICS:
+            parts = attn.emulated_partitions(backend, cfg.N, cfg.Hkv, max(lens), sms)
+            slots = attn.emulated_num_slots(backend, x.max_blocks, parts)
+            ws = torch.empty(attn.lib().attn_emulated_workspace_bytes(cfg.N, cfg.Hq, cfg.d, slots),
+                             dtype=torch.uint8, device=dev)
+            ms = timed(lambda: attn.decode_paged_emulated(dq, kc, vc, bt, sl, numerics=backend, partitions=parts,
+                                                          scale=cfg.scale, out=do, lse=dl, workspace=ws,
+                                                          stream=stream))
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            out[f"{cfg.name} emulated {backend} ({slots} groups)"] = {
+                "GB/s": round(gbs, 1), "us": round(ms * 1e3, 1), "frac": round(gbs / peaks["hbm_gbs"], 4)}
+            del ws
     out["_note"] = (f"each: mean of {reps} launches with L2 flushed before each, outside the timed region; "
                     "frac against the measured bf16 dense peak (prefill) or HBM copy (decode)")
     if attn.device_status(clear=True) != 0:
@@ -497,6 +511,8 @@ def run_case(args):
                               ctx cached tokens whose last q are new
     decode:<name>:<splits>    name in {paged_decode, longctx_decode}; splits = num_splits (0 = balanced
                               mode), t<N> for split_tokens = N, or auto for the split-count rule
+    decode_emu:<name>:<backend>  the same workloads with another backend's numerics (triton, fa2, xqa,
+                              trt) and the group count it would pick on this GPU
     """
     from workloads import DECODE_CONFIGS, PREFILL_CONFIGS
     from attention_attn_prefill_gb300.build import build
@@ -532,6 +548,24 @@ def run_case(args):
 
         def launch():
             attn.prefill(q, k, v, scale=cfg.scale, causal=True, out=o, lse=lse, stream=stream)
+    elif kind == "decode_emu":
+        cfg = {c.name: c for c in DECODE_CONFIGS}[name]
+        backend = rest[0]
+        lens = decode_lens_for(cfg)
+        x = decode_inputs_for(cfg)
+        dq, kc, vc, bt, sl = (t.to(dev) for t in (x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens))
+        do = torch.empty_like(dq)
+        dl = torch.empty((cfg.N, cfg.Hq), dtype=torch.float32, device=dev)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        parts = attn.emulated_partitions(backend, cfg.N, cfg.Hkv, max(lens), sms)
+        slots = attn.emulated_num_slots(backend, x.max_blocks, parts)
+        ws = torch.empty(attn.lib().attn_emulated_workspace_bytes(cfg.N, cfg.Hq, cfg.d, slots), dtype=torch.uint8,
+                         device=dev)
+        work, unit = decode_min_bytes(lens, cfg.Hq, cfg.Hkv, cfg.d) / 1e9, "GB/s"
+
+        def launch():
+            attn.decode_paged_emulated(dq, kc, vc, bt, sl, numerics=backend, partitions=parts, scale=cfg.scale,
+                                       out=do, lse=dl, workspace=ws, stream=stream)
     else:
         cfg = {c.name: c for c in DECODE_CONFIGS}[name]
         spec = rest[0] if rest else "1"

@@ -274,6 +274,103 @@ attn_status_t attn_combine(const float* part_o, const float* part_m, const float
                            int num_splits, int d, void* o, float* lse, void* stream);
 
 /*
+ * Decode numerics of other backends ("Why your local LLM feels dumber than it
+ * is" (Part 3.14), section "Backend names expand into four decode
+ * algorithms").  Each backend splits the context into groups in its own way,
+ * stores its own per-group value and merges the groups in its own float32
+ * order:
+ *   ATTN_NUMERICS_TRITON  `partitions` contiguous groups of whole 16-token
+ *       tiles (ceil(pages / partitions) pages each; the page's Triton uses
+ *       16); stores the float32 weighted-value sum; merge: c_i = exp(m_i - M),
+ *       M = max m_i, L = sum l_i c_i, N = sum n_i c_i, out = N / L.
+ *   ATTN_NUMERICS_FA2     `partitions` contiguous groups of whole 64-token
+ *       blocks (ceil(blocks / partitions) blocks each); stores the float32
+ *       normalised output; merge: lse_i = m_i + log l_i, w_i =
+ *       exp(lse_i - max lse), out = sum o_i w_i / sum w_i.
+ *   ATTN_NUMERICS_XQA     256-token tiles dealt round-robin over
+ *       `partitions` groups (group p takes tiles p, p + partitions, ...); the
+ *       sum of weights adds the bf16-rounded weights; stores the normalised
+ *       output rounded to bf16; merge: w_i = l_i exp(m_i - M),
+ *       out = sum o_i w_i / sum w_i.
+ *   ATTN_NUMERICS_TRT     one group per 128-token tile (`partitions` is not
+ *       used); stores the weighted-value sum rounded to bf16; merge: the
+ *       groups one after another, with a running max M' = max(M, m_i),
+ *       L = L exp(M - M') + l_i exp(m_i - M'), and likewise for N;
+ *       out = N / L.
+ * Inside a group the weights are exp(score - group max), and the
+ * weighted-value sum multiplies the values by the bf16-rounded weights.  The
+ * merges run in group order, with each float32 add, multiply and divide
+ * rounded on its own (no fused multiply-add).  exp and log are evaluated in
+ * double precision and rounded once to float32.  The group arithmetic itself
+ * runs on tensor cores, whose sums have their own order: the emulation holds
+ * the geometry, the stored types and the merge order, not the bits of every
+ * partial.
+ */
+typedef enum {
+  ATTN_NUMERICS_TRITON = 1,
+  ATTN_NUMERICS_FA2 = 2,
+  ATTN_NUMERICS_XQA = 3,
+  ATTN_NUMERICS_TRT = 4
+} attn_numerics_t;
+
+/*
+ * Group count that the backend would pick for a batch of num_seqs sequences
+ * with Hkv KV heads, the longest max_tokens long, on a GPU of sm_count SMs
+ * (pure host arithmetic):
+ *   TRITON  16;
+ *   FA2     attn_split_heuristic(num_seqs * Hkv, 2 * sm_count,
+ *           ceil(max_tokens / 64), 128), which gives the page's 54 / 62 / 87
+ *           for 132 / 148 / 188 SMs at 27,525 tokens and 4 KV heads;
+ *   XQA     min(max(1, sm_count / (num_seqs * Hkv)), ceil(max_tokens / 256)):
+ *           the page's 33 on H200 (132 SMs) and 47 on SM120 (188 SMs);
+ *   TRT     ceil(max_tokens / 128), the number of its 128-token groups.
+ * Returns 0 for invalid arguments.
+ */
+int attn_emulated_partitions(int numerics, int num_seqs, int Hkv, int max_tokens, int sm_count);
+
+/*
+ * Partial slots per (sequence, query head): `partitions` (1 .. 65535) for
+ * TRITON, FA2 and XQA; ceil(max_blocks_per_seq * page_size / 128) for TRT.
+ * Returns 0 for invalid arguments (page_size must be 16).
+ */
+int attn_emulated_num_slots(int numerics, int max_blocks_per_seq, int page_size, int partitions);
+
+/* Workspace bytes of attn_decode_paged_emulated: num_seqs * Hq * slots * (d + 2) floats. */
+size_t attn_emulated_workspace_bytes(int num_seqs, int Hq, int d, int slots);
+
+/*
+ * Paged decode with the numerics of another backend.  Arguments, layouts and
+ * errors are those of attn_decode_paged, with `numerics` and `partitions` (as
+ * above) in place of num_splits / split_tokens.  It always writes partials and
+ * merges them, even with one group.  The workspace (at least
+ * attn_emulated_workspace_bytes(num_seqs, Hq, d, slots) bytes, 16-byte
+ * aligned) holds, after the call:
+ *   part_o [num_seqs * Hq, slots, d] f32  the stored value of each group
+ *   part_m [num_seqs * Hq, slots]    f32  group max of the scaled scores
+ *   part_l [num_seqs * Hq, slots]    f32  group sum of weights
+ * in that order.  An empty group has m = -inf, l = 0 and part_o = 0.
+ * o [num_seqs, Hq, d] bf16 is the merged output rounded to bf16.  lse (may be
+ * NULL) is the merge's largest max (FA2: log-sum) plus log of its merged sum.
+ */
+attn_status_t attn_decode_paged_emulated(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_table, const int32_t* seq_lens, void* o, float* lse,
+                                         int num_seqs, int Hq, int Hkv, int d, int page_size, int max_blocks_per_seq,
+                                         int num_blocks, int numerics, int partitions, float scale, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+
+/*
+ * The backend's merge alone, on caller-supplied partials in the layout above:
+ *   part_o [rows, num_splits, d] f32, part_m / part_l [rows, num_splits] f32
+ *   (a slot with part_l <= 0 is empty and skipped);
+ *   o_f32 [rows, d] f32 (may be NULL): the float32 result before the final rounding;
+ *   o     [rows, d] bf16 (may be NULL, not both): that result rounded to bf16;
+ *   lse   [rows] f32 (may be NULL).
+ * A row with no non-empty slot gets 0 and lse = -inf.  1 <= d <= 1024.
+ */
+attn_status_t attn_merge_emulated(int numerics, const float* part_o, const float* part_m, const float* part_l,
+                                  int rows, int num_splits, int d, float* o_f32, void* o, float* lse, void* stream);
+
+/*
  * Device-side status: waits for all work on the current device, then stores
  * the first error code any kernel of this library recorded since the last
  * clear (0 = none; 1 = a pipeline wait timed out; 2 = block-table entry out of

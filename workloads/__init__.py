@@ -276,3 +276,29 @@ def decode_min_bytes(lens, Hq: int, Hkv: int, d: int, page: int = PAGE_TOKENS,
     lse = 4 * N * Hq if with_lse else 0
     bt = 4 * sum((int(L) + page - 1) // page for L in lens)
     return kv + qo + lse + bt + 4 * N
+
+
+@dataclass
+class PartialInputs:
+    part_o: torch.Tensor  # [rows, splits, d] f32: a group's stored value
+    part_m: torch.Tensor  # [rows, splits] f32: group max (-inf where empty)
+    part_l: torch.Tensor  # [rows, splits] f32: group sum of weights (0 where empty)
+
+
+def make_partials(rows: int, splits: int, d: int, seed: int, *, empty_frac: float = 0.2,
+                  empty_rows=(), m_spread: float = 3.0) -> PartialInputs:
+    """Random per-group partials for merge tests: m ~ N(0, m_spread), l ~ U[1, 300), the stored
+    values N(0, 1) times a per-group magnitude in [1, 50); slots are empty with probability
+    ``empty_frac`` (every slot of the rows in ``empty_rows``)."""
+    g = _gen(seed)
+    m = torch.randn((rows, splits), generator=g) * m_spread
+    l = 1.0 + 299.0 * torch.rand((rows, splits), generator=g)
+    mag = 1.0 + 49.0 * torch.rand((rows, splits, 1), generator=g)
+    o = torch.randn((rows, splits, d), generator=g) * mag
+    empty = torch.rand((rows, splits), generator=g) < empty_frac
+    for r in empty_rows:
+        empty[r] = True
+    m[empty] = float("-inf")
+    l[empty] = 0.0
+    o[empty] = 0.0
+    return PartialInputs(o.float().contiguous(), m.float().contiguous(), l.float().contiguous())
