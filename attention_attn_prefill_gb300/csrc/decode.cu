@@ -415,14 +415,17 @@ __global__ void __launch_bounds__(NW * 32)
     }
   };
   if (wg) {
-    // ---- one group per warp: its record is the group's partial
-    for (int i = threadIdx.x; i < NW * G * D; i += NW * 32) {
-      const int w = i / (G * D), r = (i / D) % G, x = i % D;
+    // ---- one group per warp: its record is the group's partial (D is a power of two: shifts only)
+#pragma unroll 1
+    for (int w = 0; w < NW; ++w) {
       const int grp = s * NW + w;
-      if (grp >= p.splits) continue;
+      if (grp >= p.splits) break;
       const float* rm = reinterpret_cast<const float*>(rec0 + w * L::WARP_BYTES);
-      const size_t row = static_cast<size_t>(n) * p.Hq + g * G + r;
-      write_partial(row * p.splits + grp, x, rm[r], rm[16 + r], rm[32 + r * D + x]);
+      for (int i = threadIdx.x; i < G * D; i += NW * 32) {
+        const int r = i / D, x = i % D;
+        const size_t row = static_cast<size_t>(n) * p.Hq + g * G + r;
+        write_partial(row * p.splits + grp, x, rm[r], rm[16 + r], rm[32 + r * D + x]);
+      }
     }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     return;
@@ -962,19 +965,35 @@ int decode_split_ctas_per_sm(int d) {
   return 0;
 }
 
-cudaError_t decode_split_launch(int d, const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream) {
-  // 4 warps x 2 pages in flight (3 CTAs per SM) at d = 128; 3 warps x 2 pages (2 CTAs per SM) at
-  // d = 256: more resident warps per SM than deeper per-warp pipelines, measured on GB300
-  if (d == 128) return launch_split<128, 4, 2>(maps, p, stream);
-  if (d == 256) return launch_split<256, 3, 2>(maps, p, stream);
+namespace {
+
+// 4 warps x 2 pages in flight (3 CTAs per SM) at d = 128; 3 warps x 2 pages (2 CTAs per SM) at
+// d = 256: more resident warps per SM than deeper per-warp pipelines, measured on GB300.  A grid
+// of no more CTAs than SMs (one short batch) takes CTAs of twice the warps instead (8 at d = 128,
+// 6 at d = 256, one CTA per SM), so that each SM keeps twice as many pages in flight.
+template <bool EMU>
+cudaError_t launch_split_for(int d, const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int nw = d == 128 ? 4 : 3;  // warps per CTA of the default shape
+  const long long xs = EMU && p.warp_groups ? (p.splits + nw - 1) / nw : p.splits;
+  const bool few = xs * p.Hkv * p.N <= sms && !(EMU && p.warp_groups);
+  if (d == 128) return few ? launch_split<128, 8, 2, EMU>(maps, p, stream) : launch_split<128, 4, 2, EMU>(maps, p, stream);
+  if (d == 256) return few ? launch_split<256, 6, 2, EMU>(maps, p, stream) : launch_split<256, 3, 2, EMU>(maps, p, stream);
   return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t decode_split_launch(int d, const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream) {
+  return launch_split_for<false>(d, maps, p, stream);
 }
 
 cudaError_t decode_split_emulated_launch(int d, const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream) {
   if (p.emu == kEmuNone || p.write_final) return cudaErrorInvalidValue;
-  if (d == 128) return launch_split<128, 4, 2, true>(maps, p, stream);
-  if (d == 256) return launch_split<256, 3, 2, true>(maps, p, stream);
-  return cudaErrorInvalidValue;
+  return launch_split_for<true>(d, maps, p, stream);
 }
 
 cudaError_t combine_launch(int d, const float* part_o, const float* part_m, const float* part_l, int rows,

@@ -19,8 +19,8 @@
 // One CTA per row: the per-slot factors of a chunk of slots are computed in parallel (the
 // running maxima of the ordered merge by a warp-wide max scan) and kept in shared memory; then
 // every thread runs the sequential accumulation for its own NC consecutive output components,
-// with the stored values of the next U slots loaded ahead into registers, so that the loads
-// overlap while the additions stay in slot order.
+// with the stored values of the next U slots loaded into registers while the current U are added,
+// so that the loads overlap while the additions stay in slot order.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(MT) merge_emulated_kernel(const float* __restr
                                                             int mode, float* __restrict__ o32,
                                                             __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  __shared__ float f_a[CHUNK], f_b[CHUNK], f_l[CHUNK];
+  __shared__ float f_a[CHUNK], f_b[CHUNK], f_l[CHUNK], f_m[CHUNK];
   __shared__ float red[MT / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const size_t row = blockIdx.x;
@@ -82,13 +82,19 @@ __global__ void __launch_bounds__(MT) merge_emulated_kernel(const float* __restr
 
   for (int base = 0; base < splits; base += CHUNK) {
     const int n = splits - base < CHUNK ? splits - base : CHUNK;
+    // the chunk's group sums and maxima, loaded by all threads at once
+    for (int j = tid; j < n; j += MT) {
+      f_l[j] = pl[base + j];
+      f_m[j] = pm[base + j];
+    }
+    __syncthreads();
     if (mode == kEmuTrt) {
       // warp 0: running max before (f_a) and after (f_b) each slot, by a max scan over the live slots
       if (warp == 0) {
         for (int j0 = 0; j0 < n; j0 += 32) {
           const int j = j0 + lane;
-          const float l = j < n ? pl[base + j] : 0.f;
-          const float v = l > 0.f ? pm[base + j] : -INFINITY;
+          const float l = j < n ? f_l[j] : 0.f;
+          const float v = l > 0.f ? f_m[j] : -INFINITY;
           float incl = v;
 #pragma unroll
           for (int off = 1; off < 32; off <<= 1) {
@@ -101,7 +107,6 @@ __global__ void __launch_bounds__(MT) merge_emulated_kernel(const float* __restr
           if (j < n) {
             f_a[j] = excl;
             f_b[j] = incl;
-            f_l[j] = l;
           }
           run = __shfl_sync(0xffffffffu, incl, 31);
         }
@@ -112,14 +117,13 @@ __global__ void __launch_bounds__(MT) merge_emulated_kernel(const float* __restr
         if (!(l > 0.f)) continue;
         const float before = f_a[j], after = f_b[j];
         f_a[j] = before == -INFINITY ? 0.f : exp_rn(__fsub_rn(before, after));  // keeps the running state
-        f_b[j] = exp_rn(__fsub_rn(pm[base + j], after));                          // takes the new group
+        f_b[j] = exp_rn(__fsub_rn(f_m[j], after));                                // takes the new group
       }
     } else {
       for (int j = tid; j < n; j += MT) {
-        const float l = pl[base + j];
-        f_l[j] = l;
+        const float l = f_l[j];
         if (!(l > 0.f)) continue;
-        const float m = pm[base + j];
+        const float m = f_m[j];
         if (mode == kEmuFa2)
           f_a[j] = exp_rn(__fsub_rn(log_sum(m, l), top));
         else if (mode == kEmuXqa)
@@ -129,9 +133,9 @@ __global__ void __launch_bounds__(MT) merge_emulated_kernel(const float* __restr
       }
     }
     __syncthreads();
-    // the groups in slot order, each thread on its own components
-    for (int j0 = 0; j0 < n; j0 += U) {
-      float val[U][NC];
+    // the groups in slot order, each thread on its own components; the values of the next U slots
+    // are loaded while the current U are added
+    auto load_batch = [&](float (&v)[U][NC], int j0) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         // indices clamped into the row, so that every load is in bounds; the value is dropped there
@@ -140,9 +144,14 @@ __global__ void __launch_bounds__(MT) merge_emulated_kernel(const float* __restr
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
           const int x = x0 + c < d ? x0 + c : d - 1;
-          val[u][c] = (j0 + u < n && x0 + c < d) ? src[x] : 0.f;
+          v[u][c] = (j0 + u < n && x0 + c < d) ? src[x] : 0.f;
         }
       }
+    };
+    float cur[U][NC], nxt[U][NC];
+    load_batch(cur, 0);
+    for (int j0 = 0; j0 < n; j0 += U) {
+      if (j0 + U < n) load_batch(nxt, j0 + U);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int j = j0 + u;
@@ -153,14 +162,18 @@ __global__ void __launch_bounds__(MT) merge_emulated_kernel(const float* __restr
           const float a = f_a[j], b = f_b[j];
           wsum = __fadd_rn(__fmul_rn(wsum, a), __fmul_rn(l, b));
 #pragma unroll
-          for (int c = 0; c < NC; ++c) acc[c] = __fadd_rn(__fmul_rn(acc[c], a), __fmul_rn(bf16_rn(val[u][c]), b));
+          for (int c = 0; c < NC; ++c) acc[c] = __fadd_rn(__fmul_rn(acc[c], a), __fmul_rn(bf16_rn(cur[u][c]), b));
         } else {
           const float w = f_a[j];
           wsum = __fadd_rn(wsum, mode == kEmuTriton ? __fmul_rn(l, w) : w);
 #pragma unroll
-          for (int c = 0; c < NC; ++c) acc[c] = __fadd_rn(acc[c], __fmul_rn(val[u][c], w));
+          for (int c = 0; c < NC; ++c) acc[c] = __fadd_rn(acc[c], __fmul_rn(cur[u][c], w));
         }
       }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int c = 0; c < NC; ++c) cur[u][c] = nxt[u][c];
     }
     __syncthreads();
   }
@@ -184,7 +197,7 @@ cudaError_t merge_emulated_launch(int numerics, const float* part_o, const float
   if (numerics < kEmuTriton || numerics > kEmuTrt || rows < 1 || splits < 1 || d < 1 || d > MAX_D)
     return cudaErrorInvalidValue;
   void (*kern)(const float*, const float*, const float*, int, int, int, float*, __nv_bfloat16*, float*) =
-      d <= MT ? merge_emulated_kernel<1, 32>
+      d <= MT ? merge_emulated_kernel<1, 16>
               : d <= 2 * MT ? merge_emulated_kernel<2, 32>
                             : d <= 4 * MT ? merge_emulated_kernel<4, 16> : merge_emulated_kernel<8, 8>;
   // programmatic dependent launch: the partials may come from the kernel just before it
