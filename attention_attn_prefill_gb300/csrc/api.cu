@@ -298,8 +298,8 @@ attn::DecodeParams decode_params(const void* q, const int32_t* block_table, cons
   return p;
 }
 
-static_assert(ATTN_NUMERICS_TRITON == attn::kEmuTriton && ATTN_NUMERICS_FA2 == attn::kEmuFa2 &&
-                  ATTN_NUMERICS_XQA == attn::kEmuXqa && ATTN_NUMERICS_TRT == attn::kEmuTrt,
+static_assert(int{ATTN_NUMERICS_TRITON} == int{attn::kEmuTriton} && int{ATTN_NUMERICS_FA2} == int{attn::kEmuFa2} &&
+                  int{ATTN_NUMERICS_XQA} == int{attn::kEmuXqa} && int{ATTN_NUMERICS_TRT} == int{attn::kEmuTrt},
               "public and internal numerics codes must agree");
 
 bool numerics_valid(int numerics) { return numerics >= ATTN_NUMERICS_TRITON && numerics <= ATTN_NUMERICS_TRT; }
