@@ -24,6 +24,15 @@ int main(void) {
   if (attn_decode_workspace_bytes(2, 8, 128, 4) != (size_t)2 * 8 * 4 * 130 * 4) return 7;
   /* host argument checks return before any CUDA call */
   if (attn_prefill(NULL, NULL, NULL, NULL, NULL, 1, 1, 1, 1, 128, 0.1f, 1, NULL) != ATTN_ERR_INVALID_ARG) return 8;
+  /* other backends' group counts at 27,525 tokens, four KV heads: XQA 33 on 132 SMs, 47 on 188 */
+  if (attn_emulated_partitions(ATTN_NUMERICS_XQA, 1, 4, 27525, 132) != 33) return 9;
+  if (attn_emulated_partitions(ATTN_NUMERICS_XQA, 1, 4, 27525, 188) != 47) return 10;
+  if (attn_emulated_partitions(ATTN_NUMERICS_FA2, 1, 4, 27525, 148) != 62) return 11;
+  if (attn_emulated_partitions(ATTN_NUMERICS_TRITON, 1, 4, 27525, 148) != 16) return 12;
+  if (attn_emulated_num_slots(ATTN_NUMERICS_TRT, 1721, 16, 0) != 216) return 13;
+  if (attn_emulated_workspace_bytes(2, 8, 128, 3) != (size_t)2 * 8 * 3 * 130 * 4) return 14;
+  if (attn_merge_emulated(ATTN_NUMERICS_TRT, NULL, NULL, NULL, 1, 1, 128, NULL, NULL, NULL, NULL) !=
+      ATTN_ERR_INVALID_ARG) return 15;
   puts("ok");
   return 0;
 }

@@ -147,6 +147,25 @@ def test_partials_and_output(attn, gpu, backend, d, partitions):
     assert not to_np(o)[empty].any() and np.all(to_np(lse)[empty] == -np.inf)
 
 
+@pytest.mark.parametrize("backend", BACKENDS)
+@pytest.mark.parametrize("hq_hkv,d", [((16, 1), 128), ((4, 4), 256), ((32, 2), 128)])
+def test_group_shapes_and_more_groups_than_tiles(attn, gpu, backend, hq_hkv, d):
+    """All 16 MMA rows in use (G = 16), one query head per KV head (G = 1), and G = 16 at d = 128 with
+    two KV heads; 40 groups, more than the short sequences have tiles; wide CTAs (a small grid) and
+    the default shape (40 groups x sequences x KV heads above the SM count) both run."""
+    Hq, Hkv = hq_hkv
+    lens = [3, 100, 600, 2500, 5000]
+    x = make_decode_inputs(lens, Hq=Hq, Hkv=Hkv, d=d, seed=80 + Hq + d, nan_tail=True)
+    args = [t.to(gpu) for t in (x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens)]
+    scale = 1.0 / math.sqrt(d)
+    for parts in (40, 2):
+        o, lse, _ = attn.decode_paged_emulated(*args, numerics=backend, partitions=parts, scale=scale)
+        torch.cuda.synchronize()
+        wo, wl = oa.decode_paged(x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens, scale)
+        check_o(to_np(o), wo, f"{backend} G={Hq // Hkv} d={d} parts={parts}")
+        check_backend_lse(backend, to_np(lse), wl, f"{backend} G={Hq // Hkv} parts={parts}")
+
+
 def test_worked_example_every_backend(attn, gpu):
     """The teaching input (one-hot query, k_t = score_t e_0, v_t = value_t) through each backend's
     geometry for H200, B200 and SM120: every result is one of the two bf16 neighbours of the exact
