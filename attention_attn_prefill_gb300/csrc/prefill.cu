@@ -51,6 +51,7 @@
 #include <cstdint>
 
 #include "prefill.h"
+#include "prefill_tile.cuh"
 #include "prefill_walk.cuh"
 #include "sm103.cuh"
 
@@ -69,10 +70,8 @@ constexpr int MMA_WARP = 9;      // issues S = Q K^T, owns the TMEM allocation
 constexpr int PV_WARP = 10;      // issues O += P V
 constexpr int EPI_WARP0 = 12;    // warps 12..15: epilogue, one thread per row
 constexpr uint32_t TMEM_COLS = 512;
-constexpr float RESCALE_LOG2_THRESHOLD = 8.0f;
 constexpr uint32_t REG_SOFTMAX = 168, REG_OTHER = 64, REG_EPI = 112;  // registers per thread, see below
 static_assert(8 * 32 * REG_SOFTMAX + 4 * 32 * REG_OTHER + 4 * 32 * REG_EPI == 128 * NUM_THREADS, "register split");
-constexpr float P_PARTIAL_LIMIT = 4294967296.0f;  // 2^32: bound on a thread's share of a step's row sum
 using pf::PANEL_ROW;             // bytes of one 128B-swizzle panel row: 64 bf16
 
 // Tiling and shared-memory layout per head dim.  d <= 128: 128-key K/V tiles, two Q buffers (the
@@ -468,16 +467,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp < PRODUCER_WARP) {
     regs_inc<REG_SOFTMAX>();
-    // ------------------------------------------------------------ softmax
-    // Warp w takes 16 whole rows: TMEM lanes r0 .. r0 + 15 with r0 = 32 (w % 4) + 16 (w / 4).
-    // Through the 16x256b TMEM shape four threads share a row: thread t holds rows r0 + t/4 ("a")
-    // and r0 + t/4 + 8 ("b"), columns 8i + 2(t % 4) and 8i + 2(t % 4) + 1 of each group i of 8
-    // columns.  A row max is then two shuffles, and no warp waits for another.  A wait that runs
-    // out of time clears `ok`; the warp then skips its remaining waits.
-    constexpr int NG = BN / 8;  // 8-column groups per S tile
+    // ------------------------------------------------------------ softmax (prefill_tile.cuh)
+    // Warp w takes the 16 rows r0 .. r0 + 15 of each tile, four threads per row.
     const int r0 = (warp & 3) * 32 + (warp >> 2) * 16;
     const int ra = r0 + (lane >> 2);  // row a; row b is ra + 8
-    const int cq = 2 * (lane & 3);    // this thread's first column in each group
+    const int cq = 2 * (lane & 3);    // this thread's first column in each group of 8
     const uint32_t lane_base = static_cast<uint32_t>(r0) << 16;
     const float c2 = p.scale_log2;
     const uint64_t c2x2 = f2_pack(c2, c2);
@@ -485,234 +479,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int gs = 0;
     TileWalk walk;
     WorkTile t;
+    pf::SoftmaxRows rows;
     for (int k = 0; walk.next(p, t); ++k) {
       const int qa = t.q_off + t.qt * BM + ra;  // positions of rows a and b among the keys
-      const int qb = qa + 8;
       const int nkv = tile_nkv(t);
-      float m_a = -INFINITY, m_b = -INFINITY;  // raw-score maxima that O and l currently refer to
-      float l_a = 0.f, l_b = 0.f;              // this thread's shares of the row sums
+      rows.reset();
       for (int j = 0; j < nkv; ++j, ++gs) {
         const int sb = gs % NSB;
-        const uint32_t s_tmem = tmem + lane_base + sb * BN;
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (gs / NSB) & 1));
         tc_fence_after();
-        uint32_t sr[4 * NG];
-        tmem_ld16_256b<NG>(s_tmem, sr);
-        tmem_ld_wait();
-        // last visible column of each row in this tile: below BN - 1 only where the tile crosses
-        // the causal diagonal or the end of the sequence
-        const int key0 = j * BN;
-        int lim_a = t.kv_len - 1 - key0, lim_b = lim_a;
-        if (p.causal) {
-          lim_a = min(lim_a, qa - key0);
-          lim_b = min(lim_b, qb - key0);
-        }
-        if (min(lim_a, lim_b) < BN - 1) {
-#pragma unroll
-          for (int i = 0; i < NG; ++i)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int c = 8 * i + cq + e;
-              if (c > lim_a) sr[4 * i + e] = __float_as_uint(-INFINITY);
-              if (c > lim_b) sr[4 * i + 2 + e] = __float_as_uint(-INFINITY);
-            }
-        }
-        // The exponentials are taken against a reference max per row: exact for any reference (O
-        // and l always refer to the same one), and nothing overflows while every p stays below
-        // 2^32.  The first step of a tile takes the row max as the reference.  A later step keeps
-        // the reference unless one of this thread's partial row sums leaves that range; only then
-        // does it take the row max, move the reference (rescaling O and l when the max has grown by
-        // more than 2^8) and compute its P again.
-        float alpha_a = 1.f, alpha_b = 1.f;
-        bool rescale_o = false;
-        uint32_t pk[2 * NG];
-        float ps_a = 0.f, ps_b = 0.f;  // this step's shares of the two row sums
-        const bool need_max = __any_sync(0xffffffffu, j == 0 || !(m_a > -INFINITY) || !(m_b > -INFINITY));
-        for (int pass = need_max ? 1 : 0; pass < 2; ++pass) {
-          if (pass == 1) {
-            float mxa = -INFINITY, mxb = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < NG; ++i) {
-              mxa = fmax3(mxa, __uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1]));
-              mxb = fmax3(mxb, __uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3]));
-            }
-            mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
-            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
-            mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
-            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
-            if (!(m_a > -INFINITY)) {
-              m_a = mxa;
-            } else if ((mxa - m_a) * c2 > RESCALE_LOG2_THRESHOLD) {
-              alpha_a = ex2_approx((m_a - mxa) * c2);
-              l_a *= alpha_a;
-              m_a = mxa;
-              rescale_o = true;
-            }
-            if (!(m_b > -INFINITY)) {
-              m_b = mxb;
-            } else if ((mxb - m_b) * c2 > RESCALE_LOG2_THRESHOLD) {
-              alpha_b = ex2_approx((m_b - mxb) * c2);
-              l_b *= alpha_b;
-              m_b = mxb;
-              rescale_o = true;
-            }
-          }
-          const float mba = (m_a == -INFINITY) ? 0.f : m_a * c2;
-          const float mbb = (m_b == -INFINITY) ? 0.f : m_b * c2;
-          const uint64_t nma = f2_pack(-mba, -mba), nmb = f2_pack(-mbb, -mbb);
-          // p = 2^(s*scale*log2e - m*scale*log2e) in f32x2 pairs.  P (bf16, two per column) goes to
-          // the first BN / 2 columns of this S buffer: the pair of columns 8i + cq, + 1 to column
-          // 4i + cq/2, which is where the 16x128b shape puts this thread's registers 2i (row a) and
-          // 2i + 1 (row b).
-          uint64_t acc_a = 0ull, acc_b = 0ull;
-#pragma unroll
-          for (int i = 0; i < NG; ++i) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1])), c2x2, nma), x0,
-                      x1);
-            const float pa0 = ex2_approx(x0), pa1 = ex2_approx(x1);
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3])), c2x2, nmb),
-                      x0, x1);
-            const float pb0 = ex2_approx(x0), pb1 = ex2_approx(x1);
-            acc_a = f2_add(acc_a, f2_pack(pa0, pa1));
-            acc_b = f2_add(acc_b, f2_pack(pb0, pb1));
-            pk[2 * i] = pack_bf16x2(pa0, pa1);
-            pk[2 * i + 1] = pack_bf16x2(pb0, pb1);
-          }
-          float a0, a1, b0, b1;
-          f2_unpack(acc_a, a0, a1);
-          f2_unpack(acc_b, b0, b1);
-          ps_a = a0 + a1;
-          ps_b = b0 + b1;
-          if (pass == 1 || !__any_sync(0xffffffffu, !(ps_a <= P_PARTIAL_LIMIT) || !(ps_b <= P_PARTIAL_LIMIT))) break;
-        }
-        l_a += ps_a;
-        l_b += ps_b;
-        tmem_st16_128b<NG>(s_tmem, pk);
-        if (__any_sync(0xffffffffu, rescale_o)) {
-          // O must hold P V of the previous step before it is rescaled
-          if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(gs - 1) % NSB], ((gs - 1) / NSB) & 1));
-          tc_fence_after();
-#pragma unroll 1
-          for (int c64 = 0; c64 < D; c64 += 64) {
-            uint32_t r[32];
-            tmem_ld16_256b_x8(tmem + lane_base + O_COL + c64, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              r[4 * i] = __float_as_uint(__uint_as_float(r[4 * i]) * alpha_a);
-              r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) * alpha_a);
-              r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) * alpha_b);
-              r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) * alpha_b);
-            }
-            tmem_st16_256b_x8(tmem + lane_base + O_COL + c64, r);
-          }
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
+        pf::softmax_step<BN, D, NSB>(p, t, j, gs, tmem + lane_base + sb * BN, tmem + lane_base + O_COL, qa, qa + 8,
+                                     cq, c2, c2x2, pv_done, rows, ok);
         if (lane == 0) mbar_arrive(&p_full[sb]);  // one arrival per warp: 256 would queue on the barrier
       }
-      // ---- end of tile: add the four threads' shares of each row sum and hand l and the row max
-      // to the epilogue warps, which write LSE and divide O by l; the softmax warps go straight on.
-      l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-      l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-      l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-      l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-      const int tb = k & 1;
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&l_empty[tb], ((k >> 1) & 1) ^ 1));
-      float* xt = xl + tb * 2 * 128;
-      if ((lane & 3) == 0) {
-        xt[ra] = l_a;
-        xt[ra + 8] = l_b;
-        xt[128 + ra] = m_a;
-        xt[128 + ra + 8] = m_b;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&l_full[tb]);
+      pf::softmax_tile_end(k, ra, lane, rows, l_empty, l_full, xl, ok);
     }
     if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
   } else {
     regs_dec<REG_EPI>();
-    // ------------------------------------------------------------ epilogue
-    // One thread per row: wait for the tile's last P.V, read O out of TMEM (bf16 pairs after
-    // the division by l), release O, then store 64-column panels through the staging buffer.
-    // The last tile of a packed sequence that ends inside it is written row by row instead, so
-    // that the rows of the next sequence are left alone.
+    // ------------------------------------------------------------ epilogue (prefill_tile.cuh)
     const int row = (warp & 3) * 32 + lane;
     const int et = threadIdx.x - EPI_WARP0 * 32;
     const uint32_t o_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + O_COL;
+    auto release_o = [&]() {
+      if (lane == 0) mbar_arrive(o_free);
+    };
     bool ok = true;
     TileWalk walk;
     WorkTile t;
-    for (int k = 0; walk.next(p, t); ++k) {
-      const int tb = k & 1;
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&l_full[tb], (k >> 1) & 1));
-      const float* xt = xl + tb * 2 * 128;
-      const float l = xt[row];
-      const float m_row = xt[128 + row];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&l_empty[tb]);
-      const float inv_l = 1.f / l;
-      const uint64_t il2 = f2_pack(inv_l, inv_l);
-      if (p.lse != nullptr && t.qt * BM + row < t.len)
-        p.lse[(static_cast<size_t>(t.z) * p.Hq + t.hq) * p.S + t.base + t.qt * BM + row] = m_row * p.scale + logf(l);
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_full, k & 1));
-      tc_fence_after();
-      const bool rowwise = p.cu_seqlens != nullptr && t.qt * BM + BM > t.len;
-      // O in groups of OGRP columns (all of it for d <= 128): bf16 pairs after the division by l
-#pragma unroll 1
-      for (int g0 = 0; g0 < D; g0 += L::OGRP) {
-        uint32_t ob[L::OGRP / 2];
-#pragma unroll
-        for (int c4 = 0; c4 < L::OGRP / 32; ++c4) {
-          uint32_t r[32];
-          tmem_ld32(o_row + g0 + c4 * 32, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-          {
-            float o0, o1;
-            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])), il2), o0, o1);
-            ob[c4 * 16 + c] = pack_bf16x2(o0, o1);
-          }
-        }
-        if (g0 + L::OGRP == D) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(o_free);  // the next tile's first P.V may overwrite O now
-        }
-        if (rowwise) {
-          if (t.qt * BM + row < t.len) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
-                                                  (static_cast<size_t>(t.base + t.qt * BM + row) * p.Hq + t.hq) * D +
-                                                  g0);
-#pragma unroll
-            for (int u = 0; u < L::OGRP / 8; ++u)
-              dst[u] = make_uint4(ob[4 * u], ob[4 * u + 1], ob[4 * u + 2], ob[4 * u + 3]);
-          }
-          continue;
-        }
-        uint8_t* line = sO + row * PANEL_ROW;
-#pragma unroll
-        for (int c = 0; c < L::OGRP / 64; ++c) {
-          if (et == 0) tma_store_wait_read0();  // the previous panel's store has read the staging buffer
-          named_barrier_sync(2, 128);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint4 w = make_uint4(ob[32 * c + 4 * u], ob[32 * c + 4 * u + 1], ob[32 * c + 4 * u + 2],
-                                       ob[32 * c + 4 * u + 3]);
-            *reinterpret_cast<uint4*>(line + ((u ^ (row & 7)) << 4)) = w;
-          }
-          fence_proxy_async_smem();
-          named_barrier_sync(2, 128);
-          if (et == 0) {
-            tma_store_3d(&tm_o, sO, t.hq * D + g0 + c * 64, t.base + t.qt * BM, t.z);
-            tma_store_commit();
-          }
-        }
-      }
-    }
+    for (int k = 0; walk.next(p, t); ++k)
+      pf::epilogue_tile<D, L::OGRP>(p, t, k, row, et, lane, o_row, xl, l_full, l_empty, o_full, sO, &tm_o, release_o,
+                                   ok);
     if (!ok) set_error(&g_prefill_status, kDevWaitTimeout);
     if (et == 0) tma_store_wait0();
   }
