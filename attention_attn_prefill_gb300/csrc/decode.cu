@@ -141,6 +141,143 @@ __device__ __forceinline__ void emu_group_pages(const DecodeParams& p, int L, in
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
+// This lane's rows of the 16-row tiles (query heads): a = lane/4, b = lane/4 + 8.
+template <int D>
+struct WarpRows {
+  float m_a, m_b;       // raw-score maxima that o and l refer to
+  float l_a, l_b;       // this lane's shares of the row sums
+  float o[D / 8][4];    // unnormalised output, m16n8 accumulator layout
+  __device__ __forceinline__ void reset() {
+    m_a = m_b = -INFINITY;
+    l_a = l_b = 0.f;
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  }
+};
+
+// ldmatrix row addresses of this lane: Q (A operand), K panels (B, as stored), V panels (B, transposed).
+struct FragRows {
+  int a_row, a_colh, kb_tok, kb_colh, vb_tok, vb_colh;
+  __device__ __forceinline__ explicit FragRows(int lane)
+      : a_row(((lane >> 3) & 1) * 8 + (lane & 7)),
+        a_colh((lane >> 4) * 8),
+        kb_tok((lane >> 4) * 8 + (lane & 7)),
+        kb_colh(((lane >> 3) & 1) * 8),
+        vb_tok(((lane >> 3) & 1) * 8 + (lane & 7)),
+        vb_colh((lane >> 4) * 8) {}
+};
+
+// One 16-token page, already in shared memory (K, then V, as 16 x 128 B swizzled panels), for the
+// 16 query rows of a warp: S = Q K^T, masking of the tokens past the sequence (`valid` of them are
+// real), the online softmax and O += P V.  Q comes from registers (qa, d <= 128) or from the swizzled
+// rows at q_base.  `first`: the page starts the rows' state.  exact_max: every increase of a row's
+// max rescales (else only past 2^8); bf16_sum: the row sums add the bf16-rounded weights that P V
+// uses (else the unrounded ones).
+template <int D, bool Q_IN_REGS>
+__device__ __forceinline__ void decode_page(uint8_t* st, int valid, bool first, bool exact_max, bool bf16_sum,
+                                            const uint32_t (&qa)[Q_IN_REGS ? D / 16 : 1][4], uint32_t q_base,
+                                            const FragRows& fr, float c2, int lane, WarpRows<D>& w) {
+  constexpr int KV_BYTES = (D / 64) * PANEL_BYTES;
+  const uint32_t k_base = smem_u32(st);
+  const uint32_t v_base = k_base + KV_BYTES;
+  if (valid < PAGE) {
+    // zero the V rows past the end of the sequence: P is 0 there, but 0 * NaN would not be
+    for (int i = lane; i < (PAGE - valid) * (D / 8); i += 32) {
+      const int r = valid + i / (D / 8);
+      const int x = (i % (D / 8)) * 8;
+      *reinterpret_cast<uint4*>(st + KV_BYTES + panel_off(r, x)) = make_uint4(0, 0, 0, 0);
+    }
+    __syncwarp();
+  }
+  // ---- S = Q K^T (16 heads x 16 tokens)
+  float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    uint32_t a[4];
+    if constexpr (Q_IN_REGS) {
+      a[0] = qa[kk][0]; a[1] = qa[kk][1]; a[2] = qa[kk][2]; a[3] = qa[kk][3];
+    } else {
+      const int x = kk * 16 + fr.a_colh;
+      ldsm_x4(q_base + fr.a_row * (D * 2) + (((x >> 3) ^ (fr.a_row & 7)) << 4), a[0], a[1], a[2], a[3]);
+    }
+    uint32_t b0, b1, b2, b3;
+    ldsm_x4(k_base + panel_off(fr.kb_tok, kk * 16 + fr.kb_colh), b0, b1, b2, b3);
+    mma_bf16(sacc[0], a, b0, b1);
+    mma_bf16(sacc[1], a, b2, b3);
+  }
+  // ---- mask tokens past seq_len (also hides NaN keys there)
+  const int colq = 2 * (lane & 3);
+#pragma unroll
+  for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (nb * 8 + colq + (e & 1) >= valid) sacc[nb][e] = -INFINITY;
+  // ---- online softmax, rows a = lane/4 and b = lane/4 + 8
+  float mx_a = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
+  float mx_b = fmaxf(fmaxf(sacc[0][2], sacc[0][3]), fmaxf(sacc[1][2], sacc[1][3]));
+  mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+  mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+  mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+  mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+  float al_a = 1.f, al_b = 1.f;
+  bool rs = false;
+  if (first) {
+    w.m_a = mx_a;
+    w.m_b = mx_b;
+  } else {
+    if (exact_max ? mx_a > w.m_a : (mx_a - w.m_a) * c2 > RESCALE_LOG2_THRESHOLD) {
+      al_a = ex2_approx((w.m_a - mx_a) * c2);
+      w.l_a *= al_a;
+      w.m_a = mx_a;
+      rs = true;
+    }
+    if (exact_max ? mx_b > w.m_b : (mx_b - w.m_b) * c2 > RESCALE_LOG2_THRESHOLD) {
+      al_b = ex2_approx((w.m_b - mx_b) * c2);
+      w.l_b *= al_b;
+      w.m_b = mx_b;
+      rs = true;
+    }
+  }
+  if (__any_sync(0xffffffffu, rs)) {
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      w.o[i][0] *= al_a; w.o[i][1] *= al_a;
+      w.o[i][2] *= al_b; w.o[i][3] *= al_b;
+    }
+  }
+  const float mb_a = w.m_a * c2, mb_b = w.m_b * c2;
+  float pr[2][4];
+#pragma unroll
+  for (int nb = 0; nb < 2; ++nb) {
+    pr[nb][0] = ex2_approx(fmaf(sacc[nb][0], c2, -mb_a));
+    pr[nb][1] = ex2_approx(fmaf(sacc[nb][1], c2, -mb_a));
+    pr[nb][2] = ex2_approx(fmaf(sacc[nb][2], c2, -mb_b));
+    pr[nb][3] = ex2_approx(fmaf(sacc[nb][3], c2, -mb_b));
+    if (!bf16_sum) {
+      w.l_a += pr[nb][0] + pr[nb][1];
+      w.l_b += pr[nb][2] + pr[nb][3];
+    }
+  }
+  uint32_t pa[4];
+  pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+  pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+  pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+  pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+  if (bf16_sum) {
+    w.l_a += (bf16_lo(pa[0]) + bf16_hi(pa[0])) + (bf16_lo(pa[2]) + bf16_hi(pa[2]));
+    w.l_b += (bf16_lo(pa[1]) + bf16_hi(pa[1])) + (bf16_lo(pa[3]) + bf16_hi(pa[3]));
+  }
+  // ---- O += P V
+#pragma unroll
+  for (int nb = 0; nb < D / 8; nb += 2) {
+    uint32_t b0, b1, b2, b3;
+    ldsm_x4_t(v_base + panel_off(fr.vb_tok, nb * 8 + fr.vb_colh), b0, b1, b2, b3);
+    mma_bf16(w.o[nb], pa, b0, b1);
+    mma_bf16(w.o[nb + 1], pa, b2, b3);
+  }
+  __syncwarp();
+}
+
 // EMU: the variant that reproduces another backend's decode numerics (p.emu): its group
 // geometry, an exact running max (every increase rescales), XQA's bf16 weights in the sum,
 // and the backend's stored value (normalised or not, f32 or bf16-rounded).  Always writes partials.
@@ -229,31 +366,20 @@ __global__ void __launch_bounds__(NW * 32)
   __syncwarp();
 
   const uint32_t q_base = smem_u32(sQ);
-  // ldmatrix row addresses for the A (Q) fragments: matrix mi = lane/8
-  const int a_row = ((lane >> 3) & 1) * 8 + (lane & 7);
-  const int a_colh = (lane >> 4) * 8;  // 0 or 8 within the 16-wide k step
+  const FragRows fr(lane);
   uint32_t qa[Q_IN_REGS ? D / 16 : 1][4];
   if constexpr (Q_IN_REGS) {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      const int x = kk * 16 + a_colh;
-      ldsm_x4(q_base + a_row * (D * 2) + (((x >> 3) ^ (a_row & 7)) << 4), qa[kk][0], qa[kk][1], qa[kk][2],
+      const int x = kk * 16 + fr.a_colh;
+      ldsm_x4(q_base + fr.a_row * (D * 2) + (((x >> 3) ^ (fr.a_row & 7)) << 4), qa[kk][0], qa[kk][1], qa[kk][2],
               qa[kk][3]);
     }
   }
 
   const float c2 = p.scale_log2;
-  float m_a = -INFINITY, m_b = -INFINITY;  // rows lane/4 and lane/4 + 8, raw-score units
-  float l_a = 0.f, l_b = 0.f;              // this lane's share of the row sums
-  float oacc[D / 8][4];
-#pragma unroll
-  for (int i = 0; i < D / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
-
-  // B-fragment row addresses within a K panel (non-transposed) and a V panel (transposed)
-  const int kb_tok = (lane >> 4) * 8 + (lane & 7);
-  const int kb_colh = ((lane >> 3) & 1) * 8;
-  const int vb_tok = ((lane >> 3) & 1) * 8 + (lane & 7);
-  const int vb_colh = (lane >> 4) * 8;
+  WarpRows<D> w;
+  w.reset();
 
   bool ok = true;
   int consumed = 0;
@@ -262,106 +388,9 @@ __global__ void __launch_bounds__(NW * 32)
     if (!ok) break;
     consumed = k + 1;
     uint8_t* st = my_stages + (k % NS) * L::STAGE_BYTES;
-    const uint32_t k_base = smem_u32(st);
-    const uint32_t v_base = k_base + L::KV_BYTES;
     const int tok0 = page_at(wstart + k * wstep) * PAGE;
     const int valid = seq_len - tok0 < PAGE ? seq_len - tok0 : PAGE;
-    if (valid < PAGE) {
-      // zero the V rows past the end of the sequence: P is 0 there, but 0 * NaN would not be
-      for (int i = lane; i < (PAGE - valid) * (D / 8); i += 32) {
-        const int r = valid + i / (D / 8);
-        const int x = (i % (D / 8)) * 8;
-        *reinterpret_cast<uint4*>(st + L::KV_BYTES + panel_off(r, x)) = make_uint4(0, 0, 0, 0);
-      }
-      __syncwarp();
-    }
-    // ---- S = Q K^T (16 heads x 16 tokens)
-    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      uint32_t a[4];
-      if constexpr (Q_IN_REGS) {
-        a[0] = qa[kk][0]; a[1] = qa[kk][1]; a[2] = qa[kk][2]; a[3] = qa[kk][3];
-      } else {
-        const int x = kk * 16 + a_colh;
-        ldsm_x4(q_base + a_row * (D * 2) + (((x >> 3) ^ (a_row & 7)) << 4), a[0], a[1], a[2], a[3]);
-      }
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(k_base + panel_off(kb_tok, kk * 16 + kb_colh), b0, b1, b2, b3);
-      mma_bf16(sacc[0], a, b0, b1);
-      mma_bf16(sacc[1], a, b2, b3);
-    }
-    // ---- mask tokens past seq_len (also hides NaN keys there)
-    const int colq = 2 * (lane & 3);
-#pragma unroll
-    for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (nb * 8 + colq + (e & 1) >= valid) sacc[nb][e] = -INFINITY;
-    // ---- online softmax, rows a = lane/4 and b = lane/4 + 8
-    float mx_a = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
-    float mx_b = fmaxf(fmaxf(sacc[0][2], sacc[0][3]), fmaxf(sacc[1][2], sacc[1][3]));
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-    float al_a = 1.f, al_b = 1.f;
-    bool rs = false;
-    if (k == 0) {
-      m_a = mx_a;
-      m_b = mx_b;
-    } else {
-      if (EMU ? mx_a > m_a : (mx_a - m_a) * c2 > RESCALE_LOG2_THRESHOLD) {
-        al_a = ex2_approx((m_a - mx_a) * c2);
-        l_a *= al_a;
-        m_a = mx_a;
-        rs = true;
-      }
-      if (EMU ? mx_b > m_b : (mx_b - m_b) * c2 > RESCALE_LOG2_THRESHOLD) {
-        al_b = ex2_approx((m_b - mx_b) * c2);
-        l_b *= al_b;
-        m_b = mx_b;
-        rs = true;
-      }
-    }
-    if (__any_sync(0xffffffffu, rs)) {
-#pragma unroll
-      for (int i = 0; i < D / 8; ++i) {
-        oacc[i][0] *= al_a; oacc[i][1] *= al_a;
-        oacc[i][2] *= al_b; oacc[i][3] *= al_b;
-      }
-    }
-    const float mb_a = m_a * c2, mb_b = m_b * c2;
-    float pr[2][4];
-#pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
-      pr[nb][0] = ex2_approx(fmaf(sacc[nb][0], c2, -mb_a));
-      pr[nb][1] = ex2_approx(fmaf(sacc[nb][1], c2, -mb_a));
-      pr[nb][2] = ex2_approx(fmaf(sacc[nb][2], c2, -mb_b));
-      pr[nb][3] = ex2_approx(fmaf(sacc[nb][3], c2, -mb_b));
-      if (!xqa_sum) {
-        l_a += pr[nb][0] + pr[nb][1];
-        l_b += pr[nb][2] + pr[nb][3];
-      }
-    }
-    uint32_t pa[4];
-    pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
-    pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
-    pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
-    pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
-    if (xqa_sum) {
-      l_a += (bf16_lo(pa[0]) + bf16_hi(pa[0])) + (bf16_lo(pa[2]) + bf16_hi(pa[2]));
-      l_b += (bf16_lo(pa[1]) + bf16_hi(pa[1])) + (bf16_lo(pa[3]) + bf16_hi(pa[3]));
-    }
-    // ---- O += P V
-#pragma unroll
-    for (int nb = 0; nb < D / 8; nb += 2) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(v_base + panel_off(vb_tok, nb * 8 + vb_colh), b0, b1, b2, b3);
-      mma_bf16(oacc[nb], pa, b0, b1);
-      mma_bf16(oacc[nb + 1], pa, b2, b3);
-    }
-    __syncwarp();
+    decode_page<D, Q_IN_REGS>(st, valid, k == 0, EMU, xqa_sum, qa, q_base, fr, c2, lane, w);
     if (lane == 0 && k + NS < n_my) {
       fence_proxy_async_smem();
       issue(k + NS);
@@ -377,26 +406,26 @@ __global__ void __launch_bounds__(NW * 32)
   __syncwarp();
 
   // ---- per-warp record: m (log2-scaled), l, unnormalised o, rows < 16
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+  w.l_a += __shfl_xor_sync(0xffffffffu, w.l_a, 1);
+  w.l_a += __shfl_xor_sync(0xffffffffu, w.l_a, 2);
+  w.l_b += __shfl_xor_sync(0xffffffffu, w.l_b, 1);
+  w.l_b += __shfl_xor_sync(0xffffffffu, w.l_b, 2);
   float* rec_m = reinterpret_cast<float*>(my_stages);
   float* rec_l = rec_m + 16;
   float* rec_o = rec_m + 32;
   const int ra = lane >> 2, rb = ra + 8;
   if ((lane & 3) == 0) {
     const bool any = n_my > 0;
-    rec_m[ra] = any ? m_a * c2 : -INFINITY;
-    rec_m[rb] = any ? m_b * c2 : -INFINITY;
-    rec_l[ra] = any ? l_a : 0.f;
-    rec_l[rb] = any ? l_b : 0.f;
+    rec_m[ra] = any ? w.m_a * c2 : -INFINITY;
+    rec_m[rb] = any ? w.m_b * c2 : -INFINITY;
+    rec_l[ra] = any ? w.l_a : 0.f;
+    rec_l[rb] = any ? w.l_b : 0.f;
   }
 #pragma unroll
   for (int nb = 0; nb < D / 8; ++nb) {
     const int x = nb * 8 + 2 * (lane & 3);
-    *reinterpret_cast<float2*>(rec_o + ra * D + x) = make_float2(oacc[nb][0], oacc[nb][1]);
-    *reinterpret_cast<float2*>(rec_o + rb * D + x) = make_float2(oacc[nb][2], oacc[nb][3]);
+    *reinterpret_cast<float2*>(rec_o + ra * D + x) = make_float2(w.o[nb][0], w.o[nb][1]);
+    *reinterpret_cast<float2*>(rec_o + rb * D + x) = make_float2(w.o[nb][2], w.o[nb][3]);
   }
   __syncthreads();
 
@@ -664,24 +693,19 @@ __global__ void __launch_bounds__(NW * 32)
     for (int k = 0; k < npg && k < NS; ++k) issue(k);
   __syncwarp();
 
-  const int a_row = ((lane >> 3) & 1) * 8 + (lane & 7);
-  const int a_colh = (lane >> 4) * 8;
-  const int kb_tok = (lane >> 4) * 8 + (lane & 7);
-  const int kb_colh = ((lane >> 3) & 1) * 8;
-  const int vb_tok = ((lane >> 3) & 1) * 8 + (lane & 7);
-  const int vb_colh = (lane >> 4) * 8;
+  const FragRows fr(lane);
   const float c2 = p.scale_log2;
   const size_t R = static_cast<size_t>(p.warps_total) + static_cast<size_t>(p.Hkv) * N;
 
   uint32_t qa[Q_IN_REGS ? D / 16 : 1][4];
-  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-  float oacc[D / 8][4];
+  WarpRows<D> w;
+  w.reset();
   int seg_g = -1, seg_n = -1, seg_len = 0;
   bool first = true;
 
   // finish the current (g, n) segment: partial record = normalised o, max (natural units), sum
   auto flush = [&]() {
-    float la = l_a, lb = l_b;
+    float la = w.l_a, lb = w.l_b;
     la += __shfl_xor_sync(0xffffffffu, la, 1);
     la += __shfl_xor_sync(0xffffffffu, la, 2);
     lb += __shfl_xor_sync(0xffffffffu, lb, 1);
@@ -693,14 +717,14 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
     for (int nb = 0; nb < D / 8; ++nb) {
       const int x = nb * 8 + 2 * (lane & 3);
-      if (ra < G) *reinterpret_cast<float2*>(ro + ra * D + x) = make_float2(oacc[nb][0] * ia, oacc[nb][1] * ia);
-      if (rb < G) *reinterpret_cast<float2*>(ro + rb * D + x) = make_float2(oacc[nb][2] * ib, oacc[nb][3] * ib);
+      if (ra < G) *reinterpret_cast<float2*>(ro + ra * D + x) = make_float2(w.o[nb][0] * ia, w.o[nb][1] * ia);
+      if (rb < G) *reinterpret_cast<float2*>(ro + rb * D + x) = make_float2(w.o[nb][2] * ib, w.o[nb][3] * ib);
     }
     if ((lane & 3) == 0) {
       float* rm = p.rec + R * G * D + idx * G;
       float* rl = rm + R * G;
-      if (ra < G) { rm[ra] = la > 0.f ? m_a * p.scale : -INFINITY; rl[ra] = la; }
-      if (rb < G) { rm[rb] = lb > 0.f ? m_b * p.scale : -INFINITY; rl[rb] = lb; }
+      if (ra < G) { rm[ra] = la > 0.f ? w.m_a * p.scale : -INFINITY; rl[ra] = la; }
+      if (rb < G) { rm[rb] = lb > 0.f ? w.m_b * p.scale : -INFINITY; rl[rb] = lb; }
     }
   };
 
@@ -728,109 +752,19 @@ __global__ void __launch_bounds__(NW * 32)
       if constexpr (Q_IN_REGS) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const int x = kk * 16 + a_colh;
-          ldsm_x4(q_base + a_row * (D * 2) + (((x >> 3) ^ (a_row & 7)) << 4), qa[kk][0], qa[kk][1], qa[kk][2],
+          const int x = kk * 16 + fr.a_colh;
+          ldsm_x4(q_base + fr.a_row * (D * 2) + (((x >> 3) ^ (fr.a_row & 7)) << 4), qa[kk][0], qa[kk][1], qa[kk][2],
                   qa[kk][3]);
         }
       }
-      m_a = m_b = -INFINITY;
-      l_a = l_b = 0.f;
-#pragma unroll
-      for (int i = 0; i < D / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+      w.reset();
       first = true;
     }
     uint8_t* st = my_stages + (k % NS) * L::STAGE_BYTES;
-    const uint32_t k_base = smem_u32(st);
-    const uint32_t v_base = k_base + L::KV_BYTES;
     const int tok0 = cur.p * PAGE;
     const int valid = seg_len - tok0 < PAGE ? seg_len - tok0 : PAGE;
-    if (valid < PAGE) {
-      for (int i = lane; i < (PAGE - valid) * (D / 8); i += 32) {
-        const int r = valid + i / (D / 8);
-        const int x = (i % (D / 8)) * 8;
-        *reinterpret_cast<uint4*>(st + L::KV_BYTES + panel_off(r, x)) = make_uint4(0, 0, 0, 0);
-      }
-      __syncwarp();
-    }
-    // ---- S = Q K^T (16 heads x 16 tokens)
-    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      uint32_t a[4];
-      if constexpr (Q_IN_REGS) {
-        a[0] = qa[kk][0]; a[1] = qa[kk][1]; a[2] = qa[kk][2]; a[3] = qa[kk][3];
-      } else {
-        const int x = kk * 16 + a_colh;
-        ldsm_x4(q_base + a_row * (D * 2) + (((x >> 3) ^ (a_row & 7)) << 4), a[0], a[1], a[2], a[3]);
-      }
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(k_base + panel_off(kb_tok, kk * 16 + kb_colh), b0, b1, b2, b3);
-      mma_bf16(sacc[0], a, b0, b1);
-      mma_bf16(sacc[1], a, b2, b3);
-    }
-    const int colq = 2 * (lane & 3);
-#pragma unroll
-    for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (nb * 8 + colq + (e & 1) >= valid) sacc[nb][e] = -INFINITY;
-    float mx_a = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
-    float mx_b = fmaxf(fmaxf(sacc[0][2], sacc[0][3]), fmaxf(sacc[1][2], sacc[1][3]));
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-    float al_a = 1.f, al_b = 1.f;
-    bool rs = false;
-    if (first) {
-      m_a = mx_a;
-      m_b = mx_b;
-      first = false;
-    } else {
-      if ((mx_a - m_a) * c2 > RESCALE_LOG2_THRESHOLD) {
-        al_a = ex2_approx((m_a - mx_a) * c2);
-        l_a *= al_a;
-        m_a = mx_a;
-        rs = true;
-      }
-      if ((mx_b - m_b) * c2 > RESCALE_LOG2_THRESHOLD) {
-        al_b = ex2_approx((m_b - mx_b) * c2);
-        l_b *= al_b;
-        m_b = mx_b;
-        rs = true;
-      }
-    }
-    if (__any_sync(0xffffffffu, rs)) {
-#pragma unroll
-      for (int i = 0; i < D / 8; ++i) {
-        oacc[i][0] *= al_a; oacc[i][1] *= al_a;
-        oacc[i][2] *= al_b; oacc[i][3] *= al_b;
-      }
-    }
-    const float mb_a = m_a * c2, mb_b = m_b * c2;
-    float pr[2][4];
-#pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
-      pr[nb][0] = ex2_approx(fmaf(sacc[nb][0], c2, -mb_a));
-      pr[nb][1] = ex2_approx(fmaf(sacc[nb][1], c2, -mb_a));
-      pr[nb][2] = ex2_approx(fmaf(sacc[nb][2], c2, -mb_b));
-      pr[nb][3] = ex2_approx(fmaf(sacc[nb][3], c2, -mb_b));
-      l_a += pr[nb][0] + pr[nb][1];
-      l_b += pr[nb][2] + pr[nb][3];
-    }
-    uint32_t pa[4];
-    pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
-    pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
-    pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
-    pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
-#pragma unroll
-    for (int nb = 0; nb < D / 8; nb += 2) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(v_base + panel_off(vb_tok, nb * 8 + vb_colh), b0, b1, b2, b3);
-      mma_bf16(oacc[nb], pa, b0, b1);
-      mma_bf16(oacc[nb + 1], pa, b2, b3);
-    }
-    __syncwarp();
+    decode_page<D, Q_IN_REGS>(st, valid, first, false, false, qa, q_base, fr, c2, lane, w);
+    first = false;
     if (lane == 0 && k + NS < npg) {
       fence_proxy_async_smem();
       issue(k + NS);
