@@ -18,9 +18,11 @@
 //
 // One CTA per row: the per-slot factors of a chunk of slots are computed in parallel (the
 // running maxima of the ordered merge by a warp-wide max scan) and kept in shared memory; then
-// every thread runs the sequential accumulation for its own NC consecutive output components,
-// with the stored values of the next U slots loaded into registers while the current U are added,
-// so that the loads overlap while the additions stay in slot order.
+// every thread runs the sequential accumulation for its own NC consecutive output components.
+// The stored values reach the additions ahead of them, so that the loads overlap while the
+// additions stay in slot order: either the next U slots are loaded into registers while the
+// current U are added, or (d of 128 or 256) a ring of NST shared-memory stages of SB slots each is
+// filled with 16-byte cp.async copies, NST - 1 stages ahead.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -42,8 +44,21 @@ __device__ __forceinline__ float bf16_rn(float x) { return __bfloat162float(__fl
 // FA2's group statistic: m + log l, each step rounded.
 __device__ __forceinline__ float log_sum(float m, float l) { return __fadd_rn(m, log_rn(l)); }
 
-// NC: output components per thread (d <= MT * NC); U: slots whose values are loaded ahead.
-template <int NC, int U>
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// NC: output components per thread (d <= MT * NC).  NST == 0: the next U slots' values are loaded
+// into registers; NST > 0: a ring of NST stages of SB slots in dynamic shared memory (d == MT * NC,
+// part_o 16-byte aligned).
+template <int NC, int U, int NST, int SB>
 __global__ void __launch_bounds__(MT) merge_emulated_kernel(const float* __restrict__ part_o,
                                                             const float* __restrict__ part_m,
                                                             const float* __restrict__ part_l, int splits, int d,
@@ -133,47 +148,85 @@ __global__ void __launch_bounds__(MT) merge_emulated_kernel(const float* __restr
       }
     }
     __syncthreads();
-    // the groups in slot order, each thread on its own components; the values of the next U slots
-    // are loaded while the current U are added
-    auto load_batch = [&](float (&v)[U][NC], int j0) {
+    // the groups in slot order, each thread on its own components
+    auto add = [&](int j, const float (&v)[NC]) {
+      const float l = f_l[j];
+      if (!(l > 0.f)) return;
+      any = true;
+      if (mode == kEmuTrt) {
+        const float a = f_a[j], b = f_b[j];
+        wsum = __fadd_rn(__fmul_rn(wsum, a), __fmul_rn(l, b));
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        // indices clamped into the row, so that every load is in bounds; the value is dropped there
-        const int j = j0 + u < n ? j0 + u : n - 1;
-        const float* src = po + static_cast<size_t>(base + j) * d;
+        for (int c = 0; c < NC; ++c) acc[c] = __fadd_rn(__fmul_rn(acc[c], a), __fmul_rn(bf16_rn(v[c]), b));
+      } else {
+        const float w = f_a[j];
+        wsum = __fadd_rn(wsum, mode == kEmuTriton ? __fmul_rn(l, w) : w);
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-          const int x = x0 + c < d ? x0 + c : d - 1;
-          v[u][c] = (j0 + u < n && x0 + c < d) ? src[x] : 0.f;
-        }
+        for (int c = 0; c < NC; ++c) acc[c] = __fadd_rn(acc[c], __fmul_rn(v[c], w));
       }
     };
-    float cur[U][NC], nxt[U][NC];
-    load_batch(cur, 0);
-    for (int j0 = 0; j0 < n; j0 += U) {
-      if (j0 + U < n) load_batch(nxt, j0 + U);
+    if constexpr (NST == 0) {
+      // the values of the next U slots are loaded while the current U are added
+      auto load_batch = [&](float (&v)[U][NC], int j0) {
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int j = j0 + u;
-        const float l = j < n ? f_l[j] : 0.f;
-        if (!(l > 0.f)) continue;
-        any = true;
-        if (mode == kEmuTrt) {
-          const float a = f_a[j], b = f_b[j];
-          wsum = __fadd_rn(__fmul_rn(wsum, a), __fmul_rn(l, b));
+        for (int u = 0; u < U; ++u) {
+          // indices clamped into the row, so that every load is in bounds; the value is dropped there
+          const int j = j0 + u < n ? j0 + u : n - 1;
+          const float* src = po + static_cast<size_t>(base + j) * d;
 #pragma unroll
-          for (int c = 0; c < NC; ++c) acc[c] = __fadd_rn(__fmul_rn(acc[c], a), __fmul_rn(bf16_rn(cur[u][c]), b));
-        } else {
-          const float w = f_a[j];
-          wsum = __fadd_rn(wsum, mode == kEmuTriton ? __fmul_rn(l, w) : w);
-#pragma unroll
-          for (int c = 0; c < NC; ++c) acc[c] = __fadd_rn(acc[c], __fmul_rn(cur[u][c], w));
+          for (int c = 0; c < NC; ++c) {
+            const int x = x0 + c < d ? x0 + c : d - 1;
+            v[u][c] = (j0 + u < n && x0 + c < d) ? src[x] : 0.f;
+          }
         }
+      };
+      float cur[U][NC], nxt[U][NC];
+      load_batch(cur, 0);
+      for (int j0 = 0; j0 < n; j0 += U) {
+        if (j0 + U < n) load_batch(nxt, j0 + U);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (j0 + u < n) add(j0 + u, cur[u]);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int c = 0; c < NC; ++c) cur[u][c] = nxt[u][c];
       }
+    } else {
+      // stage t holds slots t * SB .. of this chunk in buffer t % NST; NST - 1 stages are in flight
+      extern __shared__ float4 ring4[];
+      float* ring = reinterpret_cast<float*>(ring4);
+      constexpr int D = MT * NC;
+      const int nst = (n + SB - 1) / SB;
+      auto issue = [&](int t) {
+        const int j0 = t * SB;
+        const int cnt = n - j0 < SB ? n - j0 : SB;
+        const float* src = po + static_cast<size_t>(base + j0) * D;
+        float* dst = ring + (t % NST) * (SB * D);
+        for (int q = tid; q < cnt * (D / 4); q += MT) cp_async16(dst + 4 * q, src + 4 * q);
+      };
 #pragma unroll
-      for (int u = 0; u < U; ++u)
+      for (int t = 0; t < NST - 1; ++t) {
+        if (t < nst) issue(t);
+        cp_async_commit();
+      }
+      for (int t = 0; t < nst; ++t) {
+        cp_async_wait<NST - 2>();  // this thread's copies of stage t have landed ...
+        __syncthreads();           // ... and everyone's
+        const float* buf = ring + (t % NST) * (SB * D) + x0;
+        const int j0 = t * SB;
+        const int cnt = n - j0 < SB ? n - j0 : SB;
+        for (int u = 0; u < cnt; ++u) {  // (measured: unrolling this loop makes it slower)
+          float v[NC];
 #pragma unroll
-        for (int c = 0; c < NC; ++c) cur[u][c] = nxt[u][c];
+          for (int c = 0; c < NC; ++c) v[c] = buf[u * D + c];
+          add(j0 + u, v);
+        }
+        __syncthreads();  // buffer t % NST is free again
+        if (t + NST - 1 < nst) issue(t + NST - 1);
+        cp_async_commit();  // an empty group past the end keeps the count uniform
+      }
+      cp_async_wait<0>();
     }
     __syncthreads();
   }
@@ -196,10 +249,21 @@ cudaError_t merge_emulated_launch(int numerics, const float* part_o, const float
                                   int rows, int splits, int d, float* o32, void* o, float* lse, cudaStream_t stream) {
   if (numerics < kEmuTriton || numerics > kEmuTrt || rows < 1 || splits < 1 || d < 1 || d > MAX_D)
     return cudaErrorInvalidValue;
-  void (*kern)(const float*, const float*, const float*, int, int, int, float*, __nv_bfloat16*, float*) =
-      d <= MT ? merge_emulated_kernel<1, 16>
-              : d <= 2 * MT ? merge_emulated_kernel<2, 32>
-                            : d <= 4 * MT ? merge_emulated_kernel<4, 16> : merge_emulated_kernel<8, 8>;
+  using Kern = void (*)(const float*, const float*, const float*, int, int, int, float*, __nv_bfloat16*, float*);
+  Kern kern = d <= MT ? merge_emulated_kernel<1, 16, 0, 0>
+                      : d <= 2 * MT ? merge_emulated_kernel<2, 32, 0, 0>
+                                    : d <= 4 * MT ? merge_emulated_kernel<4, 16, 0, 0> : merge_emulated_kernel<8, 8, 0, 0>;
+  // staged loads for rows of many groups at the head dims of the decode kernels, when the stored values
+  // are 16-byte aligned (with fewer groups, a row has too little to pipeline and the ring's shared
+  // memory only leaves fewer rows in flight)
+  int smem = 0;
+  if ((d == 128 || d == 256) && splits >= 96 && (reinterpret_cast<uintptr_t>(part_o) & 15u) == 0) {
+    constexpr int NST = 6, SB = 16;
+    smem = NST * SB * d * static_cast<int>(sizeof(float));
+    kern = d == 128 ? merge_emulated_kernel<1, 1, NST, SB> : merge_emulated_kernel<2, 1, NST, SB>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
   // programmatic dependent launch: the partials may come from the kernel just before it
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -207,6 +271,7 @@ cudaError_t merge_emulated_launch(int numerics, const float* part_o, const float
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(rows);
   cfg.blockDim = dim3(MT);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
