@@ -58,15 +58,22 @@ __device__ __forceinline__ void softmax_step(const PrefillParams& p, const WorkT
     lim_a = min(lim_a, qa - key0);
     lim_b = min(lim_b, qb - key0);
   }
+  // 64-key steps (d = 256) skip the groups of 8 columns past the last visible column of every row
+  // of this warp: their weights are 0 without masking or exponentials.  (With 128-key steps the
+  // extra test measured slower, so those steps mask every column.)
+  constexpr bool SKIP = (BN == 64);
+  const int lim_w = SKIP ? __reduce_max_sync(0xffffffffu, max(lim_a, lim_b)) : BN - 1;
   if (min(lim_a, lim_b) < BN - 1) {
 #pragma unroll
-    for (int i = 0; i < NG; ++i)
+    for (int i = 0; i < NG; ++i) {
+      if (SKIP && 8 * i > lim_w) continue;
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int c = 8 * i + cq + e;
         if (c > lim_a) sr[4 * i + e] = __float_as_uint(-INFINITY);
         if (c > lim_b) sr[4 * i + 2 + e] = __float_as_uint(-INFINITY);
       }
+    }
   }
   float alpha_a = 1.f, alpha_b = 1.f;
   bool rescale_o = false;
@@ -78,6 +85,7 @@ __device__ __forceinline__ void softmax_step(const PrefillParams& p, const WorkT
       float mxa = -INFINITY, mxb = -INFINITY;
 #pragma unroll
       for (int i = 0; i < NG; ++i) {
+        if (SKIP && 8 * i > lim_w) continue;
         mxa = fmax3(mxa, __uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1]));
         mxb = fmax3(mxb, __uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3]));
       }
@@ -112,6 +120,10 @@ __device__ __forceinline__ void softmax_step(const PrefillParams& p, const WorkT
     uint64_t acc_a = 0ull, acc_b = 0ull;
 #pragma unroll
     for (int i = 0; i < NG; ++i) {
+      if (SKIP && 8 * i > lim_w) {
+        pk[2 * i] = pk[2 * i + 1] = 0u;
+        continue;
+      }
       float x0, x1;
       f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1])), c2x2, nma), x0, x1);
       const float pa0 = ex2_approx(x0), pa1 = ex2_approx(x1);
