@@ -257,7 +257,8 @@ attn_status_t check_decode_args(const void* q, const void* k_cache, const void* 
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
   if (num_seqs < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_blocks_per_seq < 1 || num_blocks < 1)
     return ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;  // masked keys stay -inf only under a positive scale
+  // masked keys stay -inf only under a positive scale
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (page_size != kPage) return ATTN_ERR_UNSUPPORTED;
   if (d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
   if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;  // query heads per KV head fill at most 16 MMA rows

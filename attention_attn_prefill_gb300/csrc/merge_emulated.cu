@@ -45,9 +45,8 @@ __device__ __forceinline__ float bf16_rn(float x) { return __bfloat162float(__fl
 __device__ __forceinline__ float log_sum(float m, float l) { return __fadd_rn(m, log_rn(l)); }
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
-               "l"(gmem_src)
-               : "memory");
+  const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(gmem_src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -250,9 +249,13 @@ cudaError_t merge_emulated_launch(int numerics, const float* part_o, const float
   if (numerics < kEmuTriton || numerics > kEmuTrt || rows < 1 || splits < 1 || d < 1 || d > MAX_D)
     return cudaErrorInvalidValue;
   using Kern = void (*)(const float*, const float*, const float*, int, int, int, float*, __nv_bfloat16*, float*);
-  Kern kern = d <= MT ? merge_emulated_kernel<1, 16, 0, 0>
-                      : d <= 2 * MT ? merge_emulated_kernel<2, 32, 0, 0>
-                                    : d <= 4 * MT ? merge_emulated_kernel<4, 16, 0, 0> : merge_emulated_kernel<8, 8, 0, 0>;
+  Kern kern = merge_emulated_kernel<8, 8, 0, 0>;
+  if (d <= MT)
+    kern = merge_emulated_kernel<1, 16, 0, 0>;
+  else if (d <= 2 * MT)
+    kern = merge_emulated_kernel<2, 32, 0, 0>;
+  else if (d <= 4 * MT)
+    kern = merge_emulated_kernel<4, 16, 0, 0>;
   // staged loads for rows of many groups at the head dims of the decode kernels, when the stored values
   // are 16-byte aligned (with fewer groups, a row has too little to pipeline and the ring's shared
   // memory only leaves fewer rows in flight)
