@@ -41,7 +41,7 @@ if ROOT not in sys.path:
 import torch  # noqa: E402
 
 from workloads import (LLAMA8B, PAGED, decode_inputs_for, decode_lens_for, decode_min_bytes, make_chunked_inputs,  # noqa
-                       prefill_inputs_for)
+                       make_varlen_inputs, prefill_inputs_for)
 
 METRIC = "prefill TFLOP/s & decode KV GB/s on 1 GB300, as % of bf16 TC peak / HBM peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -458,6 +458,32 @@ def workload_table(attn, dev, stream, flush, peaks, paged_inputs, reps: int = 10
             out[f"{cfg.name} emulated {backend} ({slots} groups)"] = {
                 "GB/s": round(gbs, 1), "us": round(ms * 1e3, 1), "frac": round(gbs / peaks["hbm_gbs"], 4)}
             del ws
+    # packed sequences of mixed lengths and chunked prefill over a paged cache, Llama-8B heads
+    Hq, Hkv, d = 32, 8, 128
+    lens = [int(v) for v in torch.randint(256, 4097, (8,), generator=torch.Generator().manual_seed(12))]
+    xv = make_varlen_inputs(lens, Hq=Hq, Hkv=Hkv, d=d, seed=12)
+    vq, vk, vv, vcu = (t.to(dev) for t in (xv.q, xv.k, xv.v, xv.cu_seqlens))
+    vo = torch.empty_like(vq)
+    vl = torch.empty((Hq, vq.shape[0]), dtype=torch.float32, device=dev)
+    ms = timed(lambda: attn.prefill_varlen(vq, vk, vv, vcu, xv.max_seqlen, scale=d ** -0.5, out=vo, lse=vl,
+                                           stream=stream))
+    flops = 4.0 * Hq * d * sum(L * (L + 1) / 2 for L in lens)
+    out[f"packed prefill, 8 sequences of {min(lens)}-{max(lens)} tokens"] = {
+        "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1), "us": round(ms * 1e3, 1),
+        "frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
+    del vq, vk, vv, vo, vl
+    for n, qn, ctxn in ((4, 2048, 8192), (16, 512, 4096)):
+        xc = make_chunked_inputs([ctxn] * n, [qn] * n, Hq=Hq, Hkv=Hkv, d=d, seed=11)
+        cargs = [t.to(dev) for t in (xc.q, xc.k_cache, xc.v_cache, xc.block_table, xc.cu_seqlens_q, xc.seq_lens)]
+        co = torch.empty_like(cargs[0])
+        cl = torch.empty((Hq, xc.q.shape[0]), dtype=torch.float32, device=dev)
+        ms = timed(lambda: attn.prefill_paged(*cargs, xc.max_seqlen_q, scale=d ** -0.5, causal=True, out=co, lse=cl,
+                                              stream=stream))
+        flops = 4.0 * Hq * d * n * sum(ctxn - qn + i + 1 for i in range(qn))
+        out[f"chunked prefill, {n} x {qn} new tokens over {ctxn}-token contexts"] = {
+            "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1), "us": round(ms * 1e3, 1),
+            "frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
+        del cargs, co, cl
     out["_note"] = (f"each: mean of {reps} launches with L2 flushed before each, outside the timed region; "
                     "frac against the measured bf16 dense peak (prefill) or HBM copy (decode)")
     if attn.device_status(clear=True) != 0:
