@@ -51,6 +51,8 @@ _SIGNATURES = {
     "attn_prefill_varlen": (c_int, [c_void_p] * 6 + [c_int] * 6 + [c_float, c_int, c_void_p]),
     "attn_prefill_paged": (c_int, [c_void_p] * 8 + [c_int] * 9 + [c_float, c_int, c_void_p]),
     "attn_decode_auto_splits": (c_int, [c_int] * 4),
+    "attn_split_tokens_rule": (c_int, [c_void_p] + [c_int] * 4),
+    "attn_decode_auto_split_tokens": (c_int, [c_void_p] + [c_int] * 4),
     "attn_emulated_partitions": (c_int, [c_int] * 5),
     "attn_emulated_num_slots": (c_int, [c_int] * 4),
     "attn_emulated_workspace_bytes": (c_size_t, [c_int] * 4),
@@ -208,6 +210,26 @@ def decode_auto_splits(num_seqs: int, Hkv: int, d: int, max_blocks_per_seq: int)
     return n
 
 
+def _host_lens(seq_lens) -> tuple[ctypes.Array, int]:
+    vals = [int(x) for x in (seq_lens.tolist() if isinstance(seq_lens, torch.Tensor) else seq_lens)]
+    return (ctypes.c_int32 * max(1, len(vals)))(*vals), len(vals)
+
+
+def split_tokens_rule(seq_lens, Hkv: int, capacity: int, max_blocks_per_seq: int) -> int:
+    """Length-aware group size (host arithmetic only) for given host lengths; 0 for invalid arguments."""
+    arr, n = _host_lens(seq_lens)
+    return int(lib().attn_split_tokens_rule(ctypes.addressof(arr), n, Hkv, capacity, max_blocks_per_seq))
+
+
+def decode_auto_split_tokens(seq_lens, Hkv: int, d: int, max_blocks_per_seq: int) -> int:
+    """split_tokens the length-aware rule picks on the current device, from host lengths."""
+    arr, n = _host_lens(seq_lens)
+    t = int(lib().attn_decode_auto_split_tokens(ctypes.addressof(arr), n, Hkv, d, max_blocks_per_seq))
+    if t < 1:
+        raise AttnError(1, "attn_decode_auto_split_tokens")
+    return t
+
+
 def decode_balanced_workspace_bytes(num_seqs: int, Hq: int, Hkv: int, d: int) -> int:
     return int(lib().attn_decode_balanced_workspace_bytes(num_seqs, Hq, Hkv, d))
 
@@ -219,7 +241,8 @@ def decode_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, 
     """Paged split-KV decode: q [N,Hq,d]; caches [num_blocks,16,Hkv,d] bf16 -> (o [N,Hq,d], lse [N,Hq]).
 
     num_splits=0 with split_tokens=0 selects balanced mode (equal page shares per worker warp);
-    num_splits="auto" takes the count decode_auto_splits picks.
+    num_splits="auto" takes the count decode_auto_splits picks; split_tokens="auto" takes the group
+    size decode_auto_split_tokens picks from the lengths (read back to the host once, a device sync).
     """
     N, Hq, d = q.shape
     num_blocks, page, Hkv, dk = k_cache.shape
@@ -232,6 +255,9 @@ def decode_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, 
         scale = 1.0 / math.sqrt(d)
     if num_splits == "auto":
         num_splits = decode_auto_splits(N, Hkv, d, max_blocks)
+    if split_tokens == "auto":
+        split_tokens = decode_auto_split_tokens(seq_lens.cpu(), Hkv, d, max_blocks)
+        num_splits = 0
     if num_splits == 0 and split_tokens == 0:
         need = int(lib().attn_decode_balanced_workspace_bytes(N, Hq, Hkv, d))   # balanced mode
         if need == 0:

@@ -4,7 +4,9 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
+#include <vector>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -226,6 +228,59 @@ int attn_decode_auto_splits(int num_seqs, int Hkv, int d, int max_blocks_per_seq
   return attn_split_heuristic(num_seqs * Hkv, sms * per_sm, max_blocks_per_seq, kAutoMaxSplits);
 }
 
+int attn_split_tokens_rule(const int32_t* seq_lens, int num_seqs, int Hkv, int capacity, int max_blocks_per_seq) {
+  if (seq_lens == nullptr || num_seqs < 1 || Hkv < 1 || capacity < 1 || max_blocks_per_seq < 1) return 0;
+  const int64_t max_tokens = static_cast<int64_t>(max_blocks_per_seq) * kPage;
+  if (max_tokens > (int64_t(1) << 30)) return 0;
+  std::vector<int> pages(num_seqs);
+  int max_pages = 0;
+  int64_t total = 0;
+  for (int n = 0; n < num_seqs; ++n) {
+    const int64_t L = std::min<int64_t>(std::max<int64_t>(seq_lens[n], 0), max_tokens);
+    pages[n] = static_cast<int>((L + kPage - 1) / kPage);
+    max_pages = std::max(max_pages, pages[n]);
+    total += pages[n];
+  }
+  if (max_pages == 0) return kPage;  // nothing to read: any group size serves
+  auto items = [&](int span) {
+    int64_t groups = 0;
+    for (int p : pages) groups += (p + span - 1) / span;
+    return groups * Hkv;
+  };
+  constexpr int kMinPages = 32;  // 512 tokens
+  const int64_t work = total * Hkv;  // pages of all (sequence, KV head) pairs
+  int span = 0;
+  if (items(max_pages) <= capacity) {
+    // one wave: the smallest span whose groups all fit (items falls as span grows)
+    int lo = 1, hi = max_pages;
+    while (lo < hi) {
+      const int mid = lo + (hi - lo) / 2;
+      if (items(mid) <= capacity) hi = mid; else lo = mid + 1;
+    }
+    lo = std::max(lo, std::min(kMinPages, max_pages));
+    // kept only if its groups are near-equal: at most 5/4 of the average work per CTA
+    if (4 * static_cast<int64_t>(lo) * capacity <= 5 * work || lo == std::min(kMinPages, max_pages)) span = lo;
+  }
+  if (span == 0) {
+    // several waves: about three waves of equal power-of-two groups
+    const int64_t target = std::max<int64_t>(kMinPages, work / (3 * static_cast<int64_t>(capacity)));
+    span = kMinPages;
+    while (static_cast<int64_t>(span) * 2 <= target) span *= 2;
+    span = std::min(span, max_pages);
+  }
+  return span * kPage;
+}
+
+int attn_decode_auto_split_tokens(const int32_t* seq_lens, int num_seqs, int Hkv, int d, int max_blocks_per_seq) {
+  if (seq_lens == nullptr || num_seqs < 1 || Hkv < 1 || max_blocks_per_seq < 1 || (d != 128 && d != 256)) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  const int per_sm = attn::decode_split_ctas_per_sm(d);
+  if (per_sm < 1) return 0;
+  return attn_split_tokens_rule(seq_lens, num_seqs, Hkv, sms * per_sm, max_blocks_per_seq);
+}
+
 size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d, int slots) {
   if (num_seqs < 1 || Hq < 1 || d < 1 || slots < 1) return 0;
   if (slots == 1) return 0;
@@ -263,6 +318,7 @@ attn_status_t check_decode_args(const void* q, const void* k_cache, const void* 
   if (d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
   if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;  // query heads per KV head fill at most 16 MMA rows
   if (num_seqs > 65535 || Hkv > 65535) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(num_seqs) * Hq > (int64_t(1) << 30)) return ATTN_ERR_INVALID_ARG;  // rows of the combine
   if (static_cast<int64_t>(num_blocks) * page_size > (int64_t(1) << 31) - 1) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
@@ -370,7 +426,10 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = attn::decode_split_launch(d, maps, p, st);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
-  if (slots > 1) e = attn::combine_launch(d, p.part_o, p.part_m, p.part_l, static_cast<int>(nrow), slots, o, lse, st);
+  if (slots > 1) {
+    const attn::CombineGeometry geo{seq_lens, Hq, max_blocks_per_seq, p.split_pages, p.num_splits};
+    e = attn::combine_launch(d, p.part_o, p.part_m, p.part_l, static_cast<int>(nrow), slots, geo, o, lse, st);
+  }
   return from_cuda(e);
 }
 
@@ -383,7 +442,8 @@ attn_status_t attn_combine(const float* part_o, const float* part_m, const float
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
   if (rows < 1 || num_splits < 1) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
-  return from_cuda(attn::combine_launch(d, part_o, part_m, part_l, rows, num_splits, o, lse,
+  const attn::CombineGeometry all_slots{nullptr, 1, 1, 0, 1};
+  return from_cuda(attn::combine_launch(d, part_o, part_m, part_l, rows, num_splits, all_slots, o, lse,
                                         static_cast<cudaStream_t>(stream)));
 }
 

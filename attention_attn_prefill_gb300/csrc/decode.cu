@@ -323,21 +323,13 @@ __global__ void __launch_bounds__(NW * 32)
     return pfirst + i;
   };
   const bool xqa_sum = EMU && p.emu == kEmuXqa;  // the sum adds the bf16-rounded weights
-
-  // Q rows of the G heads sharing KV head g (rows >= G are zero), swizzled by 16-byte unit.
-  for (int i = threadIdx.x; i < 16 * (D / 8); i += NW * 32) {
-    const int r = i / (D / 8);
-    const int u = i % (D / 8);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < G)
-      v = *reinterpret_cast<const uint4*>(p.q + ((static_cast<size_t>(n) * p.Hq + g * G + r) * D + u * 8));
-    *reinterpret_cast<uint4*>(sQ + r * (D * 2) + ((u ^ (r & 7)) << 4)) = v;
+  if constexpr (!EMU) {
+    // An empty group writes nothing: the combine visits only the groups a sequence has.
+    if (npages <= 0 && !p.write_final) {
+      asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+      return;
+    }
   }
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NW * NS; ++i) mbar_init(&bars[i], 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
 
   uint8_t* my_stages = smem + L::STAGE_OFF + warp * L::WARP_BYTES;
   uint64_t* my_bars = bars + warp * NS;
@@ -360,10 +352,23 @@ __global__ void __launch_bounds__(NW * 32)
     }
   };
 
+  // Each warp's lane 0 sets up its own barriers and requests its first pages at once; the Q rows
+  // arrive meanwhile, and the CTA barrier below makes both visible to every thread.
   if (lane == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(&my_bars[i], 1);
+    fence_mbar_init();
     for (int k = 0; k < n_my && k < NS; ++k) issue(k);
   }
-  __syncwarp();
+  // Q rows of the G heads sharing KV head g (rows >= G are zero), swizzled by 16-byte unit.
+  for (int i = threadIdx.x; i < 16 * (D / 8); i += NW * 32) {
+    const int r = i / (D / 8);
+    const int u = i % (D / 8);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < G)
+      v = *reinterpret_cast<const uint4*>(p.q + ((static_cast<size_t>(n) * p.Hq + g * G + r) * D + u * 8));
+    *reinterpret_cast<uint4*>(sQ + r * (D * 2) + ((u ^ (r & 7)) << 4)) = v;
+  }
+  __syncthreads();
 
   const uint32_t q_base = smem_u32(sQ);
   const FragRows fr(lane);
@@ -491,45 +496,102 @@ __global__ void __launch_bounds__(NW * 32)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// One warp per (sequence, query head): O = sum_i w_i o_i / sum_i w_i, w_i = l_i exp(m_i - M).
-template <int D>
-__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
+// Merge of the partials of each row (sequence, query head): O = sum_i w_i o_i / sum_i w_i with
+// w_i = l_i exp(m_i - M), M = max of the non-empty slots' m_i, LSE = M + ln sum_i w_i.
+//
+// WPR warps share a row and take its slots round-robin, each loading U slots at a time so that
+// their loads are in flight together; the warps' sums (all at the same M) are then added through
+// shared memory.  With a row's group count known (geometry g.seq_lens != null) only its groups
+// are visited, so slots past them need not have been written; otherwise every slot is visited and
+// a slot counts only if its l_i > 0.
+template <int D, int WPR>
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_o,
                                                       const float* __restrict__ part_m,
                                                       const float* __restrict__ part_l, int rows, int splits,
-                                                      __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+                                                      CombineGeometry geo, __nv_bfloat16* __restrict__ o,
+                                                      float* __restrict__ lse) {
   // the partials come from the preceding kernel in the stream: wait until they are all visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int RPC = 8 / WPR;           // rows per CTA of 8 warps
+  constexpr int PER = D / 32;            // output columns per lane
+  constexpr int U = D <= 128 ? 8 : 4;    // slots in flight per warp
+  __shared__ __align__(16) float s_acc[WPR > 1 ? 8 : 1][WPR > 1 ? D : 1];
+  __shared__ float s_w[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + warp;
-  if (row >= rows) return;
-  const float* pm = part_m + static_cast<size_t>(row) * splits;
-  const float* pl = part_l + static_cast<size_t>(row) * splits;
+  const int wr = warp % WPR;
+  const int row = blockIdx.x * RPC + warp / WPR;
+  const bool live = row < rows;
+  int nvalid = splits;
+  if (live && geo.seq_lens != nullptr) {
+    int L = geo.seq_lens[row / geo.Hq];
+    L = L < 0 ? 0 : (L > geo.max_blocks * PAGE ? geo.max_blocks * PAGE : L);
+    const int pages = (L + PAGE - 1) / PAGE;
+    const int span = geo.split_pages > 0 ? geo.split_pages : (pages + geo.num_splits - 1) / geo.num_splits;
+    const int groups = span > 0 ? (pages + span - 1) / span : 0;
+    nvalid = groups < splits ? groups : splits;
+  }
+  const size_t rbase = static_cast<size_t>(live ? row : 0) * splits;
+  const float* pm = part_m + rbase;
+  const float* pl = part_l + rbase;
   float M = -INFINITY;
-  for (int i = lane; i < splits; i += 32)
-    if (pl[i] > 0.f) M = fmaxf(M, pm[i]);
+  if (live)
+    for (int i = lane; i < nvalid; i += 32)
+      if (pl[i] > 0.f) M = fmaxf(M, pm[i]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  constexpr int PER = D / 32;  // output columns per lane
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float W = 0.f;
-  if (M != -INFINITY) {
-    const float* po = part_o + static_cast<size_t>(row) * splits * D;
-    for (int i = 0; i < splits; ++i) {
-      const float li = pl[i];
-      if (!(li > 0.f)) continue;
-      const float w = li * expf(pm[i] - M);
-      W += w;
-      const float* src = po + static_cast<size_t>(i) * D + lane * PER;
+  if (live && M != -INFINITY) {
+    const float* po = part_o + rbase * D + lane * PER;
+    for (int i0 = wr; i0 < nvalid; i0 += WPR * U) {
+      float li[U], mi[U], v[U][PER];
 #pragma unroll
-      for (int e = 0; e < PER; e += 2) {
-        const float2 v = *reinterpret_cast<const float2*>(src + e);
-        acc[e] += w * v.x;
-        acc[e + 1] += w * v.y;
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * WPR;
+        li[u] = 0.f;
+        mi[u] = -INFINITY;
+        if (i < nvalid) {
+          li[u] = pl[i];
+          mi[u] = pm[i];
+          const float* src = po + static_cast<size_t>(i) * D;
+#pragma unroll
+          for (int e = 0; e < PER; e += (PER >= 4 ? 4 : 2)) {
+            if constexpr (PER >= 4) {
+              const float4 t = *reinterpret_cast<const float4*>(src + e);
+              v[u][e] = t.x; v[u][e + 1] = t.y; v[u][e + 2] = t.z; v[u][e + 3] = t.w;
+            } else {
+              const float2 t = *reinterpret_cast<const float2*>(src + e);
+              v[u][e] = t.x; v[u][e + 1] = t.y;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (!(li[u] > 0.f)) continue;  // an empty group carries no weight (its stored values are not read)
+        const float w = li[u] * expf(mi[u] - M);
+        W += w;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, v[u][e], acc[e]);
       }
     }
   }
+  if constexpr (WPR > 1) {
+#pragma unroll
+    for (int e = 0; e < PER; ++e) s_acc[warp][lane * PER + e] = acc[e];
+    if (lane == 0) s_w[warp] = W;
+    __syncthreads();
+    if (wr != 0) return;
+#pragma unroll
+    for (int j = 1; j < WPR; ++j) {
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] += s_acc[warp + j][lane * PER + e];
+      W += s_w[warp + j];
+    }
+  }
+  if (!live) return;
   const float inv = W > 0.f ? 1.f / W : 0.f;
   __nv_bfloat16* dst = o + static_cast<size_t>(row) * D + lane * PER;
 #pragma unroll
@@ -782,24 +844,33 @@ __global__ void __launch_bounds__(NW * 32)
   flush();
 }
 
-// One warp per (sequence n, query head hq): merge the records of the warps that covered (g, n).
-template <int D>
-__global__ void __launch_bounds__(128) combine_balanced_kernel(const BalancedParams p) {
+// WPR warps per (sequence n, query head hq), 8 / WPR rows per CTA of 8 warps: merge the records of
+// the worker warps that covered (g, n).  Every warp of a row finds the covering range and its largest
+// max; the row's warps then take its records round-robin, U at a time so that their loads are in
+// flight together, and their sums (all at the same max) are added through shared memory.
+template <int D, int WPR>
+__global__ void __launch_bounds__(256) combine_balanced_kernel(const BalancedParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int RPC = 8 / WPR;         // rows per CTA
+  constexpr int PER = D / 32;          // output columns per lane
+  constexpr int U = D <= 128 ? 8 : 4;  // records in flight per warp
+  __shared__ __align__(16) float s_acc[WPR > 1 ? 8 : 1][WPR > 1 ? D : 1];
+  __shared__ float s_w[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + warp;
-  if (row >= p.N * p.Hq) return;
+  const int wr = warp % WPR;
+  const int row_raw = blockIdx.x * RPC + warp / WPR;
+  const bool live = row_raw < p.N * p.Hq;
+  const int row = live ? row_raw : 0;
   const int n = row / p.Hq, hq = row % p.Hq;
   const int G = p.G, g = hq / G, r = hq % G;
   long long Wt, before;
   int n_at;
   page_scan(p.seq_lens, p.N, p.max_blocks, lane, -1, Wt, n_at, before, p.Hkv);
-  constexpr int PER = D / 32;
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float M = -INFINITY, W = 0.f;
-  const int np = pages_of(p.seq_lens, n, p.max_blocks);
+  const int np = live ? pages_of(p.seq_lens, n, p.max_blocks) : 0;
   if (np > 0) {
     // pages of the sequences before n (each appears once per KV head in the list)
     long long pre = 0;
@@ -820,28 +891,57 @@ __global__ void __launch_bounds__(128) combine_balanced_kernel(const BalancedPar
     const float* rl = rm + R * G;
     // a warp whose share is empty (fewer pages than warps) wrote no record
     auto has_pages = [&](int uu) { return (uu + 1) * Wt / Wp > uu * Wt / Wp; };
-    for (int uu = u0; uu <= u1; ++uu) {
+    for (int uu = u0 + lane; uu <= u1; uu += 32) {
       const size_t idx = uu + j;
       if (has_pages(uu) && rl[idx * G + r] > 0.f) M = fmaxf(M, rm[idx * G + r]);
     }
-    if (M != -INFINITY) {
-      for (int uu = u0; uu <= u1; ++uu) {
-        if (!has_pages(uu)) continue;
-        const size_t idx = uu + j;
-        const float li = rl[idx * G + r];
-        if (!(li > 0.f)) continue;
-        const float w = li * expf(rm[idx * G + r] - M);
-        W += w;
-        const float* src = p.rec + (idx * G + r) * D + lane * PER;
 #pragma unroll
-        for (int e = 0; e < PER; e += 2) {
-          const float2 v = *reinterpret_cast<const float2*>(src + e);
-          acc[e] += w * v.x;
-          acc[e + 1] += w * v.y;
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (M != -INFINITY) {
+      for (int u_0 = u0 + wr; u_0 <= u1; u_0 += WPR * U) {
+        float li[U], mi[U], v[U][PER];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int uu = u_0 + u * WPR;
+          li[u] = 0.f;
+          mi[u] = -INFINITY;
+          if (uu <= u1 && has_pages(uu)) {
+            const size_t idx = uu + j;
+            li[u] = rl[idx * G + r];
+            mi[u] = rm[idx * G + r];
+            const float* src = p.rec + (idx * G + r) * D + lane * PER;
+#pragma unroll
+            for (int e = 0; e < PER; e += 4) {
+              const float4 t = *reinterpret_cast<const float4*>(src + e);
+              v[u][e] = t.x; v[u][e + 1] = t.y; v[u][e + 2] = t.z; v[u][e + 3] = t.w;
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (!(li[u] > 0.f)) continue;
+          const float w = li[u] * expf(mi[u] - M);
+          W += w;
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, v[u][e], acc[e]);
         }
       }
     }
   }
+  if constexpr (WPR > 1) {
+#pragma unroll
+    for (int e = 0; e < PER; ++e) s_acc[warp][lane * PER + e] = acc[e];
+    if (lane == 0) s_w[warp] = W;
+    __syncthreads();
+    if (wr != 0) return;
+#pragma unroll
+    for (int w = 1; w < WPR; ++w) {
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] += s_acc[warp + w][lane * PER + e];
+      W += s_w[warp + w];
+    }
+  }
+  if (!live) return;
   const float inv = W > 0.f ? 1.f / W : 0.f;
   __nv_bfloat16* dst = p.o + static_cast<size_t>(row) * D + lane * PER;
 #pragma unroll
@@ -862,12 +962,20 @@ cudaError_t launch_balanced(const DecodeMaps& m, const BalancedParams& p, cudaSt
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((p.N * p.Hq + 3) / 4);
-  cfg.blockDim = dim3(128);
+  // a row's records are spread over the warps that covered it; with few rows, several warps share a row
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const long long rows = static_cast<long long>(p.N) * p.Hq;
+  const int wpr = rows * 8 <= 16LL * sms ? 8 : rows * 2 <= 16LL * sms ? 2 : 1;
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + 8 / wpr - 1) / (8 / wpr)));
+  cfg.blockDim = dim3(256);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_balanced_kernel<D>, p);
+  if (wpr == 8) return cudaLaunchKernelEx(&cfg, combine_balanced_kernel<D, 8>, p);
+  if (wpr == 2) return cudaLaunchKernelEx(&cfg, combine_balanced_kernel<D, 2>, p);
+  return cudaLaunchKernelEx(&cfg, combine_balanced_kernel<D, 1>, p);
 }
 
 template <int D, int NW, int NS, bool EMU = false>
@@ -930,26 +1038,47 @@ cudaError_t decode_split_emulated_launch(int d, const DecodeMaps& maps, const De
   return launch_split_for<true>(d, maps, p, stream);
 }
 
-cudaError_t combine_launch(int d, const float* part_o, const float* part_m, const float* part_l, int rows,
-                           int splits, void* o, float* lse, cudaStream_t stream) {
-  auto* out = static_cast<__nv_bfloat16*>(o);
-  void (*kern)(const float*, const float*, const float*, int, int, __nv_bfloat16*, float*) = nullptr;
-  if (d == 128) kern = combine_kernel<128>;
-  else if (d == 256) kern = combine_kernel<256>;
-  else if (d == 64) kern = combine_kernel<64>;
-  else return cudaErrorInvalidValue;
+namespace {
+
+template <int D>
+cudaError_t launch_combine(const float* part_o, const float* part_m, const float* part_l, int rows, int splits,
+                           const CombineGeometry& geo, __nv_bfloat16* o, float* lse, cudaStream_t stream) {
+  // warps per row: enough that each warp has about U slots, at most the CTA's 8, and fewer when
+  // the rows alone give every SM work
+  constexpr int U = D <= 128 ? 8 : 4;
+  int wpr = splits <= U ? 1 : splits <= 2 * U ? 2 : splits <= 4 * U ? 4 : 8;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  while (wpr > 1 && static_cast<long long>(rows) * wpr > 16LL * sms) wpr /= 2;
+  void (*kern)(const float*, const float*, const float*, int, int, CombineGeometry, __nv_bfloat16*, float*) =
+      wpr == 1 ? combine_kernel<D, 1> : wpr == 2 ? combine_kernel<D, 2> : wpr == 4 ? combine_kernel<D, 4>
+                                                                                 : combine_kernel<D, 8>;
   // programmatic dependent launch: may begin before the previous kernel in the stream has finished
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((rows + 3) / 4);
-  cfg.blockDim = dim3(128);
+  const int rpc = 8 / wpr;
+  cfg.gridDim = dim3((rows + rpc - 1) / rpc);
+  cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, part_o, part_m, part_l, rows, splits, out, lse);
+  return cudaLaunchKernelEx(&cfg, kern, part_o, part_m, part_l, rows, splits, geo, o, lse);
+}
+
+}  // namespace
+
+cudaError_t combine_launch(int d, const float* part_o, const float* part_m, const float* part_l, int rows,
+                           int splits, const CombineGeometry& geo, void* o, float* lse, cudaStream_t stream) {
+  auto* out = static_cast<__nv_bfloat16*>(o);
+  if (d == 128) return launch_combine<128>(part_o, part_m, part_l, rows, splits, geo, out, lse, stream);
+  if (d == 256) return launch_combine<256>(part_o, part_m, part_l, rows, splits, geo, out, lse, stream);
+  if (d == 64) return launch_combine<64>(part_o, part_m, part_l, rows, splits, geo, out, lse, stream);
+  return cudaErrorInvalidValue;
 }
 
 // Worker warps per CTA, pages in flight per warp and CTAs per SM of the balanced kernel.

@@ -77,8 +77,15 @@ cudaError_t decode_split_emulated_launch(int d, const DecodeMaps& maps, const De
 cudaError_t merge_emulated_launch(int numerics, const float* part_o, const float* part_m, const float* part_l,
                                   int rows, int splits, int d, float* o32, void* o, float* lse, cudaStream_t stream);
 int decode_split_ctas_per_sm(int d);  // resident split-kernel CTAs per SM on the current device (0 on error)
+// Which slots of a row the combine visits.  seq_lens == null: all of them (a slot counts if its l > 0).
+// Otherwise row r belongs to sequence r / Hq, whose groups follow the split kernel's geometry
+// (split_pages > 0 pages per group, else ceil(pages / num_splits)); only those slots are read.
+struct CombineGeometry {
+  const int32_t* seq_lens;
+  int Hq, max_blocks, split_pages, num_splits;
+};
 cudaError_t combine_launch(int d, const float* part_o, const float* part_m, const float* part_l, int rows,
-                           int splits, void* o, float* lse, cudaStream_t stream);
+                           int splits, const CombineGeometry& geo, void* o, float* lse, cudaStream_t stream);
 cudaError_t decode_status(uint32_t* out, bool clear);
 
 }  // namespace attn

@@ -11,9 +11,20 @@
 // The array is ATTN_DECODE_NOALLOC_SCRATCH_BYTES (32 MiB) on every device that
 // loads the library, held until the process exits.  Calls share it: two calls
 // whose work overlaps on the GPU (different streams, or different host
-// threads) race on it.  The split kernel writes every partial slot a call uses
-// before the combine reads it, so stale contents from an earlier call are
-// never read and nothing needs clearing.
+// threads) race on it.  In every split mode, balanced mode included, the
+// split kernel writes each partial a call's combine reads, earlier in the
+// same call, so stale contents from an earlier call are never read and
+// nothing needs clearing.
+//
+// The entry point hands the array to attn_decode_paged as its workspace, with
+// the array's size as workspace_bytes.  So every check runs in that call's own
+// order: argument errors first, and ATTN_ERR_WORKSPACE (the partials would not
+// fit) last, before anything is enqueued.
+//
+// The array's address is looked up once per device ordinal and kept.  It
+// belongs to the runtime's primary context of that device, so the cache
+// assumes that context is the one current at every call and is never reset
+// (cudaDeviceReset) while the library is in use.
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -54,16 +65,10 @@ extern "C" attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_
                                                    float* lse, int num_seqs, int Hq, int Hkv, int d, int page_size,
                                                    int max_blocks_per_seq, int num_blocks, int num_splits,
                                                    int split_tokens, float scale, void* stream) {
-  const int slots = attn_decode_num_slots(max_blocks_per_seq, page_size, num_splits, split_tokens);
-  if (slots < 1 || num_seqs < 1 || Hq < 1) return ATTN_ERR_INVALID_ARG;
-  const size_t need = attn_decode_workspace_bytes(num_seqs, Hq, d, slots);
-  if (need > kScratchBytes) return ATTN_ERR_WORKSPACE;  // the partials would not fit the fixed array
   void* scratch = nullptr;
-  if (need > 0) {
-    const attn_status_t st = scratch_of_current_device(&scratch);
-    if (st != ATTN_OK) return st;
-  }
+  const attn_status_t st = scratch_of_current_device(&scratch);
+  if (st != ATTN_OK) return st;
   return attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, num_seqs, Hq, Hkv, d, page_size,
-                           max_blocks_per_seq, num_blocks, num_splits, split_tokens, scale, scratch,
-                           need > 0 ? kScratchBytes : 0, stream);
+                           max_blocks_per_seq, num_blocks, num_splits, split_tokens, scale, scratch, kScratchBytes,
+                           stream);
 }

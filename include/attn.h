@@ -178,6 +178,35 @@ int attn_split_heuristic(int units, int capacity, int blocks, int max_splits);
 int attn_decode_auto_splits(int num_seqs, int Hkv, int d, int max_blocks_per_seq);
 
 /*
+ * Length-aware group size for attn_decode_paged (pass the result as
+ * split_tokens).  The rule of "Why your local LLM feels dumber than it is"
+ * (Part 3.14), section "Why FlashAttention 2 selects 54, 62, or 87 groups",
+ * sizes every sequence's groups from the longest one; with mixed lengths that
+ * leaves long groups on the long sequences and short ones on the rest.  This
+ * rule instead gives every group the same number of pages s, so a sequence's
+ * group count is proportional to its length (ceil(pages_n / s)):
+ *   items(s) = Hkv * sum_n ceil(pages_n / s) groups, capacity = CTAs the
+ *   device runs at once;
+ *   one wave: s1 is the smallest page count with items(s1) <= capacity, but
+ *   at least 32 pages (512 tokens) or the longest sequence's page count if
+ *   that is smaller; it is taken when such a count exists and its groups are
+ *   near-equal, i.e. 4 * s1 * capacity <= 5 * (total pages * Hkv), or s1 is
+ *   that lower bound;
+ *   otherwise (several waves): s is the largest power of two that is at most
+ *   max(32, total pages * Hkv / (3 * capacity)), capped by the longest
+ *   sequence (about three waves of equal groups).
+ *   seq_lens   host array [num_seqs] of the lengths the decode will see
+ *              (entries are clamped to [0, max_blocks_per_seq * 16]).
+ * Returns s * 16 (a multiple of page_size = 16), or 0 for invalid arguments.
+ * attn_split_tokens_rule is the pure host arithmetic with an explicit
+ * capacity; attn_decode_auto_split_tokens applies it on the current device
+ * (capacity = SMs x resident split-kernel CTAs per SM) and also returns 0 when
+ * no CUDA device can be queried.
+ */
+int attn_split_tokens_rule(const int32_t* seq_lens, int num_seqs, int Hkv, int capacity, int max_blocks_per_seq);
+int attn_decode_auto_split_tokens(const int32_t* seq_lens, int num_seqs, int Hkv, int d, int max_blocks_per_seq);
+
+/*
  * Bytes of workspace attn_decode_paged needs: num_seqs * Hq * slots * (d + 2)
  * floats when slots > 1, else 0.
  */
@@ -234,17 +263,21 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
  * such as a plugin inside a host framework that owns all device memory and
  * hands out no scratch buffers, or a serving loop that forbids device
  * allocations once it has started.
- *   Arguments, layouts, results and errors are those of attn_decode_paged,
- *   without workspace / workspace_bytes: the per-split partials live in a
- *   fixed array of ATTN_DECODE_NOALLOC_SCRATCH_BYTES inside the library's own
- *   device memory, present on every device that loads the library until the
- *   process exits.  No cudaMalloc, cudaFree or other allocating call is made.
- *   If the partials need more than that (num_seqs * Hq * slots * (d + 2) * 4
- *   bytes with slots > 1), the call returns ATTN_ERR_WORKSPACE and enqueues
- *   nothing.
+ *   Arguments, layouts, results and errors are those of attn_decode_paged
+ *   (balanced mode included), without workspace / workspace_bytes: the
+ *   partials live in a fixed array of ATTN_DECODE_NOALLOC_SCRATCH_BYTES
+ *   inside the library's own device memory, present on every device that
+ *   loads the library until the process exits.  No cudaMalloc, cudaFree or
+ *   other allocating call is made.  The array is passed to attn_decode_paged
+ *   as a workspace of that many bytes, so argument errors are reported first,
+ *   and a call whose partials need more (attn_decode_workspace_bytes, or
+ *   attn_decode_balanced_workspace_bytes in balanced mode) returns
+ *   ATTN_ERR_WORKSPACE and enqueues nothing.
  *   The first call on a device looks up the array's device address (once per
- *   device, with that device current); make that first call before any
- *   stream capture.
+ *   device, with that device current) and keeps it; make that first call
+ *   before any stream capture.  The kept address belongs to the device's
+ *   primary context: do not reset the device (cudaDeviceReset) while the
+ *   library is in use, nor call it from another context on the same device.
  *   All calls share the array: calls whose work overlaps on the GPU (other
  *   streams, other host threads) race on it.  Every partial a call reads was
  *   written earlier in the same call, so leftovers of earlier calls are
