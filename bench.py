@@ -276,6 +276,10 @@ def run_gpu(args):
         torch.distributed.barrier()
     pre_ms = [a.elapsed_time(b) for a, b, _ in rec]
     dec_ms = [b.elapsed_time(c) for _, b, c in rec]
+    spread = {"prefill_us": {"mean": round(statistics.mean(pre_ms) * 1e3, 2),
+                             "median": round(statistics.median(pre_ms) * 1e3, 2), "min": round(min(pre_ms) * 1e3, 2)},
+              "decode_us": {"mean": round(statistics.mean(dec_ms) * 1e3, 2),
+                            "median": round(statistics.median(dec_ms) * 1e3, 2), "min": round(min(dec_ms) * 1e3, 2)}}
     pre_mean, dec_mean = statistics.mean(pre_ms), statistics.mean(dec_ms)
     step_ms = pre_mean + dec_mean
     if world > 1:
@@ -373,7 +377,11 @@ def run_gpu(args):
                 "peak_source": f"{peak_src} bf16 dense (burst)",
                 "traffic": traffic_record("prefill_cta2_kernel"), "algorithmic_bytes": cfg.min_bytes,
             },
+            "flops_convention": "exact causal pairs, 4*B*Hq*d*S(S+1)/2",
+            "s2_over_2": {"flops_per_step": cfg.s2_flops,
+                          "TFLOP/s": round(world * cfg.s2_flops / (pre_mean * 1e-3) / 1e12, 2)},
         },
+        "timing_spread": spread,
         "decode": {"value": round(gbs, 1), "unit": "GB/s", "ms": round(dec_mean, 4), "roofline": dec_roof},
         "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms": round(e2e_ms, 4)},
@@ -391,9 +399,12 @@ def run_gpu(args):
         torch.distributed.destroy_process_group()
 
 
-def workload_table(attn, dev, stream, flush, peaks, paged_inputs, reps: int = 10):
-    """Every seeded workload (outside the timed region): mean of `reps` launches, L2 flushed before each."""
+def workload_table(attn, dev, stream, flush, peaks, paged_inputs, reps: int = 50):
+    """Every seeded workload (outside the timed region): `reps` launches, L2 flushed before each.
+
+    Each entry's value is from the mean launch time; the median and the fastest launch ride along."""
     from workloads import DECODE_CONFIGS, PREFILL_CONFIGS
+    spread = {}
 
     def timed(launch):
         launch()
@@ -407,7 +418,10 @@ def workload_table(attn, dev, stream, flush, peaks, paged_inputs, reps: int = 10
             b.record(stream)
             ms.append((a, b))
         torch.cuda.synchronize()
-        return statistics.mean(a.elapsed_time(b) for a, b in ms)
+        t = [a.elapsed_time(b) for a, b in ms]
+        spread["us_median"] = round(statistics.median(t) * 1e3, 1)
+        spread["us_min"] = round(min(t) * 1e3, 1)
+        return statistics.mean(t)
 
     out = {}
     for cfg in PREFILL_CONFIGS:
@@ -417,8 +431,9 @@ def workload_table(attn, dev, stream, flush, peaks, paged_inputs, reps: int = 10
         lse = torch.empty((cfg.B, cfg.Hq, cfg.S), dtype=torch.float32, device=dev)
         ms = timed(lambda: attn.prefill(q, k, v, scale=cfg.scale, causal=True, out=o, lse=lse, stream=stream))
         tf = cfg.causal_flops / (ms * 1e-3) / 1e12
-        out[cfg.name] = {"TFLOP/s": round(tf, 1), "us": round(ms * 1e3, 1),
-                         "frac": round(tf / peaks["bf16_tflops"], 4)}
+        out[cfg.name] = {"TFLOP/s": round(tf, 1), "us": round(ms * 1e3, 1), **spread,
+                         "frac": round(tf / peaks["bf16_tflops"], 4),
+                         "TFLOP/s_s2_over_2": round(cfg.s2_flops / (ms * 1e-3) / 1e12, 1)}
         del q, k, v, o, lse
     for cfg in DECODE_CONFIGS:
         if cfg.name == "paged_decode":
@@ -431,18 +446,21 @@ def workload_table(attn, dev, stream, flush, peaks, paged_inputs, reps: int = 10
         do = torch.empty_like(dq)
         dl = torch.empty((cfg.N, cfg.Hq), dtype=torch.float32, device=dev)
         specs = [dict(num_splits=n) for n in cfg.num_splits] + [dict(split_tokens=t) for t in cfg.split_tokens]
-        specs += [dict(num_splits=attn.decode_auto_splits(cfg.N, cfg.Hkv, cfg.d, x.max_blocks)),
+        auto_t = attn.decode_auto_split_tokens(lens, cfg.Hkv, cfg.d, x.max_blocks)
+        specs += [dict(split_tokens=auto_t),
+                  dict(num_splits=attn.decode_auto_splits(cfg.N, cfg.Hkv, cfg.d, x.max_blocks)),
                   dict(num_splits=0)]
         names = [f"splits={sp['num_splits']}" if "num_splits" in sp else f"split_tokens={sp['split_tokens']}"
                  for sp in specs]
-        names[-2] = f"auto ({specs[-2]['num_splits']} splits)"
+        names[-3] = f"auto (length-aware, {auto_t}-token groups)"
+        names[-2] = f"FA2 rule ({specs[-2]['num_splits']} splits)"
         names[-1] = "balanced"
         for name, sp in zip(names, specs):
             ws = torch.empty(max(1, decode_ws_bytes(attn, x.max_blocks, cfg, **sp)), dtype=torch.uint8, device=dev)
             ms = timed(lambda: attn.decode_paged(dq, kc, vc, bt, sl, scale=cfg.scale, out=do, lse=dl, workspace=ws,
                                                  stream=stream, **sp))
             gbs = nbytes / (ms * 1e-3) / 1e9
-            out[f"{cfg.name} {name}"] = {"GB/s": round(gbs, 1), "us": round(ms * 1e3, 1),
+            out[f"{cfg.name} {name}"] = {"GB/s": round(gbs, 1), "us": round(ms * 1e3, 1), **spread,
                                          "frac": round(gbs / peaks["hbm_gbs"], 4)}
         # other backends' decode numerics, with the group counts they would pick on this GPU
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -456,7 +474,7 @@ def workload_table(attn, dev, stream, flush, peaks, paged_inputs, reps: int = 10
                                                           stream=stream))
             gbs = nbytes / (ms * 1e-3) / 1e9
             out[f"{cfg.name} emulated {backend} ({slots} groups)"] = {
-                "GB/s": round(gbs, 1), "us": round(ms * 1e3, 1), "frac": round(gbs / peaks["hbm_gbs"], 4)}
+                "GB/s": round(gbs, 1), "us": round(ms * 1e3, 1), **spread, "frac": round(gbs / peaks["hbm_gbs"], 4)}
             del ws
     # packed sequences of mixed lengths and chunked prefill over a paged cache, Llama-8B heads
     Hq, Hkv, d = 32, 8, 128
@@ -469,7 +487,7 @@ def workload_table(attn, dev, stream, flush, peaks, paged_inputs, reps: int = 10
                                            stream=stream))
     flops = 4.0 * Hq * d * sum(L * (L + 1) / 2 for L in lens)
     out[f"packed prefill, 8 sequences of {min(lens)}-{max(lens)} tokens"] = {
-        "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1), "us": round(ms * 1e3, 1),
+        "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1), "us": round(ms * 1e3, 1), **spread,
         "frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
     del vq, vk, vv, vo, vl
     for n, qn, ctxn in ((4, 2048, 8192), (16, 512, 4096)):
@@ -481,11 +499,14 @@ def workload_table(attn, dev, stream, flush, peaks, paged_inputs, reps: int = 10
                                               stream=stream))
         flops = 4.0 * Hq * d * n * sum(ctxn - qn + i + 1 for i in range(qn))
         out[f"chunked prefill, {n} x {qn} new tokens over {ctxn}-token contexts"] = {
-            "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1), "us": round(ms * 1e3, 1),
+            "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1), "us": round(ms * 1e3, 1), **spread,
             "frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
         del cargs, co, cl
-    out["_note"] = (f"each: mean of {reps} launches with L2 flushed before each, outside the timed region; "
-                    "frac against the measured bf16 dense peak (prefill) or HBM copy (decode)")
+    out["_note"] = (f"each: {reps} launches with L2 flushed before each, outside the timed region; value and frac "
+                    "from the mean launch time (us), with the median and the fastest launch beside it; frac against "
+                    "the measured bf16 dense peak (prefill) or HBM copy (decode); prefill flops count the causal "
+                    "(query, key) pairs exactly, S(S+1)/2 per head, and TFLOP/s_s2_over_2 repeats the value under "
+                    "the S^2/2 convention")
     if attn.device_status(clear=True) != 0:
         out["_device_status"] = "nonzero"
     return out
@@ -507,7 +528,34 @@ def cpu_baseline(min_seconds: float):
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"float64 numpy oracle, causal prefill B=1 S=2048 d=128: {heads} query-head passes "
                       f"(all 2048 rows each) in {dt:.2f} s, {flops / 1e9:.1f} GFLOP counted causally; "
-                      "numpy BLAS threads = host cores"}
+                      "numpy BLAS threads = host cores",
+            "single_core_tiny": single_core_tiny()}
+
+
+def single_core_tiny(seconds: float = 1.0):
+    """The oracle on the tiny config (B=1, S=128, d=64) on one host core: a child process with every
+    BLAS/OpenMP thread pool set to one thread, repeated for about `seconds`."""
+    code = (
+        "import time, oracle.attention as oa\n"
+        "from workloads import TINY, prefill_inputs_for\n"
+        "x = prefill_inputs_for(TINY)\n"
+        "oa.prefill(x.q, x.k, x.v, TINY.scale, causal=True)\n"
+        "n, t0 = 0, time.perf_counter()\n"
+        f"while time.perf_counter() - t0 < {seconds}:\n"
+        "    oa.prefill(x.q, x.k, x.v, TINY.scale, causal=True); n += 1\n"
+        "dt = time.perf_counter() - t0\n"
+        "print(n, dt, TINY.causal_flops)\n")
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               NUMEXPR_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    try:
+        out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                             timeout=120, check=True).stdout.split()
+        n, dt, fl = int(out[0]), float(out[1]), float(out[2])
+    except Exception as exc:  # reported, not fatal: the multi-core figure above stands
+        return {"error": str(exc)[:200]}
+    return {"value": n * fl / dt / 1e12, "unit": "TFLOP/s", "cores": 1,
+            "sample": f"tiny causal prefill B=1 Hq=1 S=128 d=64, {n} passes in {dt:.2f} s, one thread",
+            "ms_per_pass": round(1e3 * dt / n, 3)}
 
 
 def run_reference(args):
@@ -552,7 +600,8 @@ def run_case(args):
     chunked:<n>x<q>of<ctx>    chunked prefill against the paged cache, Llama-8B heads: n sequences of
                               ctx cached tokens whose last q are new
     decode:<name>:<splits>    name in {paged_decode, longctx_decode}; splits = num_splits (0 = balanced
-                              mode), t<N> for split_tokens = N, or auto for the split-count rule
+                              mode), t<N> for split_tokens = N, auto for the FA2 split-count rule, or
+                              autot for the length-aware group size
     decode_emu:<name>:<backend>  the same workloads with another backend's numerics (triton, fa2, xqa,
                               trt) and the group count it would pick on this GPU
     """
@@ -615,6 +664,8 @@ def run_case(args):
         x = decode_inputs_for(cfg)
         if spec == "auto":
             kw = dict(num_splits=attn.decode_auto_splits(cfg.N, cfg.Hkv, cfg.d, x.max_blocks))
+        elif spec == "autot":
+            kw = dict(split_tokens=attn.decode_auto_split_tokens(lens, cfg.Hkv, cfg.d, x.max_blocks))
         elif spec.startswith("t"):
             kw = dict(split_tokens=int(spec[1:]))
         else:

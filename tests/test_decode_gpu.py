@@ -109,6 +109,16 @@ def test_auto_split_count(attn, gpu):
     compare(attn, x, 0.09, gpu, f"auto ({n} splits)", num_splits="auto")
 
 
+def test_auto_split_tokens(attn, gpu):
+    """split_tokens="auto": the length-aware group size for this device, then the usual parity."""
+    lens = [3000, 17, 1234, 9000, 640, 0, 5000]
+    x = make_decode_inputs(lens, Hq=16, Hkv=2, d=256, seed=61, nan_tail=True)
+    t = attn.decode_auto_split_tokens(x.seq_lens, 2, 256, x.block_table.shape[1])
+    assert t >= 16 and t % 16 == 0
+    live = [n for n, L in enumerate(lens) if L > 0]
+    compare(attn, x, 2.0 ** -4, gpu, f"auto ({t}-token groups)", seqs=live, split_tokens="auto")
+
+
 def test_bad_page_is_reported(attn, gpu):
     """A block-table entry outside [0, num_blocks) is recorded as a device error, not read."""
     x = make_decode_inputs([40], Hq=4, Hkv=1, d=128, seed=57)
@@ -148,21 +158,44 @@ def test_worked_example_on_gpu(attn, gpu):
         assert len(vals) == 1 and vals.pop() in (1.3203125, 1.328125), kw
 
 
-def test_paged_config_full_size(attn, gpu):
-    """64 sequences, lengths U[512, 8192], GQA 32:8, d=128; 16 sampled sequences checked per split count."""
-    x = decode_inputs_for(PAGED)
-    seqs = list(range(0, 64, 4))
-    for ns in PAGED.num_splits + (0,):
-        compare(attn, x, PAGED.scale, gpu, f"paged ns={ns}", seqs=seqs, num_splits=ns)
+_FULL = {}
 
 
-@pytest.mark.parametrize("span", LONGCTX.split_tokens + (0,))
+def _full_size(cfg):
+    """The config's inputs and the oracle's output for every sequence, computed once per session."""
+    if cfg.name not in _FULL:
+        x = decode_inputs_for(cfg)
+        _FULL[cfg.name] = (x, oa.decode_paged(x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens, cfg.scale))
+    return _FULL[cfg.name]
+
+
+def _compare_full(attn, cfg, dev, what, **kw):
+    x, (wo, wl) = _full_size(cfg)
+    o, lse = run_decode(attn, x, cfg.scale, dev, **kw)
+    check_o(to_np(o), wo, what)
+    check_lse(to_np(lse), wl, what)
+
+
+@pytest.mark.parametrize("kw", [dict(num_splits=n) for n in PAGED.num_splits] + [dict(num_splits=0), dict(auto=1)],
+                         ids=lambda k: "-".join(f"{a}{b}" for a, b in k.items()))
+def test_paged_config_full_size(attn, gpu, kw):
+    """64 sequences, lengths U[512, 8192], GQA 32:8, d=128: every output of every sequence, per split
+    choice (num_splits 0 is balanced mode; auto is the length-aware group size)."""
+    if "auto" in kw:
+        x, _ = _full_size(PAGED)
+        kw = dict(split_tokens=attn.decode_auto_split_tokens(x.seq_lens, PAGED.Hkv, PAGED.d, x.block_table.shape[1]))
+    _compare_full(attn, PAGED, gpu, f"paged {kw}", **kw)
+
+
+@pytest.mark.parametrize("span", LONGCTX.split_tokens + (0, "auto"))
 def test_longctx_config_full_size(attn, gpu, span):
-    """8 sequences up to 122,863 tokens, Hq=16, Hkv=2, d=256, scale 2^-4; two sequences checked.
+    """8 sequences up to 122,863 tokens, Hq=16, Hkv=2, d=256, scale 2^-4: every output, per group size.
 
-    span 0 is balanced mode."""
-    x = decode_inputs_for(LONGCTX)
-    compare(attn, x, LONGCTX.scale, gpu, f"longctx span={span}", seqs=[2, 7], split_tokens=span)
+    span 0 is balanced mode; auto is the length-aware group size."""
+    if span == "auto":
+        x, _ = _full_size(LONGCTX)
+        span = attn.decode_auto_split_tokens(x.seq_lens, LONGCTX.Hkv, LONGCTX.d, x.block_table.shape[1])
+    _compare_full(attn, LONGCTX, gpu, f"longctx span={span}", split_tokens=span)
 
 
 # ------------------------------------------------------------------ combine

@@ -158,13 +158,31 @@ def _sampled(attn, gpu, cfg, heads, nrows, seed):
     assert np.isfinite(on).all() and np.isfinite(ln).all()
 
 
-def test_llama8b_full_size_sampled(attn, gpu):
-    _sampled(attn, gpu, LLAMA8B, heads=[0, 5, 17, 31], nrows=48, seed=1)
+def _complete(attn, gpu, cfg):
+    """Full-size config: every output row of every head and batch element against the oracle."""
+    x = prefill_inputs_for(cfg)
+    o, lse = run_prefill(attn, x, cfg.scale, True, gpu)
+    wo, wl = oa.prefill(x.q, x.k, x.v, cfg.scale, causal=True)
+    on, ln = to_np(o), to_np(lse)
+    for b in range(cfg.B):
+        for h in range(cfg.Hq):
+            check_o(on[b, :, h], wo[b, :, h], f"{cfg.name} b={b} h={h}")
+            check_lse(ln[b, h], wl[b, h], f"{cfg.name} b={b} h={h}")
+    check_o(on, wo, f"{cfg.name} all heads")
 
 
-@pytest.mark.parametrize("cfg", SWEEP, ids=lambda c: c.name)
+def test_llama8b_full_size_complete(attn, gpu):
+    _complete(attn, gpu, LLAMA8B)
+
+
+@pytest.mark.parametrize("cfg", [c for c in SWEEP if c.S <= 2048], ids=lambda c: c.name)
+def test_sweep_full_size_complete(attn, gpu, cfg):
+    _complete(attn, gpu, cfg)
+
+
+@pytest.mark.parametrize("cfg", [c for c in SWEEP if c.S > 2048], ids=lambda c: c.name)
 def test_sweep_full_size_sampled(attn, gpu, cfg):
-    _sampled(attn, gpu, cfg, heads=[0, 13, 31], nrows=24, seed=cfg.seed)
+    _sampled(attn, gpu, cfg, heads=[0, 1, 13, 30, 31], nrows=32, seed=cfg.seed)
 
 
 def test_d256_8k_prompt_sampled(attn, gpu):

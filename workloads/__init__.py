@@ -53,6 +53,12 @@ class PrefillConfig:
         return 4.0 * self.B * self.Hq * self.d * pairs
 
     @property
+    def s2_flops(self) -> float:
+        """The same count under the S^2/2 convention for causal pairs (S^2 when not causal)."""
+        pairs = self.S * self.S / 2 if self.causal else float(self.S) * self.S
+        return 4.0 * self.B * self.Hq * self.d * pairs
+
+    @property
     def min_bytes(self) -> int:
         """Q + K + V + O in bf16 plus the f32 LSE."""
         qo = 2 * self.B * self.S * self.Hq * self.d * 2
