@@ -41,7 +41,7 @@ if ROOT not in sys.path:
 import torch  # noqa: E402
 
 from workloads import (LLAMA8B, PAGED, decode_inputs_for, decode_lens_for, decode_min_bytes, make_chunked_inputs,  # noqa
-                       make_varlen_inputs, prefill_inputs_for)
+                       make_prefill_inputs, make_varlen_inputs, prefill_inputs_for)
 
 METRIC = "prefill TFLOP/s & decode KV GB/s on 1 GB300, as % of bf16 TC peak / HBM peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -597,8 +597,11 @@ def run_case(args):
 
     prefill:<name>            name in {tiny, llama8b_prefill, sweep_s1024, sweep_s2048, sweep_s4096,
                               qwen_d256_prefill}
-    chunked:<n>x<q>of<ctx>    chunked prefill against the paged cache, Llama-8B heads: n sequences of
-                              ctx cached tokens whose last q are new
+    shape:<B>x<Hq>x<Hkv>x<S>x<d>  causal prefill of that shape (seeded N(0,1) inputs)
+    varlen:<mix|L1,L2,..>[:<Hq>x<Hkv>x<d>]  packed sequences: the workload table's mix (8 sequences)
+                              or the given lengths (Llama-8B heads unless given)
+    chunked:<n>x<q>of<ctx>[:<Hq>x<Hkv>x<d>]  chunked prefill against the paged cache (Llama-8B heads
+                              unless given): n sequences of ctx cached tokens whose last q are new
     decode:<name>:<splits>    name in {paged_decode, longctx_decode}; splits = num_splits (0 = balanced
                               mode), t<N> for split_tokens = N, auto for the FA2 split-count rule, or
                               autot for the length-aware group size
@@ -612,13 +615,41 @@ def run_case(args):
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream(dev)
     kind, name, *rest = args.case.split(":")
-    if kind == "chunked":
+    if kind == "shape":
+        # a causal prefill of any shape: name = "<B>x<Hq>x<Hkv>x<S>x<d>" (odd Hq / Hkv takes the
+        # single-head kernel at d = 128)
+        B, Hq, Hkv, S, d = (int(v) for v in name.split("x"))
+        x = make_prefill_inputs(B, Hq, Hkv, S, d, seed=21)
+        q, k, v = (t.to(dev) for t in (x.q, x.k, x.v))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
+        work, unit = 4.0 * B * Hq * d * S * (S + 1) / 2 / 1e12, "TFLOP/s"
+
+        def launch():
+            attn.prefill(q, k, v, scale=d ** -0.5, causal=True, out=o, lse=lse, stream=stream)
+    elif kind == "varlen":
+        # name "mix": the packed mix of the workload table (8 sequences of seeded lengths U[256, 4096]);
+        # else comma-separated lengths; Llama-8B heads unless <Hq>x<Hkv>x<d> follows
+        Hq, Hkv, d = (int(v) for v in rest[0].split("x")) if rest else (32, 8, 128)
+        if name == "mix":
+            lens = [int(v) for v in torch.randint(256, 4097, (8,), generator=torch.Generator().manual_seed(12))]
+        else:
+            lens = [int(v) for v in name.split(",")]
+        xv = make_varlen_inputs(lens, Hq=Hq, Hkv=Hkv, d=d, seed=12)
+        vq, vk, vv, vcu = (t.to(dev) for t in (xv.q, xv.k, xv.v, xv.cu_seqlens))
+        vo = torch.empty_like(vq)
+        vl = torch.empty((Hq, vq.shape[0]), dtype=torch.float32, device=dev)
+        work, unit = 4.0 * Hq * d * sum(L * (L + 1) / 2 for L in lens) / 1e12, "TFLOP/s"
+
+        def launch():
+            attn.prefill_varlen(vq, vk, vv, vcu, xv.max_seqlen, scale=d ** -0.5, out=vo, lse=vl, stream=stream)
+    elif kind == "chunked":
         # chunked prefill against the paged cache: <n> sequences of <ctx> cached tokens, the last <q> new
         # (name = "<n>x<q>of<ctx>"), Llama-8B heads
         n, rest_ = name.split("x")
         qn, ctxn = (int(v) for v in rest_.split("of"))
         n = int(n)
-        Hq, Hkv, d = 32, 8, 128
+        Hq, Hkv, d = (int(v) for v in rest[0].split("x")) if rest else (32, 8, 128)
         x = make_chunked_inputs([ctxn] * n, [qn] * n, Hq=Hq, Hkv=Hkv, d=d, seed=11)
         args_ = [t.to(dev) for t in (x.q, x.k_cache, x.v_cache, x.block_table, x.cu_seqlens_q, x.seq_lens)]
         o = torch.empty_like(args_[0])
