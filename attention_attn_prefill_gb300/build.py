@@ -51,21 +51,28 @@ def _stamp(extra: list[str]) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile and link libattn.so; returns its path."""
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          variant: str | None = None) -> str:
+    """Compile and link libattn.so; returns its path.
+
+    variant: a named build with extra_flags (for example a test-only variant), linked to
+    _build/<variant>/libattn_<variant>.so instead of the package's libattn.so.
+    """
     extra = list(extra_flags or [])
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    stamp_file = os.path.join(BUILD_DIR, "stamp")
+    build_dir = BUILD_DIR if variant is None else os.path.join(BUILD_DIR, variant)
+    lib_path = LIB_PATH if variant is None else os.path.join(build_dir, f"libattn_{variant}.so")
+    os.makedirs(build_dir, exist_ok=True)
+    stamp_file = os.path.join(build_dir, "stamp")
     stamp = _stamp(extra)
-    if not force and os.path.exists(LIB_PATH) and os.path.exists(stamp_file):
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp_file):
         with open(stamp_file) as f:
             if f.read().strip() == stamp:
-                return LIB_PATH
+                return lib_path
     nvcc = nvcc_path()
     objs = []
     cmds = []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(obj)
         cmds.append([nvcc] + NVCC_FLAGS + extra + ["-c", os.path.join(CSRC, src), "-o", obj])
 
@@ -80,12 +87,12 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
 
     with cf.ThreadPoolExecutor(max_workers=len(cmds)) as ex:
         list(ex.map(run, cmds))
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs)
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, lib_path)
     with open(stamp_file, "w") as f:
         f.write(stamp)
-    return LIB_PATH
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -41,6 +41,13 @@ namespace attn {
 
 __device__ uint32_t g_decode_status;
 
+#ifdef ATTN_TEST_DROP_COPY
+// Test-only builds (never the product library): when set, warp 0 of split CTA (0, 0, 0) never
+// requests its first page, so the wait for it runs out (after ATTN_WAIT_LIMIT_NS) and the kernel
+// takes its unwinding path and records kDevWaitTimeout.
+__device__ int g_test_drop_copy;
+#endif
+
 namespace {
 
 constexpr int PAGE = 16;
@@ -336,6 +343,9 @@ __global__ void __launch_bounds__(NW * 32)
   const int n_my = npages > wstart ? (npages - wstart + wstep - 1) / wstep : 0;
 
   auto issue = [&](int k) {
+#ifdef ATTN_TEST_DROP_COPY
+    if (g_test_drop_copy && k == 0 && warp == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) return;
+#endif
     const int pi = page_at(wstart + k * wstep);
     int pid = p.block_table[static_cast<size_t>(n) * p.max_blocks + pi];
     if (pid < 0 || pid >= p.num_blocks) {
@@ -1112,6 +1122,12 @@ cudaError_t decode_balanced_launch(int d, const DecodeMaps& maps, const Balanced
   }
   return cudaErrorInvalidValue;
 }
+
+#ifdef ATTN_TEST_DROP_COPY
+extern "C" int attn_test_drop_copy(int on) {
+  return static_cast<int>(cudaMemcpyToSymbol(g_test_drop_copy, &on, sizeof(int)));
+}
+#endif
 
 cudaError_t decode_status(uint32_t* out, bool clear) {
   cudaError_t e = cudaMemcpyFromSymbol(out, g_decode_status, sizeof(uint32_t));
