@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int RPC = 8 / WPR;           // rows per CTA of 8 warps
   constexpr int PER = D / 32;            // output columns per lane
-  constexpr int U = D <= 128 ? 8 : 4;    // slots in flight per warp
+  constexpr int U = 8;                   // slots in flight per warp
   __shared__ __align__(16) float s_acc[WPR > 1 ? 8 : 1][WPR > 1 ? D : 1];
   __shared__ float s_w[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -544,9 +544,21 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   const float* pm = part_m + rbase;
   const float* pl = part_l + rbase;
   float M = -INFINITY;
-  if (live)
-    for (int i = lane; i < nvalid; i += 32)
-      if (pl[i] > 0.f) M = fmaxf(M, pm[i]);
+  if (live) {
+    // all of a lane's loads of a pass are issued before any is used
+    for (int i0 = lane; i0 < nvalid; i0 += 32 * 4) {
+      float lv[4], mv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + 32 * u;
+        lv[u] = i < nvalid ? pl[i] : 0.f;
+        mv[u] = i < nvalid ? pm[i] : -INFINITY;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (lv[u] > 0.f) M = fmaxf(M, mv[u]);
+    }
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float acc[PER];
@@ -1055,7 +1067,7 @@ cudaError_t launch_combine(const float* part_o, const float* part_m, const float
                            const CombineGeometry& geo, __nv_bfloat16* o, float* lse, cudaStream_t stream) {
   // warps per row: enough that each warp has about U slots, at most the CTA's 8, and fewer when
   // the rows alone give every SM work
-  constexpr int U = D <= 128 ? 8 : 4;
+  constexpr int U = 8;  // slots a warp has in flight (as in the kernel)
   int wpr = splits <= U ? 1 : splits <= 2 * U ? 2 : splits <= 4 * U ? 4 : 8;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
