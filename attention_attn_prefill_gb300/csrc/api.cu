@@ -148,6 +148,25 @@ attn_status_t prefill_common(const void* q, const void* k, const void* v, void* 
   if (static_cast<int64_t>(p.num_qblocks) * p.B * p.Hq > (int64_t(1) << 30)) return ATTN_ERR_INVALID_ARG;
   p.div_heads = attn::FastDiv::make(static_cast<uint32_t>(p.Hq));
   p.div_level = attn::FastDiv::make(static_cast<uint32_t>(p.B * p.Hq));
+  // Chunked prefill over a paged cache whose keys and values (at most max_blocks pages a sequence)
+  // exceed half of L2 is walked in blocks of sequences whose keys and values take at most half of L2:
+  // every query tile streams its sequence's whole cached context, and level by level over all
+  // sequences that context would come from HBM once per level.  (For prompts prefilled from scratch
+  // the plain longest-first walk measured faster: there the blocks' tails are unbalanced.)
+  p.seq_block = p.B;
+  if (paged != nullptr) {
+    const int64_t kv_max = std::max<int64_t>(max_seqlen, static_cast<int64_t>(paged->max_blocks) * kPage);
+    const int64_t kv_seq_bytes = std::max<int64_t>(1, kv_max * Hkv * d * 2 * 2);
+    int l2_bytes = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (kv_seq_bytes * p.B > l2_bytes / 2)
+      p.seq_block = static_cast<int>(std::min<int64_t>(p.B, std::max<int64_t>(1, (l2_bytes / 2) / kv_seq_bytes)));
+  }
+  const int blocks = (p.B + p.seq_block - 1) / p.seq_block;
+  p.div_block_level = attn::FastDiv::make(static_cast<uint32_t>(p.seq_block * p.Hq));
+  p.div_block_level_last = attn::FastDiv::make(static_cast<uint32_t>((p.B - (blocks - 1) * p.seq_block) * p.Hq));
+  p.div_block = attn::FastDiv::make(static_cast<uint32_t>(p.seq_block * p.Hq * p.num_qblocks));
   if (cta2) return from_cuda(attn::prefill_cta2_launch(maps, p, static_cast<cudaStream_t>(stream)));
   return from_cuda(attn::prefill_launch(d, maps, p, static_cast<cudaStream_t>(stream)));
 }

@@ -114,14 +114,16 @@ struct Layout {
 
 using pf::WorkTile;
 
-// The walk over this kernel's work tiles (one query head each); errors go to this kernel's status.
-struct TileWalk : pf::TileWalk {
+// The walk over this kernel's work tiles (one query head each), in the order of Base (pf::TileWalk
+// or pf::BlockedTileWalk); errors go to this kernel's status.
+template <class Base>
+struct WalkOf : Base {
   __device__ __forceinline__ bool next(const PrefillParams& p, WorkTile& t) {
-    return pf::TileWalk::next(p, t, &g_prefill_status);
+    return Base::next(p, t, &g_prefill_status);
   }
 };
 
-template <int D>
+template <int D, class TileWalk>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -525,9 +527,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 int g_num_sms = 0;
 
-template <int D>
+template <int D, class Walk>
 cudaError_t launch(const PrefillMaps& m, const PrefillParams& p, cudaStream_t stream) {
-  auto kern = prefill_fwd_kernel<D>;
+  auto kern = prefill_fwd_kernel<D, Walk>;
   const int smem = Layout<D>::ALLOC;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -549,9 +551,12 @@ int prefill_tile_rows() { return BM; }
 int prefill_kv_tile_rows(int d) { return d <= 128 ? Layout<128>::BN : Layout<256>::BN; }
 
 cudaError_t prefill_launch(int d, const PrefillMaps& maps, const PrefillParams& p, cudaStream_t stream) {
-  if (d == 64) return launch<64>(maps, p, stream);
-  if (d == 128) return launch<128>(maps, p, stream);
-  if (d == 256) return launch<256>(maps, p, stream);
+  using Plain = WalkOf<pf::TileWalk>;
+  using Blocked = WalkOf<pf::BlockedTileWalk>;
+  const bool blocked = p.seq_block < p.B;
+  if (d == 64) return blocked ? launch<64, Blocked>(maps, p, stream) : launch<64, Plain>(maps, p, stream);
+  if (d == 128) return blocked ? launch<128, Blocked>(maps, p, stream) : launch<128, Plain>(maps, p, stream);
+  if (d == 256) return blocked ? launch<256, Blocked>(maps, p, stream) : launch<256, Plain>(maps, p, stream);
   return cudaErrorInvalidValue;
 }
 

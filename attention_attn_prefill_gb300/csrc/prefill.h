@@ -55,6 +55,13 @@ struct PrefillParams {
   int num_qblocks;   // query tiles of the longest sequence: ceil(S or max_seqlen / 128)
   FastDiv div_heads;  // by Hq
   FastDiv div_level;  // by B * Hq: work tiles per query-tile level
+  // Blocked walk (BlockedTileWalk): the sequences in blocks of seq_block (the last block may hold
+  // fewer), each block longest tile first, so that a block's keys and values stay in L2 while its
+  // query tiles run.
+  int seq_block;
+  FastDiv div_block_level;       // by seq_block * Hq: work tiles per query-tile level of a full block
+  FastDiv div_block_level_last;  // by (B - (blocks - 1) * seq_block) * Hq: the same for the last block
+  FastDiv div_block;             // by seq_block * Hq * num_qblocks: work tiles of a full block
 };
 
 int prefill_rows_per_cta();

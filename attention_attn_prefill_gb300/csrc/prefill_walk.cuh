@@ -82,5 +82,53 @@ struct TileWalk {
   }
 };
 
+// The same list with the sequences taken in blocks of p.seq_block whose keys and values fit in part
+// of L2, each block walked longest tile first; used when all of a batch's keys and values do not fit
+// in L2, so that the query tiles of one level do not evict what the next level reads again.
+struct BlockedTileWalk {
+  int v = 0;
+  __device__ __forceinline__ bool next(const PrefillParams& p, WorkTile& t, uint32_t* status) {
+    const int G = gridDim.x, c = blockIdx.x;
+    const int total = p.B * p.Hq * p.num_qblocks;
+    const int per_block = p.seq_block * p.Hq * p.num_qblocks;
+    while (true) {
+      const int idx = v * G + ((v & 1) ? (G - 1 - c) : c);
+      ++v;
+      if (idx >= total) return false;
+      const int blk = static_cast<int>(p.div_block.div(static_cast<uint32_t>(idx)));
+      const int r = idx - blk * per_block;
+      const int b0 = blk * p.seq_block;
+      const bool last = b0 + p.seq_block > p.B;
+      const int per_qt = (last ? p.B - b0 : p.seq_block) * p.Hq;
+      const int level = static_cast<int>((last ? p.div_block_level_last : p.div_block_level).div(static_cast<uint32_t>(r)));
+      t.qt = p.num_qblocks - 1 - level;
+      const int rem = r - level * per_qt;
+      const int bi = static_cast<int>(p.div_heads.div(static_cast<uint32_t>(rem)));
+      t.b = b0 + bi;
+      t.hq = rem - bi * p.Hq;
+      if (p.cu_seqlens == nullptr) {
+        t.base = 0;
+        t.z = t.b;
+        t.len = t.kv_len = p.S;
+        t.q_off = 0;
+        return true;
+      }
+      const int s0 = p.cu_seqlens[t.b], s1 = p.cu_seqlens[t.b + 1];
+      const int kvl = p.kv_lens != nullptr ? p.kv_lens[t.b] : s1 - s0;
+      if (s0 < 0 || s1 < s0 || s1 > p.S || s1 - s0 > p.num_qblocks * BM || kvl < s1 - s0 ||
+          (p.kv_lens != nullptr && kvl > p.max_blocks * 16)) {
+        set_error(status, kDevBadSeqlens);
+        continue;  // the sequence is skipped
+      }
+      t.base = s0;
+      t.z = 0;
+      t.len = s1 - s0;
+      t.kv_len = kvl;
+      t.q_off = kvl - t.len;
+      if (t.qt * BM < t.len) return true;
+    }
+  }
+};
+
 }  // namespace pf
 }  // namespace attn
