@@ -119,6 +119,26 @@ def test_auto_split_tokens(attn, gpu):
     compare(attn, x, 2.0 ** -4, gpu, f"auto ({t}-token groups)", seqs=live, split_tokens="auto")
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_random_shapes_and_split_modes(attn, gpu, seed):
+    """Seeded random batches (empty, one-token and long sequences; 1 to 8 query heads per KV head;
+    d = 128 or 256) under a random split choice; every non-empty sequence against the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    N = int(rng.integers(1, 24))
+    lens = [int(v) for v in rng.choice([0, 1, 15, 16, 17, 300, 1000, 2500, 5000], size=N)]
+    lens[int(rng.integers(0, N))] = int(rng.integers(1, 6000))
+    Hq, Hkv = [(8, 1), (16, 2), (12, 4), (32, 8), (6, 6)][int(rng.integers(0, 5))]
+    d = [128, 256][int(rng.integers(0, 2))]
+    x = make_decode_inputs(lens, Hq=Hq, Hkv=Hkv, d=d, seed=2000 + seed, nan_tail=True, extra_blocks=2)
+    modes = [dict(num_splits=int(rng.integers(1, 21))), dict(split_tokens=int(rng.choice([16, 48, 512, 1024]))),
+             dict(num_splits=0), dict(split_tokens="auto")]
+    kw = modes[seed % len(modes)]
+    live = [n for n, L in enumerate(lens) if L > 0]
+    if not live:
+        return
+    compare(attn, x, float(d) ** -0.5, gpu, f"seed {seed} N={N} G={Hq // Hkv} d={d} {kw}", seqs=live, **kw)
+
+
 def test_bad_page_is_reported(attn, gpu):
     """A block-table entry outside [0, num_blocks) is recorded as a device error, not read."""
     x = make_decode_inputs([40], Hq=4, Hkv=1, d=128, seed=57)
