@@ -10,9 +10,11 @@
 // rescale of this library): the exponentials are taken
 // against a reference max per row.  That is exact for any reference, because O and l always refer to
 // the same one, and nothing overflows while every p stays below 2^32.  The first step of a tile
-// takes the row max as the reference.  A later step keeps the reference unless one of this thread's
-// partial row sums leaves that range.  Only then does it take the row max, move the reference
-// (rescaling O and l when the max has grown by more than 2^8) and compute its P again.
+// takes the score of key 0 (visible to every row of a first key tile) as the reference, one shuffle
+// instead of a row max.  Every step keeps the reference unless one of this thread's partial row sums
+// leaves that range.  Only then does it take the row max, move the reference (rescaling O and l when
+// the max has grown by more than 2^8, except on the first step, which has no O or l yet) and compute
+// its P again.
 #pragma once
 
 #include <cstdint>
@@ -47,6 +49,7 @@ __device__ __forceinline__ void softmax_step(const PrefillParams& p, const WorkT
                                              uint32_t s_tmem, uint32_t o_tmem, int qa, int qb, int cq, float c2,
                                              uint64_t c2x2, uint64_t* pv_done, SoftmaxRows& st, bool& ok) {
   constexpr int NG = BN / 8;  // 8-column groups per S tile
+  const int lane_row0 = (threadIdx.x & 31) & ~3;
   uint32_t sr[4 * NG];
   tmem_ld16_256b<NG>(s_tmem, sr);
   tmem_ld_wait();
@@ -79,7 +82,13 @@ __device__ __forceinline__ void softmax_step(const PrefillParams& p, const WorkT
   bool rescale_o = false;
   uint32_t pk[2 * NG];
   float ps_a = 0.f, ps_b = 0.f;  // this step's shares of the two row sums
-  const bool need_max = __any_sync(0xffffffffu, j == 0 || !(st.m_a > -INFINITY) || !(st.m_b > -INFINITY));
+  if (j == 0) {
+    // first key tile: key 0 is visible to every row, so its score is a finite reference (the thread
+    // holding column 0 of the row shares it); a later overflow check falls back to the row max
+    st.m_a = __shfl_sync(0xffffffffu, __uint_as_float(sr[0]), lane_row0);
+    st.m_b = __shfl_sync(0xffffffffu, __uint_as_float(sr[2]), lane_row0);
+  }
+  const bool need_max = __any_sync(0xffffffffu, !(st.m_a > -INFINITY) || !(st.m_b > -INFINITY));
   for (int pass = need_max ? 1 : 0; pass < 2; ++pass) {
     if (pass == 1) {
       float mxa = -INFINITY, mxb = -INFINITY;
@@ -93,7 +102,7 @@ __device__ __forceinline__ void softmax_step(const PrefillParams& p, const WorkT
       mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
       mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
       mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
-      if (!(st.m_a > -INFINITY)) {
+      if (j == 0 || !(st.m_a > -INFINITY)) {  // step 0 has no O or l of this tile yet: nothing to rescale
         st.m_a = mxa;
       } else if ((mxa - st.m_a) * c2 > RESCALE_LOG2_THRESHOLD) {
         alpha_a = ex2_approx((st.m_a - mxa) * c2);
@@ -101,7 +110,7 @@ __device__ __forceinline__ void softmax_step(const PrefillParams& p, const WorkT
         st.m_a = mxa;
         rescale_o = true;
       }
-      if (!(st.m_b > -INFINITY)) {
+      if (j == 0 || !(st.m_b > -INFINITY)) {
         st.m_b = mxb;
       } else if ((mxb - st.m_b) * c2 > RESCALE_LOG2_THRESHOLD) {
         alpha_b = ex2_approx((st.m_b - mxb) * c2);
