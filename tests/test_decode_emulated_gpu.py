@@ -198,32 +198,34 @@ def test_worked_example_every_backend(attn, gpu):
 @pytest.fixture(scope="module")
 def longctx():
     x = decode_inputs_for(LONGCTX)
-    seqs = [2, 7]
-    want = oa.decode_paged(x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens, LONGCTX.scale, seqs=seqs)
-    return x, seqs, want
+    return x, oa.decode_paged(x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens, LONGCTX.scale)
+
+
+@pytest.fixture(scope="module")
+def paged():
+    x = decode_inputs_for(PAGED)
+    return x, oa.decode_paged(x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens, PAGED.scale)
 
 
 @pytest.mark.parametrize("backend", BACKENDS)
 def test_longctx_full_size(attn, gpu, backend, longctx):
-    """8 sequences up to 122,863 tokens, d = 256, each backend's B200 (148 SMs) group count; two checked."""
-    x, seqs, (wo, wl) = longctx
+    """8 sequences up to 122,863 tokens, d = 256, each backend's B200 (148 SMs) group count; every output."""
+    x, (wo, wl) = longctx
     args = [t.to(gpu) for t in (x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens)]
     o, lse, _ = attn.decode_paged_emulated(*args, numerics=backend, sm_count=148, scale=LONGCTX.scale,
                                            max_tokens=int(x.seq_lens.max()))
     torch.cuda.synchronize()
-    check_o(to_np(o)[seqs], wo[seqs], f"longctx {backend}")
-    check_backend_lse(backend, to_np(lse)[seqs], wl[seqs], f"longctx {backend}")
+    check_o(to_np(o), wo, f"longctx {backend}")
+    check_backend_lse(backend, to_np(lse), wl, f"longctx {backend}")
 
 
 @pytest.mark.parametrize("backend", BACKENDS)
-def test_paged_full_size(attn, gpu, backend):
-    """64 sequences of U[512, 8192] tokens, GQA 32:8, d = 128; eight sequences checked."""
-    x = decode_inputs_for(PAGED)
-    seqs = list(range(3, 64, 8))
+def test_paged_full_size(attn, gpu, backend, paged):
+    """64 sequences of U[512, 8192] tokens, GQA 32:8, d = 128, this GPU's group counts; every output."""
+    x, (wo, wl) = paged
     args = [t.to(gpu) for t in (x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens)]
     o, lse, _ = attn.decode_paged_emulated(*args, numerics=backend, scale=PAGED.scale,
                                            max_tokens=int(x.seq_lens.max()))
     torch.cuda.synchronize()
-    wo, wl = oa.decode_paged(x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens, PAGED.scale, seqs=seqs)
-    check_o(to_np(o)[seqs], wo[seqs], f"paged {backend}")
-    check_backend_lse(backend, to_np(lse)[seqs], wl[seqs], f"paged {backend}")
+    check_o(to_np(o), wo, f"paged {backend}")
+    check_backend_lse(backend, to_np(lse), wl, f"paged {backend}")
