@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(NW * 32)
 //
 // WPR warps share a row and take its slots round-robin, each loading U slots at a time so that
 // their loads are in flight together; the warps' sums (all at the same M) are then added through
-// shared memory.  With a row's group count known (geometry g.seq_lens != null) only its groups
+// shared memory.  With a row's group count known (geo.seq_lens != null) only its groups
 // are visited, so slots past them need not have been written; otherwise every slot is visited and
 // a slot counts only if its l_i > 0.
 template <int D, int WPR>
