@@ -27,6 +27,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "prefill.h"
 #include "prefill_tile.cuh"
@@ -107,10 +108,48 @@ struct PairWalk {
   }
 };
 
+// The same list for packed sequences (cu_seqlens, and with paged K/V kv_lens): units past a sequence's
+// end are skipped, alike in both CTAs of a pair, and a sequence with bad bounds is recorded and skipped.
+struct PackedPairWalk {
+  int v = 0;
+  __device__ __forceinline__ bool next(const PrefillParams& p, WorkTile& t, int rank) {
+    const int G = static_cast<int>(num_clusters_x()), c = static_cast<int>(cluster_id_x());
+    const int pairs = p.Hq >> 1;
+    const int per_qt = p.B * pairs;
+    const int total = per_qt * p.num_qblocks;
+    while (true) {
+      const int idx = v * G + ((v & 1) ? (G - 1 - c) : c);
+      ++v;
+      if (idx >= total) return false;
+      const int level = static_cast<int>(p.div_level.div(static_cast<uint32_t>(idx)));
+      t.qt = p.num_qblocks - 1 - level;
+      const int rem = idx - level * per_qt;
+      t.b = static_cast<int>(p.div_heads.div(static_cast<uint32_t>(rem)));
+      t.hq = 2 * (rem - t.b * pairs) + rank;
+      const int s0 = p.cu_seqlens[t.b], s1 = p.cu_seqlens[t.b + 1];
+      const int kvl = p.kv_lens != nullptr ? p.kv_lens[t.b] : s1 - s0;
+      if (s0 < 0 || s1 < s0 || s1 > p.S || s1 - s0 > p.num_qblocks * BM || kvl < s1 - s0 ||
+          (p.kv_lens != nullptr && kvl > p.max_blocks * 16)) {
+        if (rank == 0) set_error(&g_prefill_cta2_status, kDevBadSeqlens);
+        continue;  // the sequence is skipped
+      }
+      t.base = s0;
+      t.z = 0;
+      t.len = s1 - s0;
+      t.kv_len = kvl;
+      t.q_off = kvl - t.len;
+      if (t.qt * BM < t.len) return true;
+    }
+  }
+};
+
+// PACKED: packed sequences (PackedPairWalk), with contiguous or paged K/V; tm_vrow (one-row V boxes,
+// paged K/V only) fetches the last, partial page of a sequence row by row.
+template <bool PACKED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                        const PrefillParams p) {
+                        const __grid_constant__ CUtensorMap tm_vrow, const PrefillParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if ((smem_u32(smem) & 1023u) != 0) {  // both CTAs see the same launch: both return
     if (threadIdx.x == 0) set_error(&g_prefill_cta2_status, kDevMisaligned);
@@ -145,7 +184,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const int G = p.Hq / p.Hkv;
   auto wait = [&](uint64_t* bar, uint32_t parity) { return __all_sync(0xffffffffu, mbar_wait(bar, parity)); };
   auto tile_nkv = [&](const WorkTile& t) { return pf::tile_nkv<BN>(p, t); };
-  struct Walk : PairWalk {};
+  struct Walk : std::conditional_t<PACKED, PackedPairWalk, PairWalk> {};
 
   if (warp == PRODUCER_WARP && lane == 0) {
     for (int s = 0; s < Q_STAGES; ++s) {
@@ -222,25 +261,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           }
           if (lane == 0) {
             const uint32_t bar = cluster_addr(&q_full[qs], 0);
-            for (int c = 0; c < CHUNKS; ++c)
-              tma_load_3d_pair(sQ + qs * Q_BYTES + c * Q_PANEL, &tm_q, bar, t.hq * D + c * 64, t.qt * BM, t.z);
+            for (int c = 0; c < CHUNKS; ++c) {
+              if constexpr (PACKED)
+                tma_load_3d_pair(sQ + qs * Q_BYTES + c * Q_PANEL, &tm_q, bar, t.hq * D + c * 64, t.base + t.qt * BM,
+                                 t.z);
+              else
+                tma_load_3d_pair(sQ + qs * Q_BYTES + c * Q_PANEL, &tm_q, bar, t.hq * D + c * 64, t.qt * BM, t.z);
+            }
           }
           nq = k + 1;
         }
         const int nkv = tile_nkv(t);
         for (int j = 0; j < nkv; ++j) {
           const int st = issued % nst;
+          // paged K/V: lane l reads, before the wait, the physical page of this CTA's l-th page of the
+          // key tile -- for K its half (keys 64 * rank .. + 63: 4 pages), for V all 8 pages
+          constexpr int PAGES = BN / 16;
+          const int npg = is_k ? PAGES / 2 : PAGES;
+          const int page_first = is_k ? j * PAGES + rank * (PAGES / 2) : j * PAGES;
+          int my_pid = -1;
+          if constexpr (PACKED) {
+            if (p.kv_lens != nullptr && lane < npg && (page_first + lane) * 16 < t.kv_len)
+              my_pid = p.block_table[static_cast<size_t>(t.b) * p.max_blocks + page_first + lane];
+          }
           ok = wait(&empty[st], ((issued / nst) & 1) ^ 1);
           if (!ok) break;
           const uint32_t bar = cluster_addr(&full[st], 0);
-          if (is_k) {
-            // keys j * BN + 64 * rank .. + 63, both 64-column panels of d
-            if (lane < CHUNKS)
-              tma_load_3d_pair(sK + st * K_BYTES + lane * KH_PANEL, &tm_k, bar, g * D + lane * 64,
-                               j * BN + rank * KH_ROWS, t.z);
-          } else if (lane == 0) {
-            // all BN keys, head-dim columns 64 * rank .. + 63
-            tma_load_3d_pair(sV + st * V_BYTES, &tm_v, bar, g * D + rank * 64, j * BN, t.z);
+          if constexpr (!PACKED) {
+            if (is_k) {
+              // keys j * BN + 64 * rank .. + 63, both 64-column panels of d
+              if (lane < CHUNKS)
+                tma_load_3d_pair(sK + st * K_BYTES + lane * KH_PANEL, &tm_k, bar, g * D + lane * 64,
+                                 j * BN + rank * KH_ROWS, t.z);
+            } else if (lane == 0) {
+              // all BN keys, head-dim columns 64 * rank .. + 63
+              tma_load_3d_pair(sV + st * V_BYTES, &tm_v, bar, g * D + rank * 64, j * BN, t.z);
+            }
+          } else if (p.kv_lens == nullptr) {
+            // packed sequences, contiguous K/V: the same boxes from the sequence's first token
+            if (is_k) {
+              if (lane < CHUNKS)
+                tma_load_3d_pair(sK + st * K_BYTES + lane * KH_PANEL, &tm_k, bar, g * D + lane * 64,
+                                 t.base + j * BN + rank * KH_ROWS, t.z);
+            } else if (lane == 0) {
+              tma_load_3d_pair(sV + st * V_BYTES, &tm_v, bar, g * D + rank * 64, t.base + j * BN, t.z);
+            }
+          } else {
+            // paged K/V, one 16-row box per page: K lane l takes page l / 2 of this CTA's half and
+            // panel l % 2 of d; V lane l takes page l and this CTA's panel (rank).  Pages past the
+            // sequence are read from rows past the cache, which the copy fills with zeros.
+            const int src = is_k ? lane / CHUNKS : lane;
+            int pid = __shfl_sync(0xffffffffu, my_pid, src < npg ? src : 0);
+            const int pp = src, c = is_k ? lane % CHUNKS : rank;
+            if (is_k ? lane < npg * CHUNKS : lane < npg) {
+              const int oob = p.num_blocks * 16;
+              const int valid = t.kv_len - (page_first + pp) * 16;  // rows of this page that hold keys
+              int row0 = oob;
+              if (valid > 0) {
+                if (pid < 0 || pid >= p.num_blocks) {
+                  set_error(&g_prefill_cta2_status, kDevBadPage);
+                  pid = 0;
+                }
+                row0 = pid * 16;
+              }
+              uint8_t* dst = is_k ? sK + st * K_BYTES + c * KH_PANEL + pp * 16 * PANEL_ROW
+                                  : sV + st * V_BYTES + pp * 16 * PANEL_ROW;
+              if (!is_k && valid > 0 && valid < 16) {
+                // the V rows past the last key must be finite (P is 0 there, but 0 * NaN is not):
+                // row by row, the tail from past the cache
+#pragma unroll 1
+                for (int r = 0; r < 16; ++r)
+                  tma_load_3d_pair(dst + r * PANEL_ROW, &tm_vrow, bar, c * 64, g, r < valid ? row0 + r : oob);
+              } else {
+                tma_load_3d_pair(dst, is_k ? &tm_k : &tm_v, bar, c * 64, g, row0);
+              }
+            }
           }
           ++issued;
         }
@@ -404,11 +499,14 @@ int g_num_sms = 0;
 }  // namespace
 
 bool prefill_cta2_supported(int d, int Hq, int Hkv, bool packed) {
-  return d == D && !packed && Hkv > 0 && Hq % Hkv == 0 && (Hq / Hkv) % 2 == 0;
+  (void)packed;  // packed and paged batches take the kernel's packed instance
+  return d == D && Hkv > 0 && Hq % Hkv == 0 && (Hq / Hkv) % 2 == 0;
 }
 
 cudaError_t prefill_cta2_launch(const PrefillMaps& m, const PrefillParams& p_in, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(prefill_cta2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  const bool packed = p_in.cu_seqlens != nullptr;
+  auto kern = packed ? prefill_cta2_kernel<true> : prefill_cta2_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   if (g_num_sms == 0) {
     int dev = 0;
@@ -420,7 +518,7 @@ cudaError_t prefill_cta2_launch(const PrefillMaps& m, const PrefillParams& p_in,
   p.div_level = FastDiv::make(static_cast<uint32_t>(p.B * (p.Hq / 2)));
   const long long units = static_cast<long long>(p.num_qblocks) * p.B * (p.Hq / 2);
   const int clusters = static_cast<int>(units < g_num_sms / 2 ? units : g_num_sms / 2);
-  prefill_cta2_kernel<<<2 * clusters, NUM_THREADS, SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.o, p);
+  kern<<<2 * clusters, NUM_THREADS, SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.o, m.v_row, p);
   return cudaGetLastError();
 }
 
