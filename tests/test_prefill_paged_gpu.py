@@ -83,8 +83,10 @@ def test_chunks_over_more_context_than_l2(attn, gpu):
     compare(attn, x, 1.0 / math.sqrt(128), True, gpu, "blocked walk", heads=[0, 13, 31])
 
 
-def test_bad_page_and_bad_lengths_are_reported(attn, gpu):
-    x = make_chunked_inputs([40, 50], [10, 50], Hq=2, Hkv=1, d=64, seed=93)
+@pytest.mark.parametrize("heads", [(2, 1, 64), (4, 2, 128)], ids=["single-CTA", "CTA-pair"])
+def test_bad_page_and_bad_lengths_are_reported(attn, gpu, heads):
+    Hq, Hkv, d = heads
+    x = make_chunked_inputs([40, 50], [10, 50], Hq=Hq, Hkv=Hkv, d=d, seed=93)
     bt = x.block_table.clone()
     bt[0, 1] = x.k_cache.shape[0] + 5
     x2 = type(x)(x.q, x.k_cache, x.v_cache, bt, x.seq_lens, x.cu_seqlens_q)

@@ -75,10 +75,12 @@ def test_mixed_long_sequences_sampled(attn, gpu):
     compare(attn, x, 1.0 / math.sqrt(128), True, gpu, "mixed lengths", seqs=[1, 2, 4], heads=[0, 13, 31])
 
 
-def test_bad_offsets_are_reported(attn, gpu):
+@pytest.mark.parametrize("heads", [(2, 1, 64), (4, 2, 128)], ids=["single-CTA", "CTA-pair"])
+def test_bad_offsets_are_reported(attn, gpu, heads):
     """Offsets past the tokens or running backwards are recorded as device status 5 and skipped."""
+    Hq, Hkv, d = heads
     lens = [40, 60, 30]
-    x = make_varlen_inputs(lens, Hq=2, Hkv=1, d=64, seed=80)
+    x = make_varlen_inputs(lens, Hq=Hq, Hkv=Hkv, d=d, seed=80)
     cu = x.cu_seqlens.clone()
     cu[2] = 200                  # sequence 1 ends past the 130 tokens, sequence 2 runs backwards
     x2 = type(x)(x.q, x.k, x.v, cu, 0)
