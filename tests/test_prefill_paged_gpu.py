@@ -74,15 +74,16 @@ def test_long_context_chunks_sampled(attn, gpu):
     compare(attn, x, 1.0 / math.sqrt(128), True, gpu, "long chunks", seqs=[1, 3], heads=[0, 9, 31])
 
 
-@pytest.mark.parametrize("Hq", [32, 24], ids=["CTA-pair", "single-CTA"])
+@pytest.mark.parametrize("Hq", [8, 6], ids=["CTA-pair", "single-CTA"])
 def test_chunks_over_more_context_than_l2(attn, gpu, Hq):
-    """Eleven sequences whose cached keys and values (about 200 MB) exceed half of L2: the walk takes
-    them in blocks of a few sequences (the last block partial); every sequence is checked, in both
-    kernels (4 and 3 query heads per KV head)."""
-    ctx = [4096, 3000, 4096, 2500, 4096, 3900, 4096, 2048, 4096, 3333, 4096]
-    ql = [512, 300, 512, 257, 512, 400, 128, 512, 1, 333, 512]
-    x = make_chunked_inputs(ctx, ql, Hq=Hq, Hkv=8, d=128, seed=94)
-    compare(attn, x, 1.0 / math.sqrt(128), True, gpu, "blocked walk", heads=[0, 13, Hq - 1])
+    """Nineteen sequences whose cached keys and values (4 MB a sequence at the block table's 4096
+    tokens, about 80 MB in all) exceed half of L2: the walk takes them in blocks of a few sequences,
+    the last block partial; every sequence is checked, in both kernels (4 and 3 query heads per KV
+    head)."""
+    ctx = [4096, 3000, 4096, 2500, 4096, 3900, 4096, 2048, 4096, 3333, 4096, 1, 4000, 4096, 700, 4096, 2222, 4096, 3500]
+    ql = [512, 300, 512, 257, 512, 400, 128, 512, 1, 333, 512, 1, 129, 64, 700, 200, 17, 511, 256]
+    x = make_chunked_inputs(ctx, ql, Hq=Hq, Hkv=2, d=128, seed=94)
+    compare(attn, x, 1.0 / math.sqrt(128), True, gpu, "blocked walk", heads=[0, 5, Hq - 1])
 
 
 @pytest.mark.parametrize("heads", [(2, 1, 64), (4, 2, 128)], ids=["single-CTA", "CTA-pair"])
