@@ -22,7 +22,8 @@
 //     The even CTA's commits reach both CTAs' barriers (multicast); the odd CTA's softmax and
 //     epilogue warps arrive on the even CTA's p_full and o_free (relaxed arrivals, after their TMEM
 //     stores or loads have completed and a tcgen05 fence);
-//   * sequences are a batch of equal length (packed sequences and paged K/V use the single-head kernel).
+//   * packed sequences (cu_seqlens) and paged K/V (block table) take the instances with PACKED set:
+//     each CTA copies its half of a K tile as 4 pages x 2 panels and its V panel as 8 pages.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -112,35 +113,35 @@ struct PairWalk {
 // end are skipped, alike in both CTAs of a pair, and a sequence with bad bounds is recorded and skipped.
 // BLOCKED (chunked prefill over a paged cache larger than half of L2): the list is cut into blocks of
 // p.seq_block sequences, each block walked longest unit first before the next, so that a block's
-// cached keys and values stay in L2 while all its query tiles stream them.  It is a separate instance:
-// where the batch fits L2 the extra index arithmetic measured 2-3% slower.
+// cached keys and values stay in L2 while all its query tiles stream them.  Every block counts
+// p.seq_block sequences; the last one's units past the batch are skipped.  It is a separate
+// instance: where the batch fits L2 the extra index arithmetic measured 2-3% slower.
 template <bool BLOCKED>
 struct PackedPairWalk {
   int v = 0;
   __device__ __forceinline__ bool next(const PrefillParams& p, WorkTile& t, int rank) {
     const int G = static_cast<int>(num_clusters_x()), c = static_cast<int>(cluster_id_x());
     const int pairs = p.Hq >> 1;
-    const int total = p.B * pairs * p.num_qblocks;
+    const int seqs = BLOCKED ? (p.B + p.seq_block - 1) / p.seq_block * p.seq_block : p.B;
+    const int total = seqs * pairs * p.num_qblocks;
     while (true) {
       const int idx = v * G + ((v & 1) ? (G - 1 - c) : c);
       ++v;
       if (idx >= total) return false;
       int r = idx, b0 = 0, per_qt = p.B * pairs;
-      FastDiv div_level = p.div_level;
       if constexpr (BLOCKED) {
         const int blk = static_cast<int>(p.div_block.div(static_cast<uint32_t>(idx)));
         r = idx - blk * p.seq_block * pairs * p.num_qblocks;
         b0 = blk * p.seq_block;
-        const bool last = b0 + p.seq_block > p.B;
-        per_qt = (last ? p.B - b0 : p.seq_block) * pairs;
-        div_level = last ? p.div_block_level_last : p.div_block_level;
+        per_qt = p.seq_block * pairs;
       }
-      const int level = static_cast<int>(div_level.div(static_cast<uint32_t>(r)));
+      const int level = static_cast<int>((BLOCKED ? p.div_block_level : p.div_level).div(static_cast<uint32_t>(r)));
       t.qt = p.num_qblocks - 1 - level;
       const int rem = r - level * per_qt;
       const int bi = static_cast<int>(p.div_heads.div(static_cast<uint32_t>(rem)));
       t.b = b0 + bi;
       t.hq = 2 * (rem - bi * pairs) + rank;
+      if (BLOCKED && t.b >= p.B) continue;  // past the batch, in the last block
       const int s0 = p.cu_seqlens[t.b], s1 = p.cu_seqlens[t.b + 1];
       const int kvl = p.kv_lens != nullptr ? p.kv_lens[t.b] : s1 - s0;
       if (s0 < 0 || s1 < s0 || s1 > p.S || s1 - s0 > p.num_qblocks * BM || kvl < s1 - s0 ||
@@ -534,9 +535,7 @@ cudaError_t prefill_cta2_launch(const PrefillMaps& m, const PrefillParams& p_in,
   p.div_heads = FastDiv::make(static_cast<uint32_t>(p.Hq / 2));
   p.div_level = FastDiv::make(static_cast<uint32_t>(p.B * (p.Hq / 2)));
   // the blocked walk's divisors, counted in head pairs
-  const int blocks = (p.B + p.seq_block - 1) / p.seq_block;
   p.div_block_level = FastDiv::make(static_cast<uint32_t>(p.seq_block * (p.Hq / 2)));
-  p.div_block_level_last = FastDiv::make(static_cast<uint32_t>((p.B - (blocks - 1) * p.seq_block) * (p.Hq / 2)));
   p.div_block = FastDiv::make(static_cast<uint32_t>(p.seq_block * (p.Hq / 2) * p.num_qblocks));
   const long long units = static_cast<long long>(p.num_qblocks) * p.B * (p.Hq / 2);
   const int clusters = static_cast<int>(units < g_num_sms / 2 ? units : g_num_sms / 2);
