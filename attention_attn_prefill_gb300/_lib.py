@@ -50,6 +50,8 @@ _SIGNATURES = {
     "attn_split_heuristic": (c_int, [c_int] * 4),
     "attn_prefill_varlen": (c_int, [c_void_p] * 6 + [c_int] * 6 + [c_float, c_int, c_void_p]),
     "attn_prefill_paged": (c_int, [c_void_p] * 8 + [c_int] * 9 + [c_float, c_int, c_void_p]),
+    "attn_prefill_host": (c_int, [c_void_p] * 5 + [c_int] * 4 + [c_float, c_int, c_int, c_void_p, c_size_t, c_void_p]),
+    "attn_prefill_host_workspace_bytes": (c_size_t, [c_int] * 5),
     "attn_decode_auto_splits": (c_int, [c_int] * 4),
     "attn_split_tokens_rule": (c_int, [c_void_p] + [c_int] * 4),
     "attn_decode_auto_split_tokens": (c_int, [c_void_p] + [c_int] * 4),
@@ -185,6 +187,51 @@ def prefill_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         N, int(max_seqlen_q), T, Hq, Hkv, d, page, block_table.shape[1], num_blocks, float(scale),
         1 if causal else 0, _stream_handle(stream))
     _check(st, "attn_prefill_paged")
+    return out, lse
+
+
+def _host(t: torch.Tensor, dtype, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def prefill_host_workspace_bytes(S: int, Hq: int, Hkv: int, d: int, chunks: int = 4) -> int:
+    return int(lib().attn_prefill_host_workspace_bytes(S, Hq, Hkv, d, chunks))
+
+
+def prefill_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None, causal: bool = True,
+                 chunks: int = 4, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                 return_lse: bool = True, workspace: torch.Tensor | None = None, device=None, stream=None):
+    """Prefill of one sequence in host memory: q [S,Hq,d], k/v [S,Hkv,d] bf16 (pinned for overlap) ->
+    (o [S,Hq,d] bf16, lse [Hq,S] f32) in host memory, complete once `stream` reaches the call's end.
+    The transfers overlap the compute inside the call (attn_prefill_host); `workspace` is a device
+    uint8 tensor of prefill_host_workspace_bytes(...) bytes (allocated on `device` if not given)."""
+    S, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (S, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [S, Hkv, d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin)
+    if lse is None and return_lse:
+        lse = torch.empty((Hq, S), dtype=torch.float32, pin_memory=pin)
+    need = prefill_host_workspace_bytes(S, Hq, Hkv, d, chunks)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8,
+                                device=device if device is not None else torch.device("cuda", torch.cuda.current_device()))
+    st = lib().attn_prefill_host(
+        _host(q, torch.bfloat16, "q"), _host(k, torch.bfloat16, "k"), _host(v, torch.bfloat16, "v"),
+        _host(out, torch.bfloat16, "out"), _host(lse, torch.float32, "lse") if lse is not None else None,
+        S, Hq, Hkv, d, float(scale), 1 if causal else 0, int(chunks), _dev(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _stream_handle(stream))
+    _check(st, "attn_prefill_host")
     return out, lse
 
 

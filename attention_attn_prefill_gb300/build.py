@@ -21,7 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libattn.so")
 
-SOURCES = ("api.cu", "prefill.cu", "prefill_cta2.cu", "decode.cu", "decode_noalloc.cu", "merge_emulated.cu")
+SOURCES = ("api.cu", "prefill.cu", "prefill_cta2.cu", "prefill_host.cu", "decode.cu", "decode_noalloc.cu",
+           "merge_emulated.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
                      "--expt-relaxed-constexpr"]

@@ -209,89 +209,6 @@ def traffic_record(kernel: str):
     return rec["bytes_per_launch"] if h.hexdigest() == rec.get("sha256") else None
 
 
-class PipelinedPrefill:
-    """Causal prefill of one sequence from pinned host buffers, with the copies overlapped.
-
-    The sequence's queries are cut into `chunks` chunks of rows; chunk c attends to keys
-    0 .. end of chunk c, which is exactly its rows of the causal prefill.  Each chunk runs through the
-    public chunked-prefill call (attn.prefill_paged) against the sequence's own keys and values,
-    read as a paged cache whose block table is the identity.  Three streams overlap the host-to-device
-    copy of chunk c + 1, the prefill of chunk c and the device-to-host copy of chunk c - 1.  The output
-    lands in the host buffer as [1, S, Hq, d]; the LSE lands chunk-major, [chunks, Hq, S / chunks].
-
-    capture() records one pass (every copy and launch, with the streams' dependencies) as a CUDA
-    graph; a call then replays it, so the host enqueues one graph instead of chunks x six operations.
-    """
-
-    def __init__(self, attn, cfg, dev, host_q, host_k, host_v, host_o, host_lse, chunks: int = 8):
-        if cfg.B != 1 or cfg.S % (16 * chunks):
-            raise ValueError("one sequence whose length is a multiple of 16 * chunks")
-        self.attn, self.cfg, self.chunks = attn, cfg, chunks
-        self.rows = cfg.S // chunks
-        self.hq, self.hk, self.hv, self.ho, self.hl = host_q, host_k, host_v, host_o, host_lse
-        self.q = torch.empty(host_q.shape, dtype=host_q.dtype, device=dev)
-        self.k = torch.empty(host_k.shape, dtype=host_k.dtype, device=dev)
-        self.v = torch.empty(host_v.shape, dtype=host_v.dtype, device=dev)
-        self.o = torch.empty(host_o.shape, dtype=host_o.dtype, device=dev)
-        self.lse = torch.empty(host_lse.shape, dtype=host_lse.dtype, device=dev)
-        pages = cfg.S // 16
-        self.kc = self.k.view(pages, 16, cfg.Hkv, cfg.d)   # the sequence's keys as a paged cache
-        self.vc = self.v.view(pages, 16, cfg.Hkv, cfg.d)
-        self.bt = torch.arange(pages, dtype=torch.int32, device=dev)[None]
-        self.cu = torch.tensor([0, self.rows], dtype=torch.int32, device=dev)
-        self.lens = torch.tensor([(c + 1) * self.rows for c in range(chunks)], dtype=torch.int32, device=dev)
-        self.s_in, self.s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        self.h2d_bytes = sum(t.numel() * t.element_size() for t in (host_q, host_k, host_v))
-        self.d2h_bytes = sum(t.numel() * t.element_size() for t in (host_o, host_lse))
-
-        self.graph = None
-
-    def capture(self):
-        """Record one pass as a CUDA graph (after one eager pass has set every kernel up)."""
-        self.graph = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream(self.q.device)
-        side.wait_stream(torch.cuda.current_stream(self.q.device))
-        with torch.cuda.graph(self.graph, stream=side):
-            self._enqueue(side)
-        torch.cuda.current_stream(self.q.device).wait_stream(side)
-
-    def __call__(self, stream):
-        if self.graph is None:
-            self._enqueue(stream)
-        else:
-            with torch.cuda.stream(stream):
-                self.graph.replay()
-
-    def _enqueue(self, stream):
-        cfg, r = self.cfg, self.rows
-        start = torch.cuda.Event()
-        start.record(stream)
-        self.s_in.wait_event(start)
-        self.s_out.wait_event(start)
-        for c in range(self.chunks):
-            rs = slice(c * r, (c + 1) * r)
-            with torch.cuda.stream(self.s_in):
-                self.q[:, rs].copy_(self.hq[:, rs], non_blocking=True)
-                self.k[:, rs].copy_(self.hk[:, rs], non_blocking=True)
-                self.v[:, rs].copy_(self.hv[:, rs], non_blocking=True)
-                arrived = torch.cuda.Event()
-                arrived.record(self.s_in)
-            stream.wait_event(arrived)
-            self.attn.prefill_paged(self.q[0, rs], self.kc, self.vc, self.bt, self.cu, self.lens[c:c + 1], r,
-                                    scale=cfg.scale, causal=True, out=self.o[0, rs], lse=self.lse[c], stream=stream)
-            done = torch.cuda.Event()
-            done.record(stream)
-            self.s_out.wait_event(done)
-            with torch.cuda.stream(self.s_out):
-                self.ho[:, rs].copy_(self.o[:, rs], non_blocking=True)
-                self.hl[c].copy_(self.lse[c], non_blocking=True)
-        finished = torch.cuda.Event()
-        finished.record(self.s_out)
-        stream.wait_event(finished)
-
-
-# ---------------------------------------------------------------------------- GPU arm
-
 def run_gpu(args):
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -389,8 +306,15 @@ def run_gpu(args):
         ho.copy_(o, non_blocking=True)
         hl.copy_(lse, non_blocking=True)
 
-    hl_chunks = torch.empty((E2E_CHUNKS, cfg.Hq, cfg.S // E2E_CHUNKS), dtype=torch.float32, pin_memory=True)
-    e2e_pipe = PipelinedPrefill(attn, cfg, dev, hq, hk, hv, ho, hl_chunks, chunks=E2E_CHUNKS)
+    # the library's host-buffer prefill: the transfers overlap the chunks' compute inside the call
+    hq1, hk1, hv1, ho1 = (t[0] for t in (hq, hk, hv, ho))   # one sequence, [S, H, d]
+    hl1 = hl[0]
+    ws_host = torch.empty(attn.prefill_host_workspace_bytes(cfg.S, cfg.Hq, cfg.Hkv, cfg.d, E2E_CHUNKS),
+                          dtype=torch.uint8, device=dev)
+
+    def e2e_host():
+        attn.prefill_host(hq1, hk1, hv1, scale=cfg.scale, causal=True, chunks=E2E_CHUNKS, out=ho1, lse=hl1,
+                          workspace=ws_host, stream=stream)
 
     def timed_e2e(step_fn):
         for _ in range(args.warmup):
@@ -407,10 +331,7 @@ def run_gpu(args):
         torch.cuda.synchronize()
         return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
-    e2e_pipe(stream)           # one eager pass sets every kernel up, then one pass becomes a graph
-    torch.cuda.synchronize()
-    e2e_pipe.capture()
-    e2e_ms = timed_e2e(lambda: e2e_pipe(stream))
+    e2e_ms = timed_e2e(e2e_host)
     e2e_serial_ms = timed_e2e(e2e_serial)
     if world > 1:
         t = torch.tensor([e2e_ms], device=dev)
@@ -475,12 +396,12 @@ def run_gpu(args):
         },
         "timing_spread": spread,
         "decode": {"value": round(gbs, 1), "unit": "GB/s", "ms": round(dec_mean, 4), "roofline": dec_roof},
-        "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": e2e_pipe.h2d_bytes,
-                "d2h_bytes_per_step": e2e_pipe.d2h_bytes, "ms": round(e2e_ms, 4),
-                "how": f"q/k/v copied from pinned host memory and o/lse copied back inside the timed region, "
-                       f"pipelined in {E2E_CHUNKS} query chunks (each a chunked prefill through "
-                       "attn_prefill_paged over the sequence's own keys) on three streams, replayed as one "
-                       "CUDA graph per step",
+        "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms": round(e2e_ms, 4),
+                "how": f"one attn_prefill_host call a step: q/k/v read from pinned host memory and o/lse "
+                       f"written back to it inside the call, pipelined in {E2E_CHUNKS} query chunks (each a "
+                       "chunked prefill over the sequence's own keys) with the copies on two library "
+                       "streams",
                 "serial": {"value": round(world * flops / (e2e_serial_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                            "ms": round(e2e_serial_ms, 4), "how": "copies in, one attn_prefill, copies out, "
                                                                  "in sequence on one stream",

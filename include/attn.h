@@ -23,14 +23,17 @@
  *
  * Conventions for every entry point:
  *   - Tensor pointers are DEVICE pointers (CUDA global memory of the current
- *     device), 16-byte aligned, densely packed in the layout stated.  bf16 is
+ *     device), 16-byte aligned, densely packed in the layout stated, except
+ *     the host pointers of attn_prefill_host.  bf16 is
  *     IEEE bfloat16 (2 bytes); LSE values are float32 natural logarithms of
  *     the sum of exp(scaled scores).
  *   - `stream` is a cudaStream_t passed as an opaque pointer (NULL = legacy
  *     default stream).  Kernels are enqueued on it and run asynchronously;
  *     outputs are valid once the stream reaches that point.
  *   - The caller owns all memory.  The library allocates nothing on the
- *     device and keeps no per-call state.  Argument errors are detected on the host before
+ *     device and keeps no per-call state (attn_prefill_host keeps two copy
+ *     streams per device; attn_decode_paged_noalloc uses a fixed array inside
+ *     the library).  Argument errors are detected on the host before
  *     anything is enqueued and leave the outputs untouched.
  *   - Grouped-query attention: Hq must be a multiple of Hkv; query head h uses
  *     KV head h / (Hq / Hkv).
@@ -139,6 +142,55 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_cache, const void*
                                  const int32_t* cu_seqlens_q, const int32_t* seq_lens, void* o, float* lse,
                                  int num_seqs, int max_seqlen_q, int total_q, int Hq, int Hkv, int d, int page_size,
                                  int max_blocks_per_seq, int num_blocks, float scale, int causal, void* stream);
+
+/*
+ * Causal (or full) prefill of one sequence whose inputs and outputs are in
+ * HOST memory, with the transfers inside the call.  The attention is that of
+ * attn_prefill with B = 1 ("Why your local LLM feels dumber than it is" (Part
+ * 3.14), section "What attention is trying to calculate"); the queries are
+ * cut into `chunks` runs of ceil(S / chunks) rows.  Row i only sees keys
+ * 0 .. i, so a chunk needs only the keys up to its own last row: each chunk
+ * runs as one chunked prefill (attn_prefill_paged, the keys and values seen
+ * as a paged cache with an identity block table) as soon as its rows are
+ * on the device, while the next chunk is copied in and the previous one
+ * copied out.  With causal == 0 every row sees all S keys: all of k and v
+ * are copied in before the first chunk, and only the queries and outputs
+ * are pipelined.
+ *   q_host        [S, Hq, d] bf16, host memory
+ *   k_host,
+ *   v_host        [S, Hkv, d] bf16, host memory
+ *   o_host        [S, Hq, d] bf16, host memory (output)
+ *   lse_host      [Hq, S] f32, host memory (output, may be NULL)
+ *   chunks        1 .. 64
+ *   workspace     DEVICE memory, 256-byte aligned, of at least
+ *                 attn_prefill_host_workspace_bytes(S, Hq, Hkv, d, chunks)
+ *                 bytes: the device copies of q, k, v, o and LSE, the
+ *                 block table and the chunks' offsets.  It must not be in use
+ *                 by other work until the call's work on `stream` is done.
+ * Host buffers should be page-locked (cudaHostAlloc or cudaHostRegister): the
+ * copies then run asynchronously and overlap.  Pageable memory gives the
+ * same results, but its copies stop the calling thread and do not overlap.
+ * The chunks' prefills run on `stream`; the copies run on two streams the
+ * library creates once per device (with four events) and keeps for the life
+ * of the process: the only state the library keeps between calls.  The copies
+ * start after the work enqueued on `stream` before the call, and work
+ * enqueued on `stream` after the call starts after the last copy out, so the
+ * host outputs are complete once `stream` reaches that point (for example
+ * after cudaStreamSynchronize(stream)).  Enqueueing is serialised across host
+ * threads.
+ * Errors: argument errors (d, Hq, Hkv, S, chunks, scale, NULL pointers, an
+ * unaligned or too small workspace) return before anything is enqueued; a
+ * CUDA error while enqueueing returns ATTN_ERR_CUDA with part of the work
+ * enqueued and the outputs undefined.
+ * Arithmetic as for attn_prefill; every output equals that of attn_prefill on
+ * the same sequence.
+ */
+attn_status_t attn_prefill_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                                float* lse_host, int S, int Hq, int Hkv, int d, float scale, int causal, int chunks,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes attn_prefill_host needs; 0 for invalid arguments. */
+size_t attn_prefill_host_workspace_bytes(int S, int Hq, int Hkv, int d, int chunks);
 
 /*
  * Number of partial slots per (sequence, query head) that attn_decode_paged

@@ -92,6 +92,38 @@ def test_prefill_paged_argument_checks(attn, over, want):
     assert attn.lib().attn_prefill_paged(*_paged_prefill_args(**over)) == want
 
 
+def _host_prefill_args(**over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, S=1000, Hq=8, Hkv=2, d=128, scale=0.1, causal=1, chunks=4,
+             ws=FAKE, wsb=1 << 30, stream=None)
+    a.update(over)
+    return tuple(a.values())
+
+
+@pytest.mark.parametrize("over,want", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(o=None), 1), (dict(ws=None), 1), (dict(ws=FAKE + 16), 1),
+    (dict(S=0), 1), (dict(Hkv=3), 1), (dict(Hq=0), 1), (dict(d=96), 2), (dict(chunks=0), 1), (dict(chunks=65), 1),
+    (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(wsb=1000), 3),
+])
+def test_prefill_host_argument_checks(attn, over, want):
+    """Every argument error returns before a CUDA call (so before the copy streams exist)."""
+    assert attn.lib().attn_prefill_host(*_host_prefill_args(**over)) == want
+
+
+def test_prefill_host_workspace_bytes(attn):
+    """q, k, v (padded to whole 16-token pages), o, LSE, the block table and the chunk offsets, each
+    region rounded up to 256 bytes."""
+    S, Hq, Hkv, d = 1000, 8, 2, 128
+    up = lambda x: (x + 255) // 256 * 256
+    pages = (S + 15) // 16
+    want = (2 * up(S * Hq * d * 2) + 2 * up(pages * 16 * Hkv * d * 2) + up(S * Hq * 4) + up(pages * 4)
+            + up(64 * 16))
+    assert attn.prefill_host_workspace_bytes(S, Hq, Hkv, d, 4) == want
+    assert attn.prefill_host_workspace_bytes(S, Hq, Hkv, d, 64) == want   # the offsets take a fixed 64 slots
+    assert attn.prefill_host_workspace_bytes(S, Hq, Hkv, d, 0) == 0
+    assert attn.prefill_host_workspace_bytes(S, Hq, 3, d, 4) == 0
+    assert attn.prefill_host_workspace_bytes(S, Hq, Hkv, 96, 4) == 0
+
+
 def test_combine_argument_checks(attn):
     lib = attn.lib()
     assert lib.attn_combine(None, FAKE, FAKE, 4, 2, 128, FAKE, None, None) == 1
