@@ -6,7 +6,6 @@ attn_prefill_paged or attn_prefill_host; every output row of every head is compa
 both kernels (CTA pairs at d = 128 with even head groups, single CTAs otherwise) and their ragged,
 packed, paged and chunked forms.
 """
-import math
 
 import numpy as np
 import pytest
