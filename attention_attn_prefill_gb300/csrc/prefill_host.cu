@@ -11,7 +11,9 @@
 // chunk c - 1 copied out, and the two copy directions run at once on the host link.
 //
 // The streams and events are created once per device and kept for the life of the process; a mutex
-// serialises the enqueueing of concurrent calls (the GPU work of two calls still overlaps).
+// serialises the enqueueing of concurrent calls.  A call's copies wait for the work already on the
+// caller's stream, so calls on one stream run one after the other; calls on different streams can
+// overlap on the GPU (the copy streams are shared, in the order the calls were made).
 #include <cuda_runtime.h>
 
 #include <cmath>
