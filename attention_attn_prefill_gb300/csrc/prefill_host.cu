@@ -22,6 +22,7 @@
 
 #include "attn.h"
 
+namespace attn {
 namespace {
 
 constexpr int kPage = 16;
@@ -111,6 +112,9 @@ cudaError_t copy_streams(CopyStreams** out) {
 }
 
 }  // namespace
+}  // namespace attn
+
+using namespace attn;  // the helpers above
 
 extern "C" {
 
