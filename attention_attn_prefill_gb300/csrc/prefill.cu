@@ -550,10 +550,9 @@ int prefill_rows_per_cta() { return BM; }
 int prefill_tile_rows() { return BM; }
 int prefill_kv_tile_rows(int d) { return d <= 128 ? Layout<128>::BN : Layout<256>::BN; }
 
-cudaError_t prefill_launch(int d, const PrefillMaps& maps, const PrefillParams& p, cudaStream_t stream) {
+cudaError_t prefill_launch(int d, const PrefillMaps& maps, const PrefillParams& p, bool blocked, cudaStream_t stream) {
   using Plain = WalkOf<pf::TileWalk>;
   using Blocked = WalkOf<pf::BlockedTileWalk>;
-  const bool blocked = p.seq_block < p.B;
   if (d == 64) return blocked ? launch<64, Blocked>(maps, p, stream) : launch<64, Plain>(maps, p, stream);
   if (d == 128) return blocked ? launch<128, Blocked>(maps, p, stream) : launch<128, Plain>(maps, p, stream);
   if (d == 256) return blocked ? launch<256, Blocked>(maps, p, stream) : launch<256, Plain>(maps, p, stream);

@@ -55,19 +55,33 @@ struct PrefillParams {
   int num_qblocks;   // query tiles of the longest sequence: ceil(S or max_seqlen / 128)
   FastDiv div_heads;  // by Hq
   FastDiv div_level;  // by B * Hq: work tiles per query-tile level
-  // Blocked walk (BlockedTileWalk): the sequences in blocks of seq_block (the last block may hold
-  // fewer), each block longest tile first, so that a block's keys and values stay in L2 while its
-  // query tiles run.
+  // Blocked walks (BlockedTileWalk and the CTA-pair kernel's blocked instances), taken when a batch's
+  // keys and values do not fit in L2; the host picks the instance.
+  //  * Packed sequences: blocks of seq_block sequences (the last block may hold fewer), each block
+  //    longest tile first; the divisors are by seq_block * heads (work tiles per query-tile level of
+  //    a full block), (B - (blocks - 1) * seq_block) * heads (the same for the last block) and
+  //    seq_block * heads * num_qblocks (work tiles of a full block).
+  //  * Equal-length batches: the work units (sequence, query head) -- (sequence, head pair) in the
+  //    CTA-pair kernel -- numbered b * heads + h, in blocks of seq_block consecutive units (whole KV
+  //    heads), and the query-tile levels in kBlockedBands bands of band = ceil(num_qblocks /
+  //    kBlockedBands) levels, longest first.  Band by band, block by block, each block's levels of
+  //    the band longest first: a block's keys and values stay in L2 over a band, and the walk ends
+  //    on the shortest tiles.  The divisors are by seq_block, seq_block * band and blocks *
+  //    seq_block * band (the tiles of one band); levels and units past the batch are skipped.
+  // (The two share fields: a larger parameter block measured about 1% slower on every cell.)
   int seq_block;
-  FastDiv div_block_level;       // by seq_block * Hq: work tiles per query-tile level of a full block
-  FastDiv div_block_level_last;  // by (B - (blocks - 1) * seq_block) * Hq: the same for the last block
-  FastDiv div_block;             // by seq_block * Hq * num_qblocks: work tiles of a full block
+  FastDiv div_block_level;
+  FastDiv div_block_level_last;
+  FastDiv div_block;
 };
+
+constexpr int kBlockedBands = 4;
 
 int prefill_rows_per_cta();
 int prefill_tile_rows();            // rows of a Q / O box
 int prefill_kv_tile_rows(int d);    // rows of a K / V box for head dim d
-cudaError_t prefill_launch(int d, const PrefillMaps& maps, const PrefillParams& p, cudaStream_t stream);
+// blocked: take the blocked walk's instance (PrefillParams::seq_block)
+cudaError_t prefill_launch(int d, const PrefillMaps& maps, const PrefillParams& p, bool blocked, cudaStream_t stream);
 cudaError_t prefill_status(uint32_t* out, bool clear);  // both prefill kernels' status words
 
 // CTA-pair kernel (prefill_cta2.cu): head dim 128, an even number of query heads per KV head, a batch
@@ -75,7 +89,7 @@ cudaError_t prefill_status(uint32_t* out, bool clear);  // both prefill kernels'
 // K tile); Q, V and O maps are as for the single-head kernel.
 bool prefill_cta2_supported(int d, int Hq, int Hkv, bool packed);
 int prefill_cta2_k_rows();
-cudaError_t prefill_cta2_launch(const PrefillMaps& maps, const PrefillParams& p, cudaStream_t stream);
+cudaError_t prefill_cta2_launch(const PrefillMaps& maps, const PrefillParams& p, bool blocked, cudaStream_t stream);
 cudaError_t prefill_cta2_status(uint32_t* out, bool clear);
 
 }  // namespace attn

@@ -109,6 +109,42 @@ struct PairWalk {
   }
 };
 
+// PairWalk's list in blocks of p.unit_block consecutive (sequence, head pair) units, whole KV heads,
+// band by band of query-tile levels (equal-length batches whose keys and values exceed half of L2;
+// see PrefillParams::seq_block).
+struct LaneBlockedPairWalk {
+  int v = 0;
+  __device__ __forceinline__ bool next(const PrefillParams& p, WorkTile& t, int rank) {
+    const int G = static_cast<int>(num_clusters_x()), c = static_cast<int>(cluster_id_x());
+    const int pairs = p.Hq >> 1;
+    const int units = p.B * pairs;
+    while (true) {
+      const int idx = v * G + ((v & 1) ? (G - 1 - c) : c);
+      ++v;
+      const int band = (p.num_qblocks + kBlockedBands - 1) / kBlockedBands;  // levels a band
+      const int per_bb = p.seq_block * band;
+      const int per_band = static_cast<int>(p.div_block_level.div(static_cast<uint32_t>(units + p.seq_block - 1))) * per_bb;
+      if (idx >= kBlockedBands * per_band) return false;
+      const int bnd = static_cast<int>(p.div_block.div(static_cast<uint32_t>(idx)));
+      const int r1 = idx - bnd * per_band;
+      const int blk = static_cast<int>(p.div_block_level_last.div(static_cast<uint32_t>(r1)));
+      const int r2 = r1 - blk * per_bb;
+      const int lb = static_cast<int>(p.div_block_level.div(static_cast<uint32_t>(r2)));
+      const int level = bnd * band + lb;
+      const int u = blk * p.seq_block + (r2 - lb * p.seq_block);
+      if (level >= p.num_qblocks || u >= units) continue;
+      t.qt = p.num_qblocks - 1 - level;
+      t.b = static_cast<int>(p.div_heads.div(static_cast<uint32_t>(u)));
+      t.hq = 2 * (u - t.b * pairs) + rank;
+      t.base = 0;
+      t.z = t.b;
+      t.len = t.kv_len = p.S;
+      t.q_off = 0;
+      return true;
+    }
+  }
+};
+
 // The same list for packed sequences (cu_seqlens, and with paged K/V kv_lens): units past a sequence's
 // end are skipped, alike in both CTAs of a pair, and a sequence with bad bounds is recorded and skipped.
 // BLOCKED (chunked prefill over a paged cache larger than half of L2): the list is cut into blocks of
@@ -161,7 +197,7 @@ struct PackedPairWalk {
 
 // PACKED: packed sequences (PackedPairWalk), with contiguous or paged K/V; tm_vrow (one-row V boxes,
 // paged K/V only) fetches the last, partial page of a sequence row by row.  BLOCKED: the packed walk in
-// blocks of sequences.
+// blocks of sequences; without PACKED, the equal-length walk in blocks of units (LaneBlockedPairWalk).
 template <bool PACKED, bool BLOCKED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -201,7 +237,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const int G = p.Hq / p.Hkv;
   auto wait = [&](uint64_t* bar, uint32_t parity) { return __all_sync(0xffffffffu, mbar_wait(bar, parity)); };
   auto tile_nkv = [&](const WorkTile& t) { return pf::tile_nkv<BN>(p, t); };
-  struct Walk : std::conditional_t<PACKED, PackedPairWalk<BLOCKED>, PairWalk> {};
+  struct Walk
+      : std::conditional_t<PACKED, PackedPairWalk<BLOCKED>, std::conditional_t<BLOCKED, LaneBlockedPairWalk, PairWalk>> {
+  };
 
   if (warp == PRODUCER_WARP && lane == 0) {
     for (int s = 0; s < Q_STAGES; ++s) {
@@ -520,10 +558,10 @@ bool prefill_cta2_supported(int d, int Hq, int Hkv, bool packed) {
   return d == D && Hkv > 0 && Hq % Hkv == 0 && (Hq / Hkv) % 2 == 0;
 }
 
-cudaError_t prefill_cta2_launch(const PrefillMaps& m, const PrefillParams& p_in, cudaStream_t stream) {
+cudaError_t prefill_cta2_launch(const PrefillMaps& m, const PrefillParams& p_in, bool blocked, cudaStream_t stream) {
   const bool packed = p_in.cu_seqlens != nullptr;
-  auto kern = !packed ? prefill_cta2_kernel<false, false>
-              : p_in.seq_block < p_in.B ? prefill_cta2_kernel<true, true> : prefill_cta2_kernel<true, false>;
+  auto kern = !packed ? (blocked ? prefill_cta2_kernel<false, true> : prefill_cta2_kernel<false, false>)
+                      : (blocked ? prefill_cta2_kernel<true, true> : prefill_cta2_kernel<true, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   if (g_num_sms == 0) {
@@ -534,9 +572,10 @@ cudaError_t prefill_cta2_launch(const PrefillMaps& m, const PrefillParams& p_in,
   PrefillParams p = p_in;
   p.div_heads = FastDiv::make(static_cast<uint32_t>(p.Hq / 2));
   p.div_level = FastDiv::make(static_cast<uint32_t>(p.B * (p.Hq / 2)));
-  // the blocked walk's divisors, counted in head pairs
-  p.div_block_level = FastDiv::make(static_cast<uint32_t>(p.seq_block * (p.Hq / 2)));
-  p.div_block = FastDiv::make(static_cast<uint32_t>(p.seq_block * (p.Hq / 2) * p.num_qblocks));
+  if (packed) {  // the packed blocked walk's divisors, counted in head pairs (the host counted heads)
+    p.div_block_level = FastDiv::make(static_cast<uint32_t>(p.seq_block * (p.Hq / 2)));
+    p.div_block = FastDiv::make(static_cast<uint32_t>(p.seq_block * (p.Hq / 2) * p.num_qblocks));
+  }
   const long long units = static_cast<long long>(p.num_qblocks) * p.B * (p.Hq / 2);
   const int clusters = static_cast<int>(units < g_num_sms / 2 ? units : g_num_sms / 2);
   kern<<<2 * clusters, NUM_THREADS, SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.o, m.v_row, p);

@@ -1,0 +1,59 @@
+"""Equal-length batches at d = 128 whose keys and values exceed three quarters of L2: the blocked walk.
+
+Such batches are walked in blocks of whole KV heads, (sequence, KV head) lanes whose keys and values
+take at most an eighth of L2, band by band of query-tile levels.  The order of the walk cannot change a
+tile's arithmetic, so the output must equal, bit for bit, the same batch computed as slices of a few
+KV heads each (small enough for the plain walk); sampled rows of a few heads are also checked
+against the float64 oracle.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.attention as oa
+from parity import check_lse, check_o, to_np
+from workloads import make_prefill_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def sliced(attn, q, k, v, scale, kv_per_slice):
+    """The prefill of every slice of kv_per_slice KV heads (and their query heads) on its own."""
+    B, S, Hq, d = q.shape
+    Hkv = k.shape[2]
+    G = Hq // Hkv
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    for g0 in range(0, Hkv, kv_per_slice):
+        g1 = min(Hkv, g0 + kv_per_slice)
+        qs = q[:, :, g0 * G:g1 * G].contiguous()
+        os_, ls = attn.prefill(qs, k[:, :, g0:g1].contiguous(), v[:, :, g0:g1].contiguous(), scale=scale,
+                               causal=True)
+        o[:, :, g0 * G:g1 * G] = os_
+        lse[:, g0 * G:g1 * G] = ls
+    return o, lse
+
+
+@pytest.mark.parametrize("shape", [(4, 32, 32, 4096, 128, 4), (6, 32, 8, 8192, 128, 1), (3, 24, 24, 4096, 128, 3),
+                                   (2, 16, 16, 8192, 256, 2)],
+                         ids=["mha-single-CTA", "gqa-CTA-pairs", "mha-partial-last-block", "mha-d256-plain"])
+def test_blocked_walk_equals_slices_and_oracle(attn, gpu, shape):
+    B, Hq, Hkv, S, d, kv_per_slice = shape
+    assert S * d * 4 * B * Hkv > 130 * 2 ** 20         # more than L2: the blocked walk at d = 128
+    assert S * d * 4 * B * kv_per_slice < 40 * 2 ** 20  # a slice: the plain walk
+    x = make_prefill_inputs(B, Hq, Hkv, S, d, seed=8800 + d + Hkv)
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = (t.to(gpu) for t in (x.q, x.k, x.v))
+    o, lse = attn.prefill(q, k, v, scale=scale, causal=True)
+    os_, ls = sliced(attn, q, k, v, scale, kv_per_slice)
+    torch.cuda.synchronize()
+    assert torch.equal(o, os_) and torch.equal(lse, ls)
+    heads = [0, Hq // 2 + 1, Hq - 1]
+    rows = np.array([0, 1, 127, 128, S // 2 - 1, S // 2, S - 129, S - 1])
+    r_t, h_t = torch.tensor(rows, device=gpu), torch.tensor(heads, device=gpu)
+    for b in sorted({0, B - 1}):
+        wo, wl = oa.prefill(x.q, x.k, x.v, scale, causal=True, heads=heads, rows=rows, batches=[b])
+        check_o(to_np(o[b][r_t][:, h_t]), wo[b][rows][:, heads], f"blocked walk b={b}")
+        check_lse(to_np(lse[b][h_t][:, r_t]), wl[b][heads][:, rows], f"blocked walk b={b}")
