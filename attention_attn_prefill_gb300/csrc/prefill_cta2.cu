@@ -121,18 +121,10 @@ struct LaneBlockedPairWalk {
     while (true) {
       const int idx = v * G + ((v & 1) ? (G - 1 - c) : c);
       ++v;
-      const int band = (p.num_qblocks + kBlockedBands - 1) / kBlockedBands;  // levels a band
-      const int per_bb = p.seq_block * band;
-      const int per_band = static_cast<int>(p.div_block_level.div(static_cast<uint32_t>(units + p.seq_block - 1))) * per_bb;
-      if (idx >= kBlockedBands * per_band) return false;
-      const int bnd = static_cast<int>(p.div_block.div(static_cast<uint32_t>(idx)));
-      const int r1 = idx - bnd * per_band;
-      const int blk = static_cast<int>(p.div_block_level_last.div(static_cast<uint32_t>(r1)));
-      const int r2 = r1 - blk * per_bb;
-      const int lb = static_cast<int>(p.div_block_level.div(static_cast<uint32_t>(r2)));
-      const int level = bnd * band + lb;
-      const int u = blk * p.seq_block + (r2 - lb * p.seq_block);
-      if (level >= p.num_qblocks || u >= units) continue;
+      int level, u;
+      const int k = pf::lane_band_unit(p, idx, units, level, u);
+      if (k == 0) return false;
+      if (k == 1) continue;
       t.qt = p.num_qblocks - 1 - level;
       t.b = static_cast<int>(p.div_heads.div(static_cast<uint32_t>(u)));
       t.hq = 2 * (u - t.b * pairs) + rank;
@@ -147,17 +139,45 @@ struct LaneBlockedPairWalk {
 
 // The same list for packed sequences (cu_seqlens, and with paged K/V kv_lens): units past a sequence's
 // end are skipped, alike in both CTAs of a pair, and a sequence with bad bounds is recorded and skipped.
-// BLOCKED (chunked prefill over a paged cache larger than half of L2): the list is cut into blocks of
+// BLOCKED, chunked prefill over a paged cache larger than half of L2: the list is cut into blocks of
 // p.seq_block sequences, each block walked longest unit first before the next, so that a block's
 // cached keys and values stay in L2 while all its query tiles stream them.  Every block counts
-// p.seq_block sequences; the last one's units past the batch are skipped.  It is a separate
-// instance: where the batch fits L2 the extra index arithmetic measured 2-3% slower.
+// p.seq_block sequences; the last one's units past the batch are skipped.  BLOCKED, packed prompts
+// (no kv_lens) larger than three quarters of L2: the banded lane-blocked order of
+// LaneBlockedPairWalk.  It is a separate instance: where the batch fits L2 the extra index
+// arithmetic measured 2-3% slower.
 template <bool BLOCKED>
 struct PackedPairWalk {
   int v = 0;
   __device__ __forceinline__ bool next(const PrefillParams& p, WorkTile& t, int rank) {
     const int G = static_cast<int>(num_clusters_x()), c = static_cast<int>(cluster_id_x());
     const int pairs = p.Hq >> 1;
+    if constexpr (BLOCKED) {
+      if (p.kv_lens == nullptr) {  // packed prompts: lanes and bands
+        const int units = p.B * pairs;
+        while (true) {
+          const int idx = v * G + ((v & 1) ? (G - 1 - c) : c);
+          ++v;
+          int level, u;
+          const int k = pf::lane_band_unit(p, idx, units, level, u);
+          if (k == 0) return false;
+          if (k == 1) continue;
+          t.qt = p.num_qblocks - 1 - level;
+          t.b = static_cast<int>(p.div_heads.div(static_cast<uint32_t>(u)));
+          t.hq = 2 * (u - t.b * pairs) + rank;
+          const int s0 = p.cu_seqlens[t.b], s1 = p.cu_seqlens[t.b + 1];
+          if (s0 < 0 || s1 < s0 || s1 > p.S || s1 - s0 > p.num_qblocks * BM) {
+            if (rank == 0) set_error(&g_prefill_cta2_status, kDevBadSeqlens);
+            continue;  // the sequence is skipped
+          }
+          t.base = s0;
+          t.z = 0;
+          t.len = t.kv_len = s1 - s0;
+          t.q_off = 0;
+          if (t.qt * BM < t.len) return true;
+        }
+      }
+    }
     const int seqs = BLOCKED ? (p.B + p.seq_block - 1) / p.seq_block * p.seq_block : p.B;
     const int total = seqs * pairs * p.num_qblocks;
     while (true) {
@@ -572,7 +592,7 @@ cudaError_t prefill_cta2_launch(const PrefillMaps& m, const PrefillParams& p_in,
   PrefillParams p = p_in;
   p.div_heads = FastDiv::make(static_cast<uint32_t>(p.Hq / 2));
   p.div_level = FastDiv::make(static_cast<uint32_t>(p.B * (p.Hq / 2)));
-  if (packed) {  // the packed blocked walk's divisors, counted in head pairs (the host counted heads)
+  if (packed && p.kv_lens != nullptr) {  // the paged blocked walk's divisors, in head pairs (the host counted heads)
     p.div_block_level = FastDiv::make(static_cast<uint32_t>(p.seq_block * (p.Hq / 2)));
     p.div_block = FastDiv::make(static_cast<uint32_t>(p.seq_block * (p.Hq / 2) * p.num_qblocks));
   }

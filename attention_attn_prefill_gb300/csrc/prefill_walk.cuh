@@ -82,40 +82,63 @@ struct TileWalk {
   }
 };
 
+// Work index idx of the banded, lane-blocked order over `units` (sequence, head) units (see
+// PrefillParams::seq_block): its query-tile level and unit.  Returns 0 past the list, 1 for a slot
+// to skip (a level past the last band's or a unit past the last block's), 2 otherwise.
+__device__ __forceinline__ int lane_band_unit(const PrefillParams& p, int idx, int units, int& level, int& u) {
+  const int band = (p.num_qblocks + kBlockedBands - 1) / kBlockedBands;  // levels a band
+  const int per_bb = p.seq_block * band;
+  const int per_band = static_cast<int>(p.div_block_level.div(static_cast<uint32_t>(units + p.seq_block - 1))) * per_bb;
+  if (idx >= kBlockedBands * per_band) return 0;
+  const int bnd = static_cast<int>(p.div_block.div(static_cast<uint32_t>(idx)));
+  const int r1 = idx - bnd * per_band;
+  const int blk = static_cast<int>(p.div_block_level_last.div(static_cast<uint32_t>(r1)));
+  const int r2 = r1 - blk * per_bb;
+  const int lb = static_cast<int>(p.div_block_level.div(static_cast<uint32_t>(r2)));
+  level = bnd * band + lb;
+  u = blk * p.seq_block + (r2 - lb * p.seq_block);
+  return (level >= p.num_qblocks || u >= units) ? 1 : 2;
+}
+
 // The same list in blocks whose keys and values fit in part of L2, each block walked longest tile
 // first; used when all of a batch's keys and values do not fit in L2, so that the query tiles of one
-// level do not evict what the next level reads again.  Packed sequences go in blocks of p.seq_block
-// sequences; equal-length batches in blocks of p.unit_block (sequence, query head) units, whole KV
-// heads, band by band of query-tile levels (see PrefillParams::seq_block).
+// level do not evict what the next level reads again.  Chunked prefill over a paged cache goes in
+// blocks of p.seq_block sequences; equal-length batches and packed prompts in blocks of p.seq_block
+// (sequence, query head) units, whole KV heads, band by band of query-tile levels (see
+// PrefillParams::seq_block).
 struct BlockedTileWalk {
   int v = 0;
   __device__ __forceinline__ bool next(const PrefillParams& p, WorkTile& t, uint32_t* status) {
     const int G = gridDim.x, c = blockIdx.x;
-    if (p.cu_seqlens == nullptr) {
+    if (p.kv_lens == nullptr) {  // equal-length batches and packed prompts: lanes and bands
       const int units = p.B * p.Hq;
       while (true) {
         const int idx = v * G + ((v & 1) ? (G - 1 - c) : c);
         ++v;
-        const int band = (p.num_qblocks + kBlockedBands - 1) / kBlockedBands;  // levels a band
-        const int per_bb = p.seq_block * band;
-        const int per_band = static_cast<int>(p.div_block_level.div(static_cast<uint32_t>(units + p.seq_block - 1))) * per_bb;
-        if (idx >= kBlockedBands * per_band) return false;
-        const int bnd = static_cast<int>(p.div_block.div(static_cast<uint32_t>(idx)));
-        const int r1 = idx - bnd * per_band;
-        const int blk = static_cast<int>(p.div_block_level_last.div(static_cast<uint32_t>(r1)));
-        const int r2 = r1 - blk * per_bb;
-        const int lb = static_cast<int>(p.div_block_level.div(static_cast<uint32_t>(r2)));
-        const int level = bnd * band + lb;
-        const int u = blk * p.seq_block + (r2 - lb * p.seq_block);
-        if (level >= p.num_qblocks || u >= units) continue;
+        int level, u;
+        const int k = lane_band_unit(p, idx, units, level, u);
+        if (k == 0) return false;
+        if (k == 1) continue;
         t.qt = p.num_qblocks - 1 - level;
         t.b = static_cast<int>(p.div_heads.div(static_cast<uint32_t>(u)));
         t.hq = u - t.b * p.Hq;
-        t.base = 0;
-        t.z = t.b;
-        t.len = t.kv_len = p.S;
+        if (p.cu_seqlens == nullptr) {
+          t.base = 0;
+          t.z = t.b;
+          t.len = t.kv_len = p.S;
+          t.q_off = 0;
+          return true;
+        }
+        const int s0 = p.cu_seqlens[t.b], s1 = p.cu_seqlens[t.b + 1];
+        if (s0 < 0 || s1 < s0 || s1 > p.S || s1 - s0 > p.num_qblocks * BM) {
+          set_error(status, kDevBadSeqlens);
+          continue;  // the sequence is skipped
+        }
+        t.base = s0;
+        t.z = 0;
+        t.len = t.kv_len = s1 - s0;
         t.q_off = 0;
-        return true;
+        if (t.qt * BM < t.len) return true;
       }
     }
     const int total = p.B * p.Hq * p.num_qblocks;
