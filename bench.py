@@ -523,6 +523,17 @@ def workload_table(attn, dev, stream, flush, peaks, paged_inputs, reps: int = 50
             "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1), "us": round(ms * 1e3, 1), **spread,
             "frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
         del cargs, co, cl
+    # a batch whose keys and values (268 MB) exceed L2: MHA, 4 x 32 heads, S = 4096 (blocked walk)
+    xm = make_prefill_inputs(4, 32, 32, 4096, 128, seed=13)
+    mq, mk, mv = (t.to(dev) for t in (xm.q, xm.k, xm.v))
+    mo = torch.empty_like(mq)
+    ml = torch.empty((4, 32, 4096), dtype=torch.float32, device=dev)
+    ms = timed(lambda: attn.prefill(mq, mk, mv, scale=d ** -0.5, causal=True, out=mo, lse=ml, stream=stream))
+    flops = 4.0 * 4 * 32 * d * 4096 * 4097 / 2
+    out["MHA prefill, 4 x 32 heads, S = 4096 (K+V 268 MB, larger than L2)"] = {
+        "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1), "us": round(ms * 1e3, 1), **spread,
+        "frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
+    del mq, mk, mv, mo, ml
     out["_note"] = (f"each: {reps} launches with L2 flushed before each, outside the timed region; value and frac "
                     "from the mean launch time (us), with the median and the fastest launch beside it; frac against "
                     "the measured bf16 dense peak (prefill) or HBM copy (decode); prefill flops count the causal "
