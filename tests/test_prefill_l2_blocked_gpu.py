@@ -1,5 +1,5 @@
 """Equal-length batches whose keys and values exceed three quarters of L2 (d = 128) or one and a half
-times L2 (d = 64): the blocked walk.
+times L2 (d = 64 and 256): the blocked walk.
 
 Such batches are walked in blocks of whole KV heads, (sequence, KV head) lanes whose keys and values
 take at most an eighth of L2, band by band of query-tile levels.  The order of the walk cannot change a
@@ -39,7 +39,7 @@ def sliced(attn, q, k, v, scale, kv_per_slice):
 
 @pytest.mark.parametrize("shape", [(4, 32, 32, 4096, 128, 4), (6, 32, 8, 8192, 128, 1), (3, 24, 24, 4096, 128, 3),
                                    (4, 32, 32, 8192, 64, 4), (2, 16, 16, 8192, 256, 2)],
-                         ids=["mha-single-CTA", "gqa-CTA-pairs", "mha-partial-last-block", "mha-d64", "mha-d256-plain"])
+                         ids=["mha-single-CTA", "gqa-CTA-pairs", "mha-partial-last-block", "mha-d64", "mha-d256"])
 def test_blocked_walk_equals_slices_and_oracle(attn, gpu, shape):
     B, Hq, Hkv, S, d, kv_per_slice = shape
     assert S * d * 4 * B * Hkv > 130 * 2 ** 20         # more than L2: the blocked walk at d = 128
