@@ -170,13 +170,14 @@ attn_status_t prefill_common(const void* q, const void* k, const void* v, void* 
   p.div_block_level = attn::FastDiv::make(static_cast<uint32_t>(p.seq_block * p.Hq));
   p.div_block_level_last = attn::FastDiv::make(static_cast<uint32_t>((p.B - (blocks - 1) * p.seq_block) * p.Hq));
   p.div_block = attn::FastDiv::make(static_cast<uint32_t>(p.seq_block * p.Hq * p.num_qblocks));
-  // Equal-length batches and packed prompts whose keys and values exceed three quarters of L2 (d = 128)
-  // or one and a half times L2 (d = 64 and 256) the same way: blocks of whole KV heads, (sequence, KV head) "lanes" (sized for the longest
-  // sequence) whose keys and values take at most an eighth of L2, in bands of query-tile levels, so
-  // that a lane's keys and values are read from HBM once a band rather than once a level.  Measured: 4 x 32 heads (MHA) at S = 4096 -29%, 32 query /
-  // 8 KV heads at 4 x 8192 or 8 x 4096 (134 MB) -3 to -6%; at half of L2 (sweep S = 4096) no gain,
-  // so it keeps the plain walk.  At d = 64: MHA 4 x 32 heads at S = 8192 (268 MB) -10%, but 32 query /
-  // 8 KV heads at 8 x 8192 (134 MB) +1%; at d = 256: MHA 2 x 16 heads at S = 8192 (268 MB) -5%, but
+  // Equal-length batches and packed prompts whose keys and values exceed three quarters of L2 at
+  // d = 128, or one and a half times L2 at d = 64 and 256, go the same way in blocks of whole KV
+  // heads: (sequence, KV head) "lanes" (sized for the longest sequence) whose keys and values take at
+  // most an eighth of L2, with the query-tile levels in bands, so that a lane's keys and values are
+  // read from HBM once a band rather than once a level.  Measured at d = 128: MHA 4 x 32 heads at
+  // S = 4096 -29%; 32 query / 8 KV heads at 4 x 8192 or 8 x 4096 (134 MB) -3 to -6%; at half of L2
+  // (sweep S = 4096) no gain.  At d = 64: MHA 4 x 32 heads at S = 8192 (268 MB) -10%, but 32 query /
+  // 8 KV heads at 8 x 8192 (134 MB) +1%.  At d = 256: MHA 2 x 16 heads at S = 8192 (268 MB) -5%, but
   // 1 x 16 heads (134 MB) +4%.
   bool blocked = p.seq_block < p.B;
   if (paged == nullptr) {
