@@ -4,7 +4,7 @@ Each seed draws a batch shape (lengths around tile and page edges and long ones,
 KV head, head dim 64 / 128 / 256, causal or not) and runs it through attn_prefill, attn_prefill_varlen,
 attn_prefill_paged or attn_prefill_host; every output row of every head is compared.  The shapes reach
 both kernels (CTA pairs at d = 128 with even head groups, single CTAs otherwise) and their ragged,
-packed, paged and chunked forms.
+packed, paged and chunked forms, and batches large enough for the blocked walk.
 """
 
 import numpy as np
@@ -104,3 +104,36 @@ def test_random_host_buffer_prefill(attn, gpu, seed):
     what = f"seed {seed}: S={S} chunks={chunks} Hq={Hq} Hkv={Hkv} d={d} causal={causal}"
     check_o(to_np(o)[None], wo, what)
     check_lse(to_np(lse)[None], wl, what)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_batches_larger_than_l2(attn, gpu, seed):
+    """Equal-length batches grown until their keys and values pass the blocked walk's threshold for the
+    head dim (three quarters of L2 at d = 128, one and a half times at d = 64 and 256): bit for bit the
+    same batch computed one KV head at a time, and sampled rows against the oracle."""
+    rng, _, _, d, causal = draw(seed + 400)
+    Hq, Hkv = [(8, 8), (32, 8), (32, 32), (12, 4), (24, 8), (16, 2)][int(rng.integers(0, 6))]
+    S = int(rng.choice([2048, 4096, 8192]))
+    l2 = torch.cuda.get_device_properties(gpu).L2_cache_size
+    need = (0.8 if d == 128 else 1.6) * l2
+    B = 1
+    while S * d * 4 * B * Hkv < need:
+        B += 1
+    x = make_prefill_inputs(B, Hq, Hkv, S, d, seed=7500 + seed)
+    scale = float(d) ** -0.5
+    q, k, v = (t.to(gpu) for t in (x.q, x.k, x.v))
+    o, lse = attn.prefill(q, k, v, scale=scale, causal=causal)
+    G = Hq // Hkv
+    for g in range(Hkv):
+        og, lg = attn.prefill(q[:, :, g * G:(g + 1) * G].contiguous(), k[:, :, g:g + 1].contiguous(),
+                              v[:, :, g:g + 1].contiguous(), scale=scale, causal=causal)
+        assert torch.equal(o[:, :, g * G:(g + 1) * G], og) and torch.equal(lse[:, g * G:(g + 1) * G], lg), g
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, S // 3, S // 2, S - 1])
+    heads = sorted({0, Hq // 2, Hq - 1})
+    b = int(rng.integers(0, B))
+    wo, wl = oa.prefill(x.q, x.k, x.v, scale, causal=causal, heads=heads, rows=rows, batches=[b])
+    r_t, h_t = torch.tensor(rows, device=gpu), torch.tensor(heads, device=gpu)
+    what = f"seed {seed}: B={B} S={S} Hq={Hq} Hkv={Hkv} d={d} causal={causal}"
+    check_o(to_np(o[b][r_t][:, h_t]), wo[b][rows][:, heads], what)
+    check_lse(to_np(lse[b][h_t][:, r_t]), wl[b][heads][:, rows], what)
