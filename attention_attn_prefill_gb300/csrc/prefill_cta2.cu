@@ -109,9 +109,9 @@ struct PairWalk {
   }
 };
 
-// PairWalk's list in blocks of p.unit_block consecutive (sequence, head pair) units, whole KV heads,
-// band by band of query-tile levels (equal-length batches whose keys and values exceed half of L2;
-// see PrefillParams::seq_block).
+// PairWalk's list in blocks of p.seq_block consecutive (sequence, head pair) units, whole KV heads,
+// band by band of query-tile levels (equal-length batches whose keys and values exceed three
+// quarters of L2; see PrefillParams::seq_block).
 struct LaneBlockedPairWalk {
   int v = 0;
   __device__ __forceinline__ bool next(const PrefillParams& p, WorkTile& t, int rank) {
