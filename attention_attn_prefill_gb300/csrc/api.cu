@@ -157,8 +157,9 @@ attn_status_t prefill_common(const void* q, const void* k, const void* v, void* 
   // (For prompts prefilled from scratch the plain longest-first walk measured faster: there the
   // blocks' tails are unbalanced.)
   p.seq_block = p.B;
-  int l2_bytes = 0, dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+  int l2_bytes = 0, sms = 0, dev = 0;  // of the current device, at every call
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 2)
     return ATTN_ERR_CUDA;
   if (paged != nullptr) {
     const int64_t kv_max = std::max<int64_t>(max_seqlen, static_cast<int64_t>(paged->max_blocks) * kPage);
@@ -200,8 +201,8 @@ attn_status_t prefill_common(const void* q, const void* k, const void* v, void* 
       }
     }
   }
-  if (cta2) return from_cuda(attn::prefill_cta2_launch(maps, p, blocked, static_cast<cudaStream_t>(stream)));
-  return from_cuda(attn::prefill_launch(d, maps, p, blocked, static_cast<cudaStream_t>(stream)));
+  if (cta2) return from_cuda(attn::prefill_cta2_launch(maps, p, blocked, sms, static_cast<cudaStream_t>(stream)));
+  return from_cuda(attn::prefill_launch(d, maps, p, blocked, sms, static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace

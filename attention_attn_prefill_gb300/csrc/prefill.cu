@@ -525,21 +525,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-int g_num_sms = 0;
-
+// one persistent CTA per SM of the current device (sms), or one per work tile if fewer
 template <int D, class Walk>
-cudaError_t launch(const PrefillMaps& m, const PrefillParams& p, cudaStream_t stream) {
+cudaError_t launch(const PrefillMaps& m, const PrefillParams& p, int sms, cudaStream_t stream) {
   auto kern = prefill_fwd_kernel<D, Walk>;
   const int smem = Layout<D>::ALLOC;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  if (g_num_sms == 0) {
-    int dev = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  }
   const long long tiles = static_cast<long long>(p.num_qblocks) * p.B * p.Hq;
-  const int grid = static_cast<int>(tiles < g_num_sms ? tiles : g_num_sms);
+  const int grid = static_cast<int>(tiles < sms ? tiles : sms);
   kern<<<grid, NUM_THREADS, smem, stream>>>(m.q, m.k, m.v, m.o, m.v_row, p);
   return cudaGetLastError();
 }
@@ -550,12 +544,13 @@ int prefill_rows_per_cta() { return BM; }
 int prefill_tile_rows() { return BM; }
 int prefill_kv_tile_rows(int d) { return d <= 128 ? Layout<128>::BN : Layout<256>::BN; }
 
-cudaError_t prefill_launch(int d, const PrefillMaps& maps, const PrefillParams& p, bool blocked, cudaStream_t stream) {
+cudaError_t prefill_launch(int d, const PrefillMaps& maps, const PrefillParams& p, bool blocked, int sms,
+                           cudaStream_t stream) {
   using Plain = WalkOf<pf::TileWalk>;
   using Blocked = WalkOf<pf::BlockedTileWalk>;
-  if (d == 64) return blocked ? launch<64, Blocked>(maps, p, stream) : launch<64, Plain>(maps, p, stream);
-  if (d == 128) return blocked ? launch<128, Blocked>(maps, p, stream) : launch<128, Plain>(maps, p, stream);
-  if (d == 256) return blocked ? launch<256, Blocked>(maps, p, stream) : launch<256, Plain>(maps, p, stream);
+  if (d == 64) return blocked ? launch<64, Blocked>(maps, p, sms, stream) : launch<64, Plain>(maps, p, sms, stream);
+  if (d == 128) return blocked ? launch<128, Blocked>(maps, p, sms, stream) : launch<128, Plain>(maps, p, sms, stream);
+  if (d == 256) return blocked ? launch<256, Blocked>(maps, p, sms, stream) : launch<256, Plain>(maps, p, sms, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -80,8 +80,9 @@ constexpr int kBlockedBands = 4;
 int prefill_rows_per_cta();
 int prefill_tile_rows();            // rows of a Q / O box
 int prefill_kv_tile_rows(int d);    // rows of a K / V box for head dim d
-// blocked: take the blocked walk's instance (PrefillParams::seq_block)
-cudaError_t prefill_launch(int d, const PrefillMaps& maps, const PrefillParams& p, bool blocked, cudaStream_t stream);
+// blocked: take the blocked walk's instance (PrefillParams::seq_block); sms: the current device's SMs
+cudaError_t prefill_launch(int d, const PrefillMaps& maps, const PrefillParams& p, bool blocked, int sms,
+                           cudaStream_t stream);
 cudaError_t prefill_status(uint32_t* out, bool clear);  // both prefill kernels' status words
 
 // CTA-pair kernel (prefill_cta2.cu): head dim 128, an even number of query heads per KV head, a batch
@@ -89,7 +90,8 @@ cudaError_t prefill_status(uint32_t* out, bool clear);  // both prefill kernels'
 // K tile); Q, V and O maps are as for the single-head kernel.
 bool prefill_cta2_supported(int d, int Hq, int Hkv, bool packed);
 int prefill_cta2_k_rows();
-cudaError_t prefill_cta2_launch(const PrefillMaps& maps, const PrefillParams& p, bool blocked, cudaStream_t stream);
+cudaError_t prefill_cta2_launch(const PrefillMaps& maps, const PrefillParams& p, bool blocked, int sms,
+                                cudaStream_t stream);
 cudaError_t prefill_cta2_status(uint32_t* out, bool clear);
 
 }  // namespace attn

@@ -569,8 +569,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-int g_num_sms = 0;
-
 }  // namespace
 
 bool prefill_cta2_supported(int d, int Hq, int Hkv, bool packed) {
@@ -578,17 +576,13 @@ bool prefill_cta2_supported(int d, int Hq, int Hkv, bool packed) {
   return d == D && Hkv > 0 && Hq % Hkv == 0 && (Hq / Hkv) % 2 == 0;
 }
 
-cudaError_t prefill_cta2_launch(const PrefillMaps& m, const PrefillParams& p_in, bool blocked, cudaStream_t stream) {
+cudaError_t prefill_cta2_launch(const PrefillMaps& m, const PrefillParams& p_in, bool blocked, int sms,
+                                cudaStream_t stream) {
   const bool packed = p_in.cu_seqlens != nullptr;
   auto kern = !packed ? (blocked ? prefill_cta2_kernel<false, true> : prefill_cta2_kernel<false, false>)
                       : (blocked ? prefill_cta2_kernel<true, true> : prefill_cta2_kernel<true, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  if (g_num_sms == 0) {
-    int dev = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  }
   PrefillParams p = p_in;
   p.div_heads = FastDiv::make(static_cast<uint32_t>(p.Hq / 2));
   p.div_level = FastDiv::make(static_cast<uint32_t>(p.B * (p.Hq / 2)));
@@ -597,7 +591,7 @@ cudaError_t prefill_cta2_launch(const PrefillMaps& m, const PrefillParams& p_in,
     p.div_block = FastDiv::make(static_cast<uint32_t>(p.seq_block * (p.Hq / 2) * p.num_qblocks));
   }
   const long long units = static_cast<long long>(p.num_qblocks) * p.B * (p.Hq / 2);
-  const int clusters = static_cast<int>(units < g_num_sms / 2 ? units : g_num_sms / 2);
+  const int clusters = static_cast<int>(units < sms / 2 ? units : sms / 2);  // one pair per two SMs
   kern<<<2 * clusters, NUM_THREADS, SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.o, m.v_row, p);
   return cudaGetLastError();
 }
